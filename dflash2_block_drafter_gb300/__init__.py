@@ -1,0 +1,218 @@
+"""Python binding of libdflash2 (the GB300 library for the DFlash2 drafter's block-local tail).
+
+Argument marshalling only: every step of the path runs in the library's CUDA kernels, called
+through its C ABI (include/dflash2.h) with ctypes. PyTorch provides device memory and the
+current stream. There is no CPU fallback: if the library is missing or no GPU is present the
+calls raise.
+
+The functions carry the C names. Tensors are torch tensors on the current CUDA device,
+contiguous, dtype torch.bfloat16 or torch.float32 (activations/weights), float32 for base /
+bias / scores, int32 for ids. Outputs are allocated here when not passed in.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "Dflash2Error", "library", "library_path", "dflash2_version", "dflash2_poll_error",
+    "dflash2_conv_prepare_workspace_bytes", "dflash2_conv_prepare", "dflash2_conv_finish",
+    "dflash2_head_topk_workspace_bytes", "dflash2_head_topk", "dflash2_score_edges",
+    "dflash2_select_path", "dflash2_selftest_bounded_wait", "DTYPE_CODES",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "libdflash2.so")
+_LIB = None
+
+BF16, F32 = 0, 1
+DTYPE_CODES = {torch.bfloat16: BF16, torch.float32: F32}
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "dflash2_version": (_i, []),
+    "dflash2_status_string": (ctypes.c_char_p, [_i]),
+    "dflash2_last_error_message": (ctypes.c_char_p, []),
+    "dflash2_poll_error": (_i, [_vp]),
+    "dflash2_conv_prepare_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "dflash2_conv_prepare": (_i, [_vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dflash2_conv_finish": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _f, _vp, _i, _vp]),
+    "dflash2_head_topk_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "dflash2_head_topk": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dflash2_score_edges": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp]),
+    "dflash2_select_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
+    "dflash2_selftest_bounded_wait": (_i, [_i, _vp]),
+}
+
+
+class Dflash2Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+def library() -> ctypes.CDLL:
+    """Load libdflash2.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError(f"{library_path} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                               f"g.build()'` (needs nvcc); there is no CPU fallback")
+        lib = ctypes.CDLL(library_path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _check(rc: int):
+    if rc != 0:
+        lib = library()
+        msg = lib.dflash2_last_error_message().decode(errors="replace")
+        name = lib.dflash2_status_string(rc).decode()
+        raise Dflash2Error(rc, f"{name}: {msg}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return _vp(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t, name, dtype=None, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    return _vp(t.data_ptr())
+
+
+def _code(t):
+    try:
+        return DTYPE_CODES[t.dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float32") from None
+
+
+def _workspace(nbytes, device, ws):
+    if ws is None:
+        ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    return ws
+
+
+def dflash2_version() -> int:
+    return library().dflash2_version()
+
+
+def dflash2_poll_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word (0 = no error)."""
+    return library().dflash2_poll_error(_stream(stream))
+
+
+def dflash2_conv_prepare_workspace_bytes(B, G, H, group_size, dtype) -> int:
+    return library().dflash2_conv_prepare_workspace_bytes(B, G, H, group_size, DTYPE_CODES[dtype])
+
+
+def dflash2_conv_prepare(x, norm_w, eps, w_kp, base, group_size, out=None, coef1=None, d_full=None, workspace=None,
+                         stream=None, taps=2):
+    """Pre-sublayer conv: returns (out [B,G,H], coef1 [B,G,2,groups]); see dflash2.h."""
+    B, G, H = x.shape
+    groups = H // group_size
+    dt = x.dtype
+    out = torch.empty_like(x) if out is None else out
+    coef1 = torch.empty((B, G, 2, groups), dtype=dt, device=x.device) if coef1 is None else coef1
+    nbytes = library().dflash2_conv_prepare_workspace_bytes(B, G, H, group_size, _code(x))
+    workspace = _workspace(nbytes, x.device, workspace)
+    _check(library().dflash2_conv_prepare(
+        _dev(x, "x", dt), _dev(norm_w, "norm_w", dt, True), eps, _dev(w_kp, "w_kp", dt), _dev(base, "base", torch.float32),
+        B, G, H, group_size, taps, _code(x), _dev(out, "out", dt), _dev(coef1, "coef1", dt),
+        _dev(d_full, "d_full", torch.float32, True), _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+    return out, coef1
+
+
+def dflash2_conv_finish(y, coef1, base, group_size, residual=None, out=None, next_norm_w=None, eps=1e-6,
+                        next_n=None, next_row0=0, stream=None, taps=2):
+    """Post-sublayer conv + residual add (+ optional next RMSNorm). Returns (out, next_n)."""
+    B, G, H = y.shape
+    dt = y.dtype
+    out = torch.empty_like(y) if out is None else out
+    if next_norm_w is not None and next_n is None:
+        next_n = torch.empty((B, G - next_row0, H), dtype=dt, device=y.device)
+    _check(library().dflash2_conv_finish(
+        _dev(y, "y", dt), _dev(coef1, "coef1", dt), _dev(base, "base", torch.float32), B, G, H, group_size, taps,
+        _code(y), _dev(residual, "residual", dt, True), _dev(out, "out", dt), _dev(next_norm_w, "next_norm_w", dt, True),
+        eps, _dev(next_n, "next_n", dt, True), next_row0, _stream(stream)))
+    return out, next_n
+
+
+def dflash2_head_topk_workspace_bytes(M, H, V, K, R) -> int:
+    return library().dflash2_head_topk_workspace_bytes(M, H, V, K, R)
+
+
+def dflash2_head_topk(h, w_head, K, bias=None, w_proj=None, cand=None, unary=None, z=None, logits=None,
+                      want_logits=False, workspace=None, stream=None):
+    """Head GEMM + fused top-K (+ z). h: [M, H]. Returns (cand [M,K] int32, unary [M,K] f32, z [M,R] or None, logits or None)."""
+    M, H = h.shape
+    V = w_head.shape[0]
+    R = w_proj.shape[0] if w_proj is not None else 0
+    dt = h.dtype
+    dev = h.device
+    cand = torch.empty((M, K), dtype=torch.int32, device=dev) if cand is None else cand
+    unary = torch.empty((M, K), dtype=torch.float32, device=dev) if unary is None else unary
+    if w_proj is not None and z is None:
+        z = torch.empty((M, R), dtype=torch.float32, device=dev)
+    if want_logits and logits is None:
+        logits = torch.empty((M, V), dtype=torch.float32, device=dev)
+    nbytes = library().dflash2_head_topk_workspace_bytes(M, H, V, K, R)
+    workspace = _workspace(nbytes, dev, workspace)
+    _check(library().dflash2_head_topk(
+        _dev(h, "h", dt), M, H, _dev(w_head, "w_head", dt), V, _dev(bias, "bias", torch.float32, True),
+        _dev(w_proj, "w_proj", dt, True), R, K, _code(h), _dev(cand, "cand", torch.int32),
+        _dev(unary, "unary", torch.float32), _dev(z, "z", torch.float32, True),
+        _dev(logits, "logits", torch.float32, True), _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+    return cand, unary, z, logits
+
+
+def dflash2_score_edges(cand, unary, z, anchors, pred_book, succ_book, want_S=True, want_path=True, S=None, path=None,
+                        stream=None):
+    """Edge scores (+ fused greedy walk). cand/unary: [B,steps,K]; z: [B,steps,R]. Returns (S, path)."""
+    B, steps, K = cand.shape
+    R = z.shape[-1]
+    V = pred_book.shape[0]
+    dev = cand.device
+    if want_S and S is None:
+        S = torch.empty((B, steps, K, K), dtype=torch.float32, device=dev)
+    if want_path and path is None:
+        path = torch.empty((B, steps), dtype=torch.int32, device=dev)
+    _check(library().dflash2_score_edges(
+        _dev(cand, "cand", torch.int32), _dev(unary, "unary", torch.float32), _dev(z, "z", torch.float32),
+        _dev(anchors, "anchors", torch.int32), _dev(pred_book, "pred_book", pred_book.dtype),
+        _dev(succ_book, "succ_book", pred_book.dtype), B, steps, K, R, V, _code(pred_book),
+        _dev(S, "S", torch.float32, True), _dev(path, "path", torch.int32, True), _stream(stream)))
+    return S, path
+
+
+def dflash2_select_path(S, cand, path=None, stream=None):
+    """Greedy walk over S [B,steps,K,K]; returns path [B,steps] int32."""
+    B, steps, K, _ = S.shape
+    path = torch.empty((B, steps), dtype=torch.int32, device=S.device) if path is None else path
+    _check(library().dflash2_select_path(_dev(S, "S", torch.float32), _dev(cand, "cand", torch.int32), B, steps, K,
+                                         _dev(path, "path", torch.int32), _stream(stream)))
+    return path
+
+
+def dflash2_selftest_bounded_wait(limit_us: int, stream=None):
+    _check(library().dflash2_selftest_bounded_wait(limit_us, _stream(stream)))

@@ -1,0 +1,599 @@
+// Tensor-core GEMM for sm_103a (tcgen05 + TMEM + TMA), with two epilogues:
+//   * STORE: fp32 split-K partial sums (kernel_projection of the grouped conv);
+//   * TOPK : per-row running top-16 of the logits (+bias), the extra columns written as z
+//            (hidden_projection folded in as 64-row chunks after the vocabulary), optional
+//            full logits. Full-vocabulary logits never reach memory unless asked for.
+//
+// C[m, n] = sum_k A[m, k] * W[n, k]: A = activations [M, K] (rows on the UMMA M axis, 128 per
+// tile), W = weights [N, K] (columns on the UMMA N axis, 64-row TMA chunks, up to 256 per
+// accumulator tile). Both operands are K-major, staged by TMA with 128-byte swizzle.
+//
+// Warp roles (one CTA per SM, persistent over its column range):
+//   warp 0      : TMA producer (one elected lane)
+//   warp 1      : TMEM allocator + MMA issuer (one elected lane)
+//   warps 2..   : epilogue, 4 warps per 128-row M tile; warp w reads TMEM lanes 32*(w%4)..+31.
+// Every wait is bounded (see mbar_wait_bounded); a timeout raises a CTA-wide abort flag, records
+// DFLASH2_ERR_TIMEOUT, drains in-flight copies and MMAs and frees TMEM before returning.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dfl {
+namespace {
+
+constexpr int kChunk = 64;                         // W rows per TMA box (one column chunk)
+constexpr int kMaxTileChunks = 4;                  // 256 accumulator columns per tile
+constexpr int kATile = 128 * 128;                  // bytes of one 128-row x 128-byte A tile
+constexpr int kBChunkBytes = kChunk * 128;         // 8 KB
+constexpr int kBTile = kMaxTileChunks * kBChunkBytes;  // 32 KB
+constexpr int kTopL = 16;                          // list length kept per row
+constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms
+
+template <int MT>
+struct Cfg {
+  static constexpr int kStages = (MT == 1) ? 4 : 3;
+  static constexpr int kStageBytes = MT * kATile + kBTile;
+  static constexpr int kEpiWarps = 4 * MT;
+  static constexpr int kEpiThreads = 32 * kEpiWarps;
+  static constexpr int kThreads = 64 + kEpiThreads;
+  static constexpr int kTmemCols = 256 * MT;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kListBytes = kEpiThreads * kTopL * 8;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kListBytes;
+};
+static_assert(Cfg<2>::kSmem <= 232448, "shared memory budget");
+static_assert(Cfg<1>::kSmem <= 232448, "shared memory budget");
+
+struct GemmArgs {
+  int M, K;
+  int n_main, n_extra;
+  int main_chunks, n_chunks;
+  int m_groups, n_splits, k_splits, k_blocks;
+  float* part;            // STORE: [k_splits][M][n_main]
+  const float* bias;      // TOPK: [n_main] or null
+  float* list_val;        // TOPK: [n_splits][M][16]
+  int* list_idx;
+  float* z;               // TOPK: [M][n_extra] or null
+  float* logits;          // TOPK: [M][n_main] or null
+  int* err;
+};
+
+// Next accumulator tile of the chunk range [c, c_end): up to 4 chunks, never straddling the
+// boundary between the main and the extra operand.
+__device__ __forceinline__ bool next_tile(int& c, int c_end, int main_chunks, int& t0, int& nch) {
+  if (c >= c_end) return false;
+  t0 = c;
+  int e = min(c + kMaxTileChunks, c_end);
+  if (t0 < main_chunks && e > main_chunks) e = main_chunks;
+  nch = e - t0;
+  c = e;
+  return true;
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* err) {
+  *abort_flag = 1;
+  if (err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_TIMEOUT));
+}
+
+// Insert (v, id) into a descending list held in shared memory (stride ne between entries);
+// equal values stay behind earlier (lower-id) entries.
+__device__ __forceinline__ void list_insert(float* lv, int* li, int et, int ne, float v, int id) {
+  int pos = kTopL - 1;
+  while (pos > 0) {
+    const float pv = lv[(pos - 1) * ne + et];
+    if (!(v > pv)) break;
+    lv[pos * ne + et] = pv;
+    li[pos * ne + et] = li[(pos - 1) * ne + et];
+    --pos;
+  }
+  lv[pos * ne + et] = v;
+  li[pos * ne + et] = id;
+}
+
+template <int MT, bool TF32, int MODE>
+__global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmE, const GemmArgs a) {
+  using C = Cfg<MT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* bar_area = smem + C::kStages * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(bar_area);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* acc_full = empty + C::kStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* lv = reinterpret_cast<float*>(bar_area + C::kBarBytes);
+  int* li = reinterpret_cast<int*>(lv + kTopL * C::kEpiThreads);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int bid = blockIdx.x;
+  const int mg = bid % a.m_groups;
+  bid /= a.m_groups;
+  const int ns = bid % a.n_splits;
+  const int ks = bid / a.n_splits;
+  const int c_begin = static_cast<int>((static_cast<long long>(a.n_chunks) * ns) / a.n_splits);
+  const int c_end = static_cast<int>((static_cast<long long>(a.n_chunks) * (ns + 1)) / a.n_splits);
+  const int kb0 = static_cast<int>((static_cast<long long>(a.k_blocks) * ks) / a.k_splits);
+  const int kb1 = static_cast<int>((static_cast<long long>(a.k_blocks) * (ks + 1)) / a.k_splits);
+  const int row0 = mg * 128 * MT;
+  const int mt_valid = min(MT, (a.M - row0 + 127) / 128);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(acc_full), 1);
+    mbar_init(smem_u32(acc_empty), C::kEpiWarps);
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (a.n_extra > 0) prefetch_tmap(&tmE);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (MODE == 1 && warp >= 2) {
+    const int et = threadIdx.x - 64;
+    for (int i = 0; i < kTopL; ++i) {
+      lv[i * C::kEpiThreads + et] = -INFINITY;
+      li[i * C::kEpiThreads + et] = -1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_keep = policy_evict_last();    // activations: re-read by every column tile
+      const uint64_t pol_stream = policy_evict_first(); // weights: streamed
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      int c = c_begin, t0 = 0, nch = 0;
+      while (ok && next_tile(c, c_end, a.main_chunks, t0, nch)) {
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(mt_valid * kATile + nch * kBChunkBytes));
+          uint8_t* sa = smem + stage * C::kStageBytes;
+          uint8_t* sb = sa + MT * kATile;
+          const int kx = kb * (TF32 ? 32 : 64);
+          for (int mt = 0; mt < mt_valid; ++mt)
+            tma_load_2d(smem_u32(sa + mt * kATile), &tmA, fb, kx, row0 + mt * 128, pol_keep);
+          for (int j = 0; j < nch; ++j) {
+            const int ch = t0 + j;
+            if (ch < a.main_chunks)
+              tma_load_2d(smem_u32(sb + j * kBChunkBytes), &tmB, fb, kx, ch * kChunk, pol_stream);
+            else
+              tma_load_2d(smem_u32(sb + j * kBChunkBytes), &tmE, fb, kx, (ch - a.main_chunks) * kChunk, pol_keep);
+          }
+          ++issued;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        raise_abort(abort_flag, a.err);
+        // Wait for the copies still in flight (the last min(issued, stages) fills).
+        int s = stage;
+        uint32_t ph = phase;
+        const int n = min(issued, C::kStages);
+        for (int i = 0; i < n; ++i) {
+          if (s == 0) {
+            s = C::kStages - 1;
+            ph ^= 1u;
+          } else {
+            --s;
+          }
+          mbar_wait_bounded(smem_u32(&full[s]), ph, nullptr, kDrainLimitNs);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true, any = false;
+      int c = c_begin, t0 = 0, nch = 0;
+      while (ok && next_tile(c, c_end, a.main_chunks, t0, nch)) {
+        if (!mbar_wait_bounded(smem_u32(acc_empty), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t idesc = make_idesc(TF32, 128, nch * kChunk);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
+          const uint64_t bdesc = desc_kmajor_sw128(sa + MT * kATile);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte swizzle row
+            for (int mt = 0; mt < mt_valid; ++mt) {
+              const uint64_t adesc = desc_kmajor_sw128(sa + mt * kATile) + static_cast<uint64_t>(2 * k);
+              const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+              if (TF32)
+                mma_tf32(tmem_base + static_cast<uint32_t>(mt * 256), adesc, bdesc + static_cast<uint64_t>(2 * k),
+                         idesc, acc);
+              else
+                mma_f16(tmem_base + static_cast<uint32_t>(mt * 256), adesc, bdesc + static_cast<uint64_t>(2 * k),
+                        idesc, acc);
+            }
+          }
+          mma_commit(smem_u32(&empty[stage]));  // frees the stage once these MMAs have read it
+          any = true;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(acc_full));  // accumulator complete
+        acc_phase ^= 1u;
+      }
+      if (!ok) {
+        raise_abort(abort_flag, a.err);
+        if (any) {
+          mma_commit(smem_u32(drain));
+          mbar_wait_bounded(smem_u32(drain), 0, nullptr, kDrainLimitNs);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int e = warp - 2;
+    const int q = warp & 3;
+    const int mt = e >> 2;
+    const int et = threadIdx.x - 64;
+    const int row = row0 + mt * 128 + q * 32 + lane;
+    const bool tile_ok = mt < mt_valid;
+    const bool valid = tile_ok && row < a.M;
+    uint32_t acc_phase = 0;
+    float thr = -INFINITY;
+    int c = c_begin, t0 = 0, nch = 0;
+    while (next_tile(c, c_end, a.main_chunks, t0, nch)) {
+      if (!mbar_wait_bounded(smem_u32(acc_full), acc_phase, abort_flag, kWaitLimitNs)) {
+        if (lane == 0) raise_abort(abort_flag, a.err);
+        break;
+      }
+      tc_fence_after();
+      if (tile_ok) {
+        const bool extra = t0 >= a.main_chunks;
+        for (int cc = 0; cc < nch * 2; ++cc) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(
+              tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mt * 256 + cc * 32), r);
+          tmem_ld_wait();
+          const int col0 = t0 * kChunk + cc * 32;
+          if (MODE == 0) {
+            if (valid) {
+              float* dst = a.part + (static_cast<size_t>(ks) * a.M + row) * a.n_main + col0;
+              if (col0 + 32 <= a.n_main && (a.n_main & 3) == 0) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                  *reinterpret_cast<float4*>(dst + j) =
+                      make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                                  __uint_as_float(r[j + 3]));
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (col0 + j < a.n_main) dst[j] = __uint_as_float(r[j]);
+              }
+            }
+          } else if (extra) {
+            const int r0 = col0 - a.main_chunks * kChunk;
+            if (valid && a.z != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (r0 + j < a.n_extra) a.z[static_cast<size_t>(row) * a.n_extra + r0 + j] = __uint_as_float(r[j]);
+            }
+          } else {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int id = col0 + j;
+              float x = __uint_as_float(r[j]);
+              if (id < a.n_main) {
+                if (a.bias != nullptr) x += __ldg(a.bias + id);
+              } else {
+                x = -INFINITY;
+              }
+              v[j] = x;
+            }
+            if (a.logits != nullptr && valid) {
+              float* dst = a.logits + static_cast<size_t>(row) * a.n_main;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j < a.n_main) dst[col0 + j] = v[j];
+            }
+            float mx = v[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) mx = fmaxf(mx, v[j]);
+            const bool want = valid && (mx > thr);
+            if (__any_sync(0xffffffffu, want)) {
+              if (want) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  if (v[j] > thr) {
+                    list_insert(lv, li, et, C::kEpiThreads, v[j], col0 + j);
+                    thr = lv[(kTopL - 1) * C::kEpiThreads + et];
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(acc_empty));
+      acc_phase ^= 1u;
+    }
+    if (MODE == 1 && valid && *abort_flag == 0) {
+      const size_t o = (static_cast<size_t>(ns) * a.M + row) * kTopL;
+      for (int i = 0; i < kTopL; ++i) {
+        a.list_val[o + i] = lv[i * C::kEpiThreads + et];
+        a.list_idx[o + i] = li[i * C::kEpiThreads + et];
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------ top-K merge
+__device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
+  return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+// One warp per row: merge the per-split sorted lists into the row's top-K (value desc, id asc).
+__global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict__ lv, const int* __restrict__ li,
+                                                         int n_splits, int M, int K, int32_t* __restrict__ cand,
+                                                         float* __restrict__ unary) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  float tv[kTopL];
+  int ti[kTopL];
+#pragma unroll
+  for (int i = 0; i < kTopL; ++i) {
+    tv[i] = -INFINITY;
+    ti[i] = INT_MAX;
+  }
+  for (int s = lane; s < n_splits; s += 32) {
+    const size_t o = (static_cast<size_t>(s) * M + row) * kTopL;
+    for (int i = 0; i < kTopL; ++i) {
+      float cv = lv[o + i];
+      int ci = li[o + i];
+      if (ci < 0 || !better(cv, ci, tv[kTopL - 1], ti[kTopL - 1])) break;  // lists are sorted
+#pragma unroll
+      for (int j = 0; j < kTopL; ++j) {
+        if (better(cv, ci, tv[j], ti[j])) {
+          const float fv = tv[j];
+          const int fi = ti[j];
+          tv[j] = cv;
+          ti[j] = ci;
+          cv = fv;
+          ci = fi;
+        }
+      }
+    }
+  }
+  for (int k = 0; k < K; ++k) {
+    float bv = tv[0];
+    int bi = ti[0];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      cand[static_cast<size_t>(row) * K + k] = bi;
+      unary[static_cast<size_t>(row) * K + k] = bv;
+    }
+    if (ti[0] == bi) {  // ids are unique across lanes: the owner pops its head
+#pragma unroll
+      for (int j = 0; j < kTopL - 1; ++j) {
+        tv[j] = tv[j + 1];
+        ti[j] = ti[j + 1];
+      }
+      tv[kTopL - 1] = -INFINITY;
+      ti[kTopL - 1] = INT_MAX;
+    }
+  }
+}
+
+// One thread waits on an mbarrier that nothing completes; the bounded wait gives up.
+__global__ void wait_selftest_kernel(uint64_t limit_ns, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  fence_mbar_init();
+  if (!mbar_wait_bounded(smem_u32(&bar), 0, nullptr, limit_ns)) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_TIMEOUT));
+}
+
+// ------------------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows, cols] operand, box = 128 bytes of K x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int dtype, int rows, int cols, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const int es = dtype == DFLASH2_F32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * es};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, dtype == DFLASH2_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int MT, bool TF32, int MODE>
+int launch_tc(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mE, const GemmArgs& args, int grid,
+              cudaStream_t st) {
+  static unsigned done = 0;
+  auto kern = tc_gemm_kernel<MT, TF32, MODE>;
+  if (!ensure_smem_attr(kern, Cfg<MT>::kSmem, &done))
+    return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(cudaGetLastError()));
+  kern<<<grid, Cfg<MT>::kThreads, Cfg<MT>::kSmem, st>>>(mA, mB, mE, args);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "tc_gemm launch failed: %s", cudaGetErrorString(e));
+  return DFLASH2_OK;
+}
+
+template <int MODE>
+int dispatch_tc(int mt, bool tf32, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mE,
+                const GemmArgs& args, int grid, cudaStream_t st) {
+  if (mt == 1) return tf32 ? launch_tc<1, true, MODE>(mA, mB, mE, args, grid, st)
+                           : launch_tc<1, false, MODE>(mA, mB, mE, args, grid, st);
+  return tf32 ? launch_tc<2, true, MODE>(mA, mB, mE, args, grid, st)
+              : launch_tc<2, false, MODE>(mA, mB, mE, args, grid, st);
+}
+
+int prepare_args(const GemmProblem& p, const GemmPlan& plan, CUtensorMap* mA, CUtensorMap* mB, CUtensorMap* mE,
+                 GemmArgs* args) {
+  if (!make_map(mA, p.A, p.dtype, p.M, p.K, 128)) return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (A)");
+  if (!make_map(mB, p.Bw, p.dtype, p.n_main, p.K, kChunk)) return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (W)");
+  if (p.E != nullptr && p.n_extra > 0) {
+    if (!make_map(mE, p.E, p.dtype, p.n_extra, p.K, kChunk))
+      return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (extra)");
+  } else {
+    *mE = *mB;
+  }
+  const int bk = p.dtype == DFLASH2_F32 ? 32 : 64;
+  GemmArgs& a = *args;
+  a = GemmArgs{};
+  a.M = p.M;
+  a.K = p.K;
+  a.n_main = p.n_main;
+  a.n_extra = (p.E != nullptr) ? p.n_extra : 0;
+  a.main_chunks = (p.n_main + kChunk - 1) / kChunk;
+  a.n_chunks = plan.n_chunks;
+  a.m_groups = plan.m_groups;
+  a.n_splits = plan.n_splits;
+  a.k_splits = plan.k_splits;
+  a.k_blocks = (p.K + bk - 1) / bk;
+  a.err = device_error_word();
+  return DFLASH2_OK;
+}
+
+}  // namespace
+
+GemmPlan head_plan(int M, int K, int n_main, int n_extra, int sms) {
+  (void)K;
+  GemmPlan p{};
+  p.mt = M > 128 ? 2 : 1;
+  p.m_groups = (M + 128 * p.mt - 1) / (128 * p.mt);
+  p.n_chunks = (n_main + kChunk - 1) / kChunk + (n_extra + kChunk - 1) / kChunk;
+  p.n_splits = std::max(1, std::min(p.n_chunks, sms / p.m_groups));
+  p.k_splits = 1;
+  return p;
+}
+
+size_t head_workspace(int M, int V, int K, int R, int sms) {
+  (void)K;
+  const GemmPlan p = head_plan(M, 0, V, R, sms);
+  const size_t lists = static_cast<size_t>(p.n_splits) * M * kTopL;
+  return lists * (sizeof(float) + sizeof(int)) + 256;
+}
+
+int launch_gemm_store(const GemmProblem& p, const GemmPlan& plan, float* part, cudaStream_t st) {
+  CUtensorMap mA, mB, mE;
+  GemmArgs a;
+  int rc = prepare_args(p, plan, &mA, &mB, &mE, &a);
+  if (rc != DFLASH2_OK) return rc;
+  a.part = part;
+  const int grid = plan.m_groups * plan.n_splits * plan.k_splits;
+  return dispatch_tc<0>(plan.mt, p.dtype == DFLASH2_F32, mA, mB, mE, a, grid, st);
+}
+
+int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bias, int K, int32_t* cand,
+                     float* unary, float* z, float* logits, void* workspace, cudaStream_t st) {
+  CUtensorMap mA, mB, mE;
+  GemmArgs a;
+  int rc = prepare_args(p, plan, &mA, &mB, &mE, &a);
+  if (rc != DFLASH2_OK) return rc;
+  const size_t lists = static_cast<size_t>(plan.n_splits) * p.M * kTopL;
+  a.list_val = static_cast<float*>(workspace);
+  a.list_idx = reinterpret_cast<int*>(a.list_val + lists);
+  a.bias = bias;
+  a.z = z;
+  a.logits = logits;
+  const int grid = plan.m_groups * plan.n_splits;
+  rc = dispatch_tc<1>(plan.mt, p.dtype == DFLASH2_F32, mA, mB, mE, a, grid, st);
+  if (rc != DFLASH2_OK) return rc;
+  const int rows_per_block = 8;
+  topk_merge_kernel<<<(p.M + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0, st>>>(
+      a.list_val, a.list_idx, plan.n_splits, p.M, K, cand, unary);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "topk_merge launch failed: %s", cudaGetErrorString(e));
+  return DFLASH2_OK;
+}
+
+int launch_wait_selftest(int limit_us, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(static_cast<uint64_t>(limit_us) * 1000ull, device_error_word());
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "selftest launch failed: %s", cudaGetErrorString(e));
+  return DFLASH2_OK;
+}
+
+}  // namespace dfl

@@ -1,0 +1,88 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/dflash2.h"
+
+namespace dfl {
+
+// Device error word of the current device (defined in abi.cu): first error wins.
+int* device_error_word();
+
+// Wall-time limit of every bounded wait inside the GEMM pipeline.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Records a message for dflash2_last_error_message() and returns `status`.
+int fail(int status, const char* fmt, ...);
+
+int sm_count();  // multiprocessors of the current device (cached per device)
+
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device), outside any stream
+// work, so that later calls can be captured into a CUDA graph.
+template <typename F>
+bool ensure_smem_attr(F* kern, int bytes, unsigned* done_mask) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  const unsigned bit = 1u << (dev & 31);
+  if (*done_mask & bit) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  *done_mask |= bit;
+  return true;
+}
+
+// ---------------------------------------------------------------- conv (conv.cu)
+struct ConvShape {
+  int B, G, H, gs, groups, dtype;
+  int rows() const { return B * G; }
+};
+struct GemmPlan;
+size_t conv_prepare_workspace(const ConvShape& s, int sms);
+int launch_rmsnorm(const void* x, const void* w, float eps, void* n, int rows, int H, int dtype, cudaStream_t st);
+int launch_conv_side0(const ConvShape& s, const void* n, const float* part, int k_splits, const float* base,
+                      void* out, void* coef1, float* d_full, cudaStream_t st);
+int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, const float* base, const void* residual,
+                      void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st);
+
+// ---------------------------------------------------------------- tensor-core GEMM (gemm.cu)
+// C[m, n] = sum_k A[m, k] * Bw[n, k] over rows m < M of A ([M, K]) and the virtual column range
+// [0, n_main) of Bw ([n_main, K]) followed by [pad64(n_main), pad64(n_main) + n_extra) of E ([n_extra, K]).
+struct GemmProblem {
+  const void* A;
+  const void* Bw;
+  const void* E;  // extra operand rows (hidden_projection) or nullptr
+  int M, K, n_main, n_extra, dtype;
+};
+struct GemmPlan {
+  int mt;        // 128-row M tiles per CTA (1 or 2)
+  int m_groups;  // ceil(M / (128 * mt))
+  int n_splits;  // column ranges (balanced over 64-column chunks)
+  int k_splits;  // reduction ranges (STORE mode only)
+  int n_chunks;  // 64-column chunks over the virtual range
+};
+// Split-K plan of the kernel_projection GEMM; shared by the workspace query and the launch.
+GemmPlan kp_plan(const ConvShape& s, int sms);
+GemmPlan head_plan(int M, int K, int n_main, int n_extra, int sms);
+size_t head_workspace(int M, int V, int K, int R, int sms);
+// mode 0: write fp32 partial sums part[k_split][M][n_main].
+int launch_gemm_store(const GemmProblem& p, const GemmPlan& plan, float* part, cudaStream_t st);
+// mode 1: per-row running top-16 over the main columns (+bias), z for the extra columns,
+// optional full logits; then a merge into cand/unary.
+int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bias, int K, int32_t* cand,
+                     float* unary, float* z, float* logits, void* workspace, cudaStream_t st);
+int launch_wait_selftest(int limit_us, cudaStream_t st);
+
+// ---------------------------------------------------------------- selector (selector.cu)
+int launch_score_edges(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
+                       const void* pred, const void* succ, int B, int steps, int K, int R, int V, int dtype,
+                       float* S, int32_t* path, cudaStream_t st);
+int launch_select_path(const float* S, const int32_t* cand, int B, int steps, int K, int32_t* path,
+                       cudaStream_t st);
+
+}  // namespace dfl

@@ -1,0 +1,122 @@
+"""The block tail as a sequence of library calls, with every buffer allocated once.
+
+``TailRunner`` holds the weights of one drafter tail on the device and preallocates all
+activations and workspaces, so a pass is a fixed sequence of C-ABI launches on one stream (and
+can be captured into a CUDA graph after a first eager pass). Per conv site (MAX
+DFlash2TransformerBlock; dflash2.ts #block):
+
+    a, coef1 = conv_prepare(n or x)            # side 0 (+ the first site's RMSNorm)
+    (the sublayer: here its seeded output y)
+    x = x + conv_finish(y, coef1)              # side 1 + residual, and the next site's RMSNorm
+
+then h = final_norm(x[:, 1:]), head GEMM + top-K + z, edge scores and the greedy walk.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+from . import (dflash2_conv_finish, dflash2_conv_prepare, dflash2_conv_prepare_workspace_bytes, dflash2_head_topk,
+               dflash2_head_topk_workspace_bytes, dflash2_score_edges)
+
+
+def to_device(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """Upload a stored host tensor: uint16 arrays hold bf16 bits; float32 / int32 go as they are."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(a).to(device)
+
+
+def to_pinned(a: np.ndarray) -> torch.Tensor:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(a)
+    return t.pin_memory()
+
+
+@dataclass
+class SiteWeights:
+    w_kp: torch.Tensor
+    base: torch.Tensor
+    norm_w: torch.Tensor
+
+
+class TailRunner:
+    """One drafter tail (conv sites -> final norm -> selector) with preallocated buffers."""
+
+    def __init__(self, wl, device="cuda", with_selector: bool = True):
+        self.wl = wl
+        self.device = device
+        self.dtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        B, G, H = wl.B, wl.G, wl.H
+        self.sites: List[SiteWeights] = [SiteWeights(to_device(s.w_kp, device), to_device(s.base, device),
+                                                     to_device(s.norm_w, device)) for s in wl.sites]
+        self.with_selector = with_selector and wl.w_head is not None
+        dt = self.dtype
+        self.x = torch.empty((B, G, H), dtype=dt, device=device)
+        self.a = torch.empty((B, G, H), dtype=dt, device=device)
+        self.n = torch.empty((B, G, H), dtype=dt, device=device)
+        self.coef1 = torch.empty((B, G, 2, H // wl.gs), dtype=dt, device=device)
+        ws = dflash2_conv_prepare_workspace_bytes(B, G, H, wl.gs, dt)
+        self.conv_ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        if self.with_selector:
+            self.final_norm_w = to_device(wl.final_norm_w, device) if wl.final_norm_w is not None else None
+            self.w_head = to_device(wl.w_head, device)
+            self.bias = to_device(wl.bias, device) if wl.bias is not None else None
+            self.w_proj = to_device(wl.w_proj, device)
+            self.pred = to_device(wl.pred_book, device)
+            self.succ = to_device(wl.succ_book, device)
+            M = B * wl.steps
+            self.h = torch.empty((B, wl.steps, H), dtype=dt, device=device)
+            self.cand = torch.empty((M, wl.K), dtype=torch.int32, device=device)
+            self.unary = torch.empty((M, wl.K), dtype=torch.float32, device=device)
+            self.z = torch.empty((M, wl.R), dtype=torch.float32, device=device)
+            self.S = torch.empty((B, wl.steps, wl.K, wl.K), dtype=torch.float32, device=device)
+            self.path = torch.empty((B, wl.steps), dtype=torch.int32, device=device)
+            hw = dflash2_head_topk_workspace_bytes(M, H, wl.V, wl.K, wl.R)
+            self.head_ws = torch.empty(max(hw, 256), dtype=torch.uint8, device=device)
+
+    # ------------------------------------------------------------------ passes
+    def conv_chain(self, x0: torch.Tensor, ys: List[torch.Tensor], emit_h: bool):
+        """x <- x0, then every site in order; returns the final residual stream (self.x)."""
+        wl = self.wl
+        self.x.copy_(x0)
+        nsites = len(self.sites)
+        for i, s in enumerate(self.sites):
+            if i == 0:
+                dflash2_conv_prepare(self.x, s.norm_w, wl.eps, s.w_kp, s.base, wl.gs, out=self.a, coef1=self.coef1,
+                                     workspace=self.conv_ws)
+            else:
+                dflash2_conv_prepare(self.n, None, wl.eps, s.w_kp, s.base, wl.gs, out=self.a, coef1=self.coef1,
+                                     workspace=self.conv_ws)
+            if i + 1 < nsites:
+                dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=self.x, out=self.x,
+                                    next_norm_w=self.sites[i + 1].norm_w, eps=wl.eps, next_n=self.n, next_row0=0)
+            elif emit_h:
+                dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=self.x, out=self.x,
+                                    next_norm_w=self.final_norm_w, eps=wl.eps, next_n=self.h, next_row0=1)
+            else:
+                dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=self.x, out=self.x)
+        return self.x
+
+    def selector(self, h: torch.Tensor, anchors: torch.Tensor, want_S: bool = True):
+        wl = self.wl
+        M = h.shape[0] * h.shape[1]
+        dflash2_head_topk(h.view(M, wl.H), self.w_head, wl.K, bias=self.bias, w_proj=self.w_proj, cand=self.cand,
+                          unary=self.unary, z=self.z, workspace=self.head_ws)
+        B = h.shape[0]
+        dflash2_score_edges(self.cand.view(B, wl.steps, wl.K), self.unary.view(B, wl.steps, wl.K),
+                            self.z.view(B, wl.steps, wl.R), anchors, self.pred, self.succ, want_S=want_S,
+                            want_path=True, S=self.S if want_S else None, path=self.path)
+        return self.path
+
+    def full(self, x0: torch.Tensor, ys: List[torch.Tensor], anchors: torch.Tensor, want_S: bool = True):
+        """The whole block tail; returns path [B, steps] int32 (device)."""
+        self.conv_chain(x0, ys, emit_h=True)
+        return self.selector(self.h, anchors, want_S=want_S)

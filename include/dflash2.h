@@ -1,0 +1,197 @@
+/*
+ * dflash2.h — C ABI of the GB300 (sm_103a) library for the block-local tail of the
+ * DFlash2 speculative-decoding drafter.
+ *
+ * The library computes two things, on one GPU, for B independent draft blocks of G rows
+ * (an anchor row followed by G-1 mask rows):
+ *
+ *  1. the two-tap dynamic grouped depthwise convolution wrapped around each drafter
+ *     sublayer. kernel_projection of the RMS-normed sublayer input emits
+ *     D[t, side, tap, group] for both sides at once; side 0 is applied before the
+ *     sublayer (prepare) and side 1 after it (finish):
+ *         Conv_side(y)[t, c] = sum_tau (base[side, tau, c] + D[t, side, tau, c / gs]) * y[t - tau, c]
+ *     with t block-local and y[-1] = 0, so nothing is read across a block boundary.
+ *     (dflash2.ts of "@mlx-bun/inference 1.0.0": header comment, #coefficients, #conv;
+ *      MAX API "max.pipelines.architectures.dflash2_qwen3_5": DFlash2GroupedConv,
+ *      prepare, finish, DFlash2TransformerBlock.)
+ *
+ *  2. the candidate-path selector: the head GEMM over rows 1..G-1 with a fused top-K per
+ *     row, z = hidden_projection(h), the low-rank bilinear edge scores
+ *         S[b, l, p, c] = unary[b, l, c] + sum_r pred_book[pid(b,l,p), r] * z[b, l, r] * succ_book[cand[b, l, c], r]
+ *     (pid(b, 0, p) = anchor[b], pid(b, l, p) = cand[b, l-1, p]) and the greedy
+ *     left-to-right walk over S.
+ *     (MAX API: DFlash2CandidateSelector, score_edges, select_path,
+ *      DFlash2Qwen3_5.compute_candidates; dflash2.ts: #select.)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer is a DEVICE pointer owned by the caller, unless stated otherwise. The
+ *    library never allocates device memory per call; scratch comes from caller-owned
+ *    workspaces whose size a *_workspace_bytes() query returns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ *    default stream). A return value reports host-side validation and launch only.
+ *  - Device-side faults the kernels can detect (an id outside [0, V), a bounded wait that
+ *    ran out) are recorded in a device error word instead of trapping;
+ *    dflash2_poll_error() reads and clears it.
+ *  - dtype: DFLASH2_BF16 (production: bf16 storage, fp32 arithmetic and accumulation,
+ *    tcgen05 kind::f16) or DFLASH2_F32 (fp32 storage; elementwise work in fp32, the GEMMs
+ *    on tcgen05 kind::tf32).
+ *  - Tensors are dense, row-major, with the innermost dimension last, and 16-byte aligned.
+ *  - The first call of an entry point on a device sets kernel attributes; make it before
+ *    capturing the calls into a CUDA graph.
+ *  - Errors: DFLASH2_ERR_INVALID_ARG for a NULL required pointer, a misaligned pointer or a
+ *    shape outside the documented limits; DFLASH2_ERR_UNSUPPORTED for taps != 2 (two-tap
+ *    only, as dflash2.ts readConfig demands); DFLASH2_ERR_WORKSPACE for a workspace smaller
+ *    than the query returns; DFLASH2_ERR_CUDA if a launch failed. Nothing is launched when
+ *    an error is returned. dflash2_last_error_message() describes the last failure of the
+ *    calling thread.
+ */
+#ifndef DFLASH2_H_
+#define DFLASH2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DFLASH2_API __attribute__((visibility("default")))
+#else
+#define DFLASH2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DFLASH2_OK = 0,
+  DFLASH2_ERR_INVALID_ARG = -1,
+  DFLASH2_ERR_UNSUPPORTED = -2,
+  DFLASH2_ERR_CUDA = -3,
+  DFLASH2_ERR_WORKSPACE = -4,
+  DFLASH2_ERR_TIMEOUT = -5,  /* device: a bounded wait gave up */
+  DFLASH2_ERR_BAD_INDEX = -6 /* device: a token id outside [0, V) was read */
+} dflash2_status;
+
+typedef enum { DFLASH2_BF16 = 0, DFLASH2_F32 = 1 } dflash2_dtype;
+
+/* Library version, e.g. 100 for 0.1.0. */
+DFLASH2_API int dflash2_version(void);
+
+/* Human-readable name of a status code (static storage). */
+DFLASH2_API const char* dflash2_status_string(int status);
+
+/* Description of the last error returned to the calling host thread (thread-local storage). */
+DFLASH2_API const char* dflash2_last_error_message(void);
+
+/* Synchronises `stream`, then returns and clears the device error word of the current
+ * device (DFLASH2_OK if no kernel recorded an error), or DFLASH2_ERR_CUDA if the
+ * synchronisation itself failed. */
+DFLASH2_API int dflash2_poll_error(void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Conv, pre-sublayer side (MAX DFlash2GroupedConv.prepare; dflash2.ts #block:
+ * n = rms(x); coef = #coefficients(n); a = #conv(n, coef, 0)).
+ *
+ *   x        [B, G, H] dtype  the sublayer input (residual stream), one dense G-row block
+ *                             per draft block (MAX forward_block: the block axis is a
+ *                             reshape of the token axis).
+ *   norm_w   [H] dtype or NULL. Non-NULL: n = x / sqrt(mean(x^2) + eps) * norm_w is
+ *                             computed first. NULL: x is already normalised (n = x).
+ *   eps      RMSNorm epsilon.
+ *   w_kp     [2*taps*groups, H] dtype, kernel_projection weight stored (out, in); output
+ *                             column o = (side*taps + tap)*groups + group.
+ *   base     [2, taps, H] fp32 base kernel (side, tap, channel).
+ *   B >= 1, 2 <= G <= 64, H % 64 == 0, group_size % 8 == 0, H % group_size == 0,
+ *   groups = H / group_size, taps == 2.
+ *   out      [B, G, H] dtype   a = side-0 conv of n (fp32 arithmetic, rounded to dtype).
+ *   coef1    [B, G, taps, groups] dtype  side 1's deltas D[t, 1, tap, g], WITHOUT the base
+ *                             kernel (finish adds base[1] back).
+ *   d_full   [B, G, 2, taps, groups] fp32 or NULL: the full projection D (diagnostics).
+ *   workspace / workspace_bytes: at least dflash2_conv_prepare_workspace_bytes(...) bytes
+ *                             of device memory, 256-byte aligned; contents are scratch.
+ * ---------------------------------------------------------------------------------- */
+DFLASH2_API size_t dflash2_conv_prepare_workspace_bytes(int B, int G, int H, int group_size, int dtype);
+DFLASH2_API int dflash2_conv_prepare(const void* x, const void* norm_w, float eps, const void* w_kp, const float* base,
+                         int B, int G, int H, int group_size, int taps, int dtype, void* out, void* coef1,
+                         float* d_full, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Conv, post-sublayer side plus the residual add (MAX DFlash2GroupedConv.finish and
+ * DFlash2TransformerBlock: r += conv.finish(h); dflash2.ts #block: x = x + #conv(out, coef, 1)
+ * with the add in fp32).
+ *
+ *   y         [B, G, H] dtype   the sublayer output.
+ *   coef1     [B, G, taps, groups] dtype  from dflash2_conv_prepare.
+ *   base      [2, taps, H] fp32 (side 1 is used).
+ *   residual  [B, G, H] dtype or NULL. out = residual + Conv_1(y) (fp32 add, one rounding),
+ *                             or out = Conv_1(y) when NULL. out may alias residual.
+ *   out       [B, G, H] dtype.
+ *   next_norm_w [H] dtype or NULL; next_n dtype or NULL (both or neither):
+ *             next_n[b, t - next_row0, :] = rms(out[b, t, :]) * next_norm_w for
+ *             t in [next_row0, G), i.e. a [B, G - next_row0, H] tensor. next_row0 = 0 feeds
+ *             the next conv site's prepare (norm_w = NULL); next_row0 = 1 with the final
+ *             norm gives the head's input h (rows 1..G-1, dflash2.ts #block).
+ *             Requires H / 8 <= 1024 (the row reduction runs in one thread-block cluster).
+ * ---------------------------------------------------------------------------------- */
+DFLASH2_API int dflash2_conv_finish(const void* y, const void* coef1, const float* base, int B, int G, int H,
+                        int group_size, int taps, int dtype, const void* residual, void* out,
+                        const void* next_norm_w, float eps, void* next_n, int next_row0, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Head GEMM + fused top-K + hidden_projection (MAX DFlash2Qwen3_5.compute_candidates and
+ * DFlash2CandidateSelector's proj(h); dflash2.ts #block: logits = head(h), z = selProj(h),
+ * #select's per-row top-K). Full-vocabulary logits are never written to memory.
+ *
+ *   h         [M, H] dtype   the normed drafter rows (M = B * (G - 1), rows 1..G-1 of each block).
+ *   w_head    [V, H] dtype   the borrowed head, stored (out, in).
+ *   bias      [V] fp32 or NULL, added to every logit.
+ *   w_proj    [R, H] dtype or NULL (then z must be NULL): hidden_projection weight.
+ *   cand      [M, K] int32   the K best vocabulary ids per row, by value descending; equal
+ *                            values keep the lower id first (the same rule decides the K-th place).
+ *   unary     [M, K] fp32    their logits.
+ *   z         [M, R] fp32 or NULL: h @ w_proj^T.
+ *   logits    [M, V] fp32 or NULL: every logit (diagnostics only; costs M*V*4 bytes of writes).
+ *   1 <= K <= 16, K <= V, H % 64 == 0, R % 16 == 0 and R <= 256 when w_proj is given.
+ *   workspace: at least dflash2_head_topk_workspace_bytes(M, H, V, K, R) bytes.
+ * ---------------------------------------------------------------------------------- */
+DFLASH2_API size_t dflash2_head_topk_workspace_bytes(int M, int H, int V, int K, int R);
+DFLASH2_API int dflash2_head_topk(const void* h, int M, int H, const void* w_head, int V, const float* bias, const void* w_proj,
+                      int R, int K, int dtype, int32_t* cand, float* unary, float* z, float* logits,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Edge scores, optionally fused with the greedy walk (MAX DFlash2CandidateSelector.score_edges
+ * and select_path; dflash2.ts #select).
+ *
+ *   cand      [B, steps, K] int32 candidate ids (from dflash2_head_topk, M = B * steps).
+ *   unary     [B, steps, K] fp32.
+ *   z         [B, steps, R] fp32.
+ *   anchors   [B] int32, the last verified token of each block.
+ *   pred_book, succ_book [V, R] dtype  predecessor / successor codebooks.
+ *   1 <= steps <= 63, 1 <= K <= 32, 8 <= R <= 128 with R % 8 == 0.
+ *   S         [B, steps, K, K] fp32 indexed [b, l, p, c], or NULL.
+ *   path      [B, steps] int32 or NULL: the greedy walk (slot 0 reads row p = 0; slot l reads
+ *             the row of the position chosen at l-1; ties go to the lowest position).
+ *   At least one of S and path must be non-NULL. An id outside [0, V) sets
+ *   DFLASH2_ERR_BAD_INDEX and reads as a zero codebook row.
+ * ---------------------------------------------------------------------------------- */
+DFLASH2_API int dflash2_score_edges(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
+                        const void* pred_book, const void* succ_book, int B, int steps, int K, int R, int V,
+                        int dtype, float* S, int32_t* path, void* stream);
+
+/* The greedy walk alone, over a given S (MAX DFlash2CandidateSelector.select_path without a
+ * sampler). S [B, steps, K, K] fp32, cand [B, steps, K] int32 -> path [B, steps] int32.
+ * 1 <= steps, 1 <= K <= 32. */
+DFLASH2_API int dflash2_select_path(const float* S, const int32_t* cand, int B, int steps, int K, int32_t* path, void* stream);
+
+/* Self-test of the bounded-wait machinery: launches one block that waits on an mbarrier that
+ * nothing completes, with a limit of `limit_us` microseconds (1..1000000). The wait gives up,
+ * records DFLASH2_ERR_TIMEOUT in the device error word and the kernel returns; read it with
+ * dflash2_poll_error(). Has no counterpart on the pages. */
+DFLASH2_API int dflash2_selftest_bounded_wait(int limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH2_H_ */

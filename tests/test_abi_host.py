@@ -1,0 +1,133 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads, exports every
+symbol include/dflash2.h declares, and rejects bad arguments before launching anything."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "dflash2.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dflash2_block_drafter_gb300 import _build
+    import dflash2_block_drafter_gb300 as pkg
+    _build.build()
+    return pkg.library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"DFLASH2_API\s+[\w\s\*]+?\b(dflash2_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("dflash2_conv_prepare", "dflash2_conv_finish", "dflash2_head_topk", "dflash2_score_edges",
+                     "dflash2_select_path"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from dflash2_block_drafter_gb300 import library_path
+    out = subprocess.run(["nm", "-D", "--defined-only", library_path], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(dflash2_\w+)", out))
+    for name in declared_symbols():
+        assert name in exported, f"{name} declared in dflash2.h but not exported"
+        assert hasattr(lib, name)
+    # nothing else leaks out of the library's namespace
+    assert all(n.startswith("dflash2_") for n in exported)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.dflash2_version() == 100
+    assert lib.dflash2_status_string(0) == b"DFLASH2_OK"
+    assert lib.dflash2_status_string(-1) == b"DFLASH2_ERR_INVALID_ARG"
+    assert lib.dflash2_status_string(-5) == b"DFLASH2_ERR_TIMEOUT"
+    assert lib.dflash2_status_string(12345) == b"DFLASH2_ERR_UNKNOWN"
+
+
+FAKE = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced: validation fails first
+FAKE_MIS = ctypes.c_void_p(0x10008)  # misaligned
+
+
+def _prep(lib, **kw):
+    a = dict(x=FAKE, norm_w=None, eps=1e-6, w_kp=FAKE, base=FAKE, B=1, G=16, H=5120, gs=16, taps=2, dtype=0,
+             out=FAKE, coef1=FAKE, d_full=None, ws=FAKE, ws_bytes=0, stream=None)
+    a.update(kw)
+    return lib.dflash2_conv_prepare(a["x"], a["norm_w"], a["eps"], a["w_kp"], a["base"], a["B"], a["G"], a["H"],
+                                    a["gs"], a["taps"], a["dtype"], a["out"], a["coef1"], a["d_full"], a["ws"],
+                                    a["ws_bytes"], a["stream"])
+
+
+def test_conv_prepare_rejects_bad_arguments(lib):
+    assert _prep(lib, taps=3) == -2                      # two-tap only
+    assert _prep(lib, G=1) == -1                         # no zero-draft-row blocks
+    assert _prep(lib, G=65) == -1
+    assert _prep(lib, H=5000) == -1                      # H % 64
+    assert _prep(lib, gs=12) == -1                       # group size % 8
+    assert _prep(lib, gs=24, H=5120) == -1               # H % group size
+    assert _prep(lib, B=0) == -1
+    assert _prep(lib, dtype=7) == -1
+    assert _prep(lib, x=None) == -1
+    assert _prep(lib, x=FAKE_MIS) == -1
+    assert _prep(lib, ws=ctypes.c_void_p(0x10010)) == -1  # workspace not 256-aligned
+    assert _prep(lib, ws_bytes=16) == -4                  # workspace too small
+    assert b"workspace" in lib.dflash2_last_error_message()
+
+
+def test_conv_finish_rejects_bad_arguments(lib):
+    f = lib.dflash2_conv_finish
+    assert f(FAKE, FAKE, FAKE, 1, 16, 5120, 16, 2, 0, None, FAKE, FAKE, 1e-6, None, 0, None) == -1  # half a norm pair
+    assert f(FAKE, FAKE, FAKE, 1, 16, 5120, 16, 2, 0, None, FAKE, FAKE, 1e-6, FAKE, 16, None) == -1  # next_row0 >= G
+    assert f(FAKE, FAKE, FAKE, 1, 16, 5120, 16, 3, 0, None, FAKE, None, 1e-6, None, 0, None) == -2
+    assert f(None, FAKE, FAKE, 1, 16, 5120, 16, 2, 0, None, FAKE, None, 1e-6, None, 0, None) == -1
+    assert f(FAKE, FAKE, FAKE, 1, 16, 5120, 16, 2, 0, FAKE_MIS, FAKE, None, 1e-6, None, 0, None) == -1
+
+
+def test_head_topk_rejects_bad_arguments(lib):
+    f = lib.dflash2_head_topk
+    ok = dict(h=FAKE, M=15, H=5120, w=FAKE, V=248320, bias=None, wp=FAKE, R=64, K=16, dt=0, cand=FAKE, unary=FAKE,
+              z=FAKE, logits=None, ws=FAKE, wsb=0, st=None)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(a["h"], a["M"], a["H"], a["w"], a["V"], a["bias"], a["wp"], a["R"], a["K"], a["dt"], a["cand"],
+                 a["unary"], a["z"], a["logits"], a["ws"], a["wsb"], a["st"])
+    assert call(K=17) == -1
+    assert call(K=0) == -1
+    assert call(V=8) == -1        # K > V
+    assert call(M=0) == -1
+    assert call(H=100) == -1
+    assert call(R=24) == -1       # R % 16
+    assert call(z=None) == -1     # w_proj without z
+    assert call(h=FAKE_MIS) == -1
+    assert call() == -4           # workspace too small
+    assert lib.dflash2_head_topk_workspace_bytes(15, 5120, 248320, 16, 64) > 0
+
+
+def test_score_edges_and_walk_reject_bad_arguments(lib):
+    f = lib.dflash2_score_edges
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 15, 16, 64, 1000, 0, None, None, None) == -1  # no output
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 15, 33, 64, 1000, 0, FAKE, None, None) == -1  # K > 32
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 16, 64, 1000, 0, FAKE, None, None) == -1  # steps > 63
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 15, 16, 60, 1000, 0, FAKE, None, None) == -1  # R % 8
+    assert f(FAKE, FAKE, FAKE_MIS, FAKE, FAKE, FAKE, 1, 15, 16, 64, 1000, 0, FAKE, None, None) == -1
+    g = lib.dflash2_select_path
+    assert g(FAKE, FAKE, 1, 15, 0, FAKE, None) == -1
+    assert g(None, FAKE, 1, 15, 16, FAKE, None) == -1
+    assert lib.dflash2_selftest_bounded_wait(0, None) == -1
+    assert lib.dflash2_selftest_bounded_wait(2000000, None) == -1
+
+
+def test_binding_requires_cuda_tensors(lib):
+    import torch
+    import dflash2_block_drafter_gb300 as d
+    x = torch.zeros(1, 16, 64, dtype=torch.bfloat16)
+    with pytest.raises((ValueError, RuntimeError)):
+        d.dflash2_conv_finish(x, torch.zeros(1, 16, 2, 4, dtype=torch.bfloat16), torch.zeros(2, 2, 64), 16)

@@ -1,0 +1,87 @@
+"""GPU parity of score_edges and the greedy walk against the float64 oracle."""
+import numpy as np
+import pytest
+
+from oracle import dflash2_oracle as O
+from synth import inputs as I
+from tests.gpu_util import require_gpu
+from tests.parity import REL_TOL, assert_close_scaled, compare_walk, scale_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return require_gpu()
+
+
+def _case(seed, B, steps, K, R, V, dtype="bf16", book_std=0.5):
+    rng = np.random.default_rng(seed)
+    cand = np.stack([np.stack([rng.choice(V, size=K, replace=False) for _ in range(steps)]) for _ in range(B)])
+    cand = cand.astype(np.int32)
+    unary = np.sort(rng.standard_normal((B, steps, K)).astype(np.float32), axis=-1)[..., ::-1].copy()
+    z = rng.standard_normal((B, steps, R)).astype(np.float32)
+    anchors = rng.integers(0, V, size=B).astype(np.int32)
+    pred = I.normal(seed, "pred", (V, R), book_std, dtype=dtype)
+    succ = I.normal(seed, "succ", (V, R), book_std, dtype=dtype)
+    return cand, unary, z, anchors, pred, succ
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("B,steps,K,R,V", [(1, 15, 16, 64, 5000), (33, 15, 16, 64, 248320), (7, 7, 16, 16, 4096),
+                                           (5, 4, 3, 8, 50), (3, 31, 32, 128, 1000)])
+def test_score_edges_and_walk(torch, dtype, B, steps, K, R, V):
+    import dflash2_block_drafter_gb300 as d
+    from dflash2_block_drafter_gb300.tail import to_device
+    cand, unary, z, anchors, pred, succ = _case(B * 100 + K, B, steps, K, R, V, dtype)
+    S, path = d.dflash2_score_edges(to_device(cand), to_device(unary), to_device(z), to_device(anchors),
+                                    to_device(pred), to_device(succ))
+    assert d.dflash2_poll_error() == 0
+    S = S.cpu().numpy()
+    path = path.cpu().numpy()
+    rS = O.score_edges(cand, unary, z, anchors, I.to_f64(pred), I.to_f64(succ))
+    assert_close_scaled(S, rS, what="S")
+    assert_close_scaled(S, rS, rel=1e-5, what="S (fp32 bound)")
+    rpath, rpos = O.select_path(rS, cand)
+    tol = REL_TOL * scale_of(rS)
+    near, checked = compare_walk(path, rpath, O.walk_margins(rS, rpos), tol)
+    # the walk over the GPU's own S is exact (same fp32 values, same tie rule)
+    gpath, _ = O.select_path(S.astype(np.float64), cand)
+    np.testing.assert_array_equal(path, gpath)
+    # the standalone walk agrees with the fused one
+    p2 = d.dflash2_select_path(to_device(S), to_device(cand)).cpu().numpy()
+    np.testing.assert_array_equal(p2, path)
+    print(f"walk: {checked} slots strict, {near} near-tie blocks")
+
+
+def test_zero_codebooks_walk_is_top1(torch):
+    import dflash2_block_drafter_gb300 as d
+    from dflash2_block_drafter_gb300.tail import to_device
+    cand, unary, z, anchors, pred, succ = _case(9, 8, 15, 16, 64, 3000)
+    zero = np.zeros_like(pred)
+    S, path = d.dflash2_score_edges(to_device(cand), to_device(unary), to_device(z), to_device(anchors),
+                                    to_device(zero), to_device(zero))
+    np.testing.assert_array_equal(path.cpu().numpy(), cand[:, :, 0])
+    np.testing.assert_array_equal(S.cpu().numpy(), np.broadcast_to(unary[:, :, None, :], S.shape))
+
+
+def test_slot0_rows_identical(torch):
+    import dflash2_block_drafter_gb300 as d
+    from dflash2_block_drafter_gb300.tail import to_device
+    cand, unary, z, anchors, pred, succ = _case(10, 4, 15, 16, 64, 3000)
+    S, _ = d.dflash2_score_edges(to_device(cand), to_device(unary), to_device(z), to_device(anchors),
+                                 to_device(pred), to_device(succ), want_path=False)
+    S = S.cpu().numpy()
+    for p in range(1, 16):
+        np.testing.assert_array_equal(S[:, 0, p], S[:, 0, 0])
+
+
+def test_bad_index_sets_error_word(torch):
+    import dflash2_block_drafter_gb300 as d
+    from dflash2_block_drafter_gb300.tail import to_device
+    cand, unary, z, anchors, pred, succ = _case(12, 2, 5, 4, 16, 100)
+    cand[1, 2, 3] = 100      # == V: out of range
+    d.dflash2_score_edges(to_device(cand), to_device(unary), to_device(z), to_device(anchors), to_device(pred),
+                          to_device(succ))
+    assert d.dflash2_poll_error() == -6
+    assert d.dflash2_poll_error() == 0   # cleared

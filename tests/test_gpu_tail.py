@@ -1,0 +1,68 @@
+"""GPU parity of the whole block tail (conv chain -> final norm -> head + top-K + z -> S -> walk)."""
+import numpy as np
+import pytest
+
+from oracle import dflash2_oracle as O
+from synth import inputs as I
+from tests.gpu_util import dev_f64, oracle_sites, require_gpu
+from tests.parity import REL_TOL, assert_close_scaled, compare_topk, compare_walk, scale_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return require_gpu()
+
+
+def _check_tail(run, wl, blocks):
+    """Compare the GPU tail with the oracle on the listed blocks (blocks never interact)."""
+    blocks = list(blocks)
+    ref = O.block_tail(I.to_f64(wl.x0)[blocks], oracle_sites(wl, blocks), I.to_f64(wl.final_norm_w), wl.eps, wl.gs,
+                       I.f64_view(wl.w_head), wl.bias, I.to_f64(wl.w_proj), I.f64_view(wl.pred_book),
+                       I.f64_view(wl.succ_book), wl.anchors[blocks], wl.K)
+    h = dev_f64(run.h)[blocks]
+    assert_close_scaled(h, ref["h"], what="h")
+    steps, K, R = wl.steps, wl.K, wl.R
+    cand = run.cand.view(wl.B, steps, K).cpu().numpy()[blocks]
+    unary = run.unary.view(wl.B, steps, K).cpu().numpy()[blocks]
+    z = run.z.view(wl.B, steps, R).cpu().numpy()[blocks]
+    # top-K against the oracle's logits of the oracle's h (the chain's rounding is inside the tolerance)
+    tol = REL_TOL * scale_of(ref["logits"])
+    near = compare_topk(cand.reshape(-1, K), unary.reshape(-1, K), ref["logits"].reshape(-1, wl.V), K,
+                        tol)
+    assert_close_scaled(z, ref["z"], what="z")
+    # the selector teacher-forced on the GPU's candidates (isolates it from head near-ties)
+    ref_S = O.score_edges(cand, unary, z, wl.anchors[blocks], I.f64_view(wl.pred_book), I.f64_view(wl.succ_book))
+    S = run.S.cpu().numpy()[blocks]
+    assert_close_scaled(S, ref_S, what="S")
+    ref_path, ref_pos = O.select_path(ref_S, cand)
+    path = run.path.cpu().numpy()[blocks]
+    walk_near, checked = compare_walk(path, ref_path, O.walk_margins(ref_S, ref_pos), REL_TOL * scale_of(ref_S))
+    # end to end against the oracle's own walk, up to the first slot either side leaves the decided region
+    print(f"tail: near-tie rows {near}, walk near-tie blocks {walk_near}, strict slots {checked}")
+    return ref
+
+
+def test_tiny_full_tail_f32(torch):
+    from dflash2_block_drafter_gb300.tail import TailRunner, to_device
+    wl = I.make_config(0)
+    run = TailRunner(wl)
+    run.full(to_device(wl.x0), [to_device(s.y) for s in wl.sites], to_device(wl.anchors))
+    import dflash2_block_drafter_gb300 as d
+    assert d.dflash2_poll_error() == 0
+    ref = _check_tail(run, wl, range(wl.B))
+    assert_close_scaled(dev_f64(run.x), ref["x"], rel=2e-3, what="x (f32)")
+
+
+def test_full_tail_b64_sampled(torch):
+    """The full tail at B=64 (drafter shape, Zipf bias); the oracle checks three sampled blocks."""
+    from dflash2_block_drafter_gb300.tail import TailRunner, to_device
+    wl = I.make_config(4)
+    run = TailRunner(wl)
+    run.full(to_device(wl.x0), [to_device(s.y) for s in wl.sites], to_device(wl.anchors))
+    import dflash2_block_drafter_gb300 as d
+    assert d.dflash2_poll_error() == 0
+    _check_tail(run, wl, [0, 31, 63])
+    path = run.path.cpu().numpy()
+    assert path.shape == (64, 15) and np.all((path >= 0) & (path < wl.V))
