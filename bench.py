@@ -1,0 +1,415 @@
+"""Benchmark of the DFlash2 block tail on GB300: draft blocks per second.
+
+One step = one pass of the whole hot path over one batch of B=64 draft blocks (G=16 rows,
+hidden 5120): ten conv sites (5 layers x attention/MLP; prepare -> seeded sublayer output ->
+finish), the final norm of rows 1..15, the head GEMM over V=248320 with the fused top-16 and
+hidden_projection, the edge scores and the greedy walk. Inputs are seeded synthetic tensors
+resident in HBM; the head weight (2.54 GB) is larger than L2 and an L2 flush (a 256 MB write)
+also runs between timed steps, outside the timed region.
+
+Prints one JSON line. ``--impl reference`` times the CPU float64 oracle instead (on a bounded
+sample of the same workload per step). Under torchrun every rank runs its own 64 blocks (weak
+scaling, no collective on the data path) and rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOADS = {
+    # name: (config index, B)
+    "full-tail-B64": (4, 64),
+    "full-tail-B8": (4, 8),
+    "selector-B1": (2, 1),
+    "selector-B32": (3, 32),
+    "conv-chain-B64": (1, 64),
+    "conv-chain-B1": (1, 1),
+}
+METRIC = "draft blocks/sec (G=16, hidden 5120) at 1 GB300; % of HBM roofline per kernel"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ algorithmic work
+
+def head_flops(M, V, R, H):
+    return 2.0 * M * (V + R) * H
+
+
+def head_bytes(M, V, R, H, K):
+    return 2.0 * (V + R) * H + 2.0 * M * H + 4.0 * V + M * (8.0 * K + 4.0 * R)
+
+
+def conv_site_bytes(B, G, H, groups):
+    """Per conv site: kp weights + prepare (n in, a out, coef1 out) + finish (y, x in, x out, next n out, coef1 in)."""
+    rows = B * G
+    return 2.0 * 4 * groups * H + rows * H * 2.0 * 2 + rows * H * 2.0 * 4 + 2 * rows * 2 * groups * 2.0
+
+
+# ------------------------------------------------------------------------------ reference arm
+
+def oracle_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_block_tail(wl, blocks):
+    """The oracle's full tail on the listed blocks of the workload (blocks never interact)."""
+    from oracle import dflash2_oracle as O
+    from synth import inputs as I
+
+    class Site:
+        pass
+    sites = []
+    for s in wl.sites:
+        o = Site()
+        o.w_kp, o.base, o.norm_w, o.y = I.to_f64(s.w_kp), s.base.astype(np.float64), I.to_f64(s.norm_w), \
+            I.to_f64(s.y)[blocks]
+        sites.append(o)
+    if wl.w_head is None:
+        return O.conv_chain(I.to_f64(wl.x0)[blocks], sites, wl.eps, wl.gs)
+    if not sites:
+        h = I.to_f64(wl.h)[blocks]
+        logits = O.head_logits(h, I.f64_view(wl.w_head), wl.bias)
+        cand, unary = O.top_k(logits, wl.K)
+        z = O.hidden_projection(h, I.to_f64(wl.w_proj))
+        S = O.score_edges(cand, unary, z, wl.anchors[blocks], I.f64_view(wl.pred_book), I.f64_view(wl.succ_book))
+        return O.select_path(S, cand)
+    return O.block_tail(I.to_f64(wl.x0)[blocks], sites, I.to_f64(wl.final_norm_w), wl.eps, wl.gs,
+                        I.f64_view(wl.w_head), wl.bias, I.to_f64(wl.w_proj), I.f64_view(wl.pred_book),
+                        I.f64_view(wl.succ_book), wl.anchors[blocks], wl.K)
+
+
+def time_oracle(wl, n_blocks, repeats):
+    times = []
+    for r in range(repeats):
+        blocks = [(r * n_blocks + i) % wl.B for i in range(n_blocks)]
+        t0 = time.perf_counter()
+        oracle_block_tail(wl, blocks)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def reference_arm(args, wl_name):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from synth import inputs as I
+    cfg, B = WORKLOADS[wl_name]
+    wl = I.make_config(cfg, B=B)
+    n_blocks = args.ref_blocks
+    for _ in range(args.warmup):
+        time_oracle(wl, n_blocks, 1)
+    times = time_oracle(wl, n_blocks, args.steps)
+    total = sum(times)
+    value = n_blocks * args.steps / total
+    cores = oracle_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl_name, "blocks": B, "G": wl.G, "hidden": wl.H, "vocab": wl.V or None,
+                   "parallelism": "none (host cores)", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n_blocks} block(s) of the {wl_name} workload per step, float64 numpy"},
+        "e2e": {"value": value, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ our arm
+
+def our_arm(args, wl_name):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import dflash2_block_drafter_gb300 as d
+    from dflash2_block_drafter_gb300.tail import TailRunner, to_device, to_pinned
+    from synth import inputs as I
+
+    cfg, B = WORKLOADS[wl_name]
+    wl = I.make_config(cfg, B=B)
+    run = TailRunner(wl, device=dev)
+    full_tail = bool(wl.sites) and run.with_selector
+    x0 = to_device(wl.x0, dev) if wl.x0 is not None else None
+    ys = [to_device(s.y, dev) for s in wl.sites]
+    anchors = to_device(wl.anchors, dev) if wl.anchors is not None else None
+    h_in = to_device(wl.h, dev) if (wl.h is not None and not wl.sites) else None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        if full_tail:
+            run.full(x0, ys, anchors)
+        elif wl.sites:
+            run.conv_chain(x0, ys, emit_h=False)
+        else:
+            run.selector(h_in, anchors)
+
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    head_ev = []
+
+    def timed_step(record_head):
+        """One step between events; the head call also gets its own events."""
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        if record_head and run.with_selector:
+            hs = torch.cuda.Event(enable_timing=True)
+            he = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            if wl.sites:
+                run.conv_chain(x0, ys, emit_h=True)
+                h = run.h
+            else:
+                h = h_in
+            hs.record(stream)
+            M = h.shape[0] * h.shape[1]
+            d.dflash2_head_topk(h.view(M, wl.H), run.w_head, wl.K, bias=run.bias, w_proj=run.w_proj, cand=run.cand,
+                                unary=run.unary, z=run.z, workspace=run.head_ws)
+            he.record(stream)
+            d.dflash2_score_edges(run.cand.view(h.shape[0], wl.steps, wl.K), run.unary.view(h.shape[0], wl.steps, wl.K),
+                                  run.z.view(h.shape[0], wl.steps, wl.R), anchors, run.pred, run.succ, S=run.S,
+                                  path=run.path)
+            e.record(stream)
+            head_ev.append((hs, he))
+        else:
+            s.record(stream)
+            step()
+            e.record(stream)
+        return s, e
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert d.dflash2_poll_error() == 0, "device error word set during warm-up"
+
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    smi_id = visible[torch.cuda.current_device()].strip() if visible and visible[0].strip() else \
+        str(torch.cuda.current_device())
+    sampler = ClockSampler(smi_id)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    evs = []
+    for _ in range(args.steps):
+        flush.zero_()
+        evs.append(timed_step(True))
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in evs]
+    total_ms = sum(step_ms)
+    head_ms = [a.elapsed_time(b) for a, b in head_ev]
+    assert d.dflash2_poll_error() == 0, "device error word set during the timed steps"
+
+    # ---------------------------------------------------------------- e2e: host buffers through the C ABI
+    h_x0 = to_pinned(wl.x0) if x0 is not None else None
+    h_ys = [to_pinned(s.y) for s in wl.sites]
+    h_h = to_pinned(wl.h) if h_in is not None else None
+    h_anchors = to_pinned(wl.anchors) if anchors is not None else None
+    out_dev = run.path if run.with_selector else run.x
+    h_out = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in ([h_x0] if h_x0 is not None else []) + h_ys +
+              ([h_h] if h_h is not None else []) + ([h_anchors] if h_anchors is not None else []))
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        if h_x0 is not None:
+            x0.copy_(h_x0, non_blocking=True)
+        for yd, yh in zip(ys, h_ys):
+            yd.copy_(yh, non_blocking=True)
+        if h_h is not None:
+            h_in.copy_(h_h, non_blocking=True)
+        if h_anchors is not None:
+            anchors.copy_(h_anchors, non_blocking=True)
+        step()
+        h_out.copy_(out_dev, non_blocking=True)
+        e.record(stream)
+        e.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(s.elapsed_time(e))
+    e2e_total = sum(e2e_ms)
+
+    t = torch.tensor([total_ms, e2e_total], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_total = float(t[0]), float(t[1])
+    blocks_total = B * world * args.steps
+    value = blocks_total / (total_ms / 1e3)
+    e2e_value = blocks_total / (e2e_total / 1e3)
+
+    pk = peaks()
+    M = B * wl.steps
+    roofline = None
+    if head_ms:
+        head_avg_s = statistics.mean(head_ms) / 1e3
+        flops = head_flops(M, wl.V, wl.R, wl.H)
+        byts = head_bytes(M, wl.V, wl.R, wl.H, wl.K)
+        tensor_bound = flops / (pk["bf16_tflops_sustained"] * 1e12) > byts / (pk["hbm_gbs"] * 1e9)
+        if tensor_bound:
+            roofline = {"kernel": "tc_gemm_kernel (head GEMM + fused top-16 + z) + topk_merge", "bound": "tensor",
+                        "achieved": flops / head_avg_s / 1e12, "peak": pk["bf16_tflops_sustained"],
+                        "unit": "TFLOP/s", "frac": flops / head_avg_s / 1e12 / pk["bf16_tflops_sustained"],
+                        "traffic": None, "peak_kind": f"bf16 sustained, {pk['source']}",
+                        "algorithmic_per_launch": flops, "avg_launch_ms": head_avg_s * 1e3}
+        else:
+            roofline = {"kernel": "tc_gemm_kernel (head GEMM + fused top-16 + z) + topk_merge", "bound": "hbm",
+                        "achieved": byts / head_avg_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": byts / head_avg_s / 1e9 / pk["hbm_gbs"], "traffic": None,
+                        "peak_kind": f"HBM copy, {pk['source']}", "algorithmic_per_launch": byts,
+                        "avg_launch_ms": head_avg_s * 1e3}
+        traffic = TRAFFIC_PER_LAUNCH.get(wl_name)
+        if traffic is not None:
+            roofline["traffic"] = traffic
+
+    launches = run.launches_per_pass() if full_tail else (
+        (1 + 3 * len(wl.sites)) if wl.sites else 3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl_name, "blocks_per_gpu": B, "G": wl.G, "hidden": wl.H, "conv_sites": len(wl.sites),
+                   "vocab": wl.V or None, "top_k": wl.K or None, "rank": wl.R or None,
+                   "parallelism": f"dp{world} (independent blocks, no collective)",
+                   "l2": "flushed between timed steps (256 MB write) and head weight 2.54 GB > L2"},
+        "rows_per_s": value * (wl.steps if run.with_selector else wl.G),
+        "head_ms": statistics.mean(head_ms) if head_ms else None,
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": "blocks/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_blocks
+        times = time_oracle(wl, n, 1)
+        line["cpu_baseline"] = {"value": n / sum(times), "unit": "blocks/s", "cores": oracle_cores(),
+                                "kind": "oracle",
+                                "sample": f"{n} block(s) of the {wl_name} workload, float64 numpy, one run"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+# per-launch DRAM traffic (bytes) of the head kernel from an ncu capture, by workload; None until
+# measured for the current kernel
+TRAFFIC_PER_LAUNCH = {}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="full-tail-B64", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-blocks", type=int, default=2)
+    ap.add_argument("--ref-blocks", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args, args.workload)
+    return our_arm(args, args.workload)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

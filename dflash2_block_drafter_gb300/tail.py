@@ -84,26 +84,31 @@ class TailRunner:
 
     # ------------------------------------------------------------------ passes
     def conv_chain(self, x0: torch.Tensor, ys: List[torch.Tensor], emit_h: bool):
-        """x <- x0, then every site in order; returns the final residual stream (self.x)."""
+        """Every site in order, starting from x0 (left unchanged); returns the final residual stream (self.x)."""
         wl = self.wl
-        self.x.copy_(x0)
         nsites = len(self.sites)
         for i, s in enumerate(self.sites):
             if i == 0:
-                dflash2_conv_prepare(self.x, s.norm_w, wl.eps, s.w_kp, s.base, wl.gs, out=self.a, coef1=self.coef1,
+                dflash2_conv_prepare(x0, s.norm_w, wl.eps, s.w_kp, s.base, wl.gs, out=self.a, coef1=self.coef1,
                                      workspace=self.conv_ws)
             else:
                 dflash2_conv_prepare(self.n, None, wl.eps, s.w_kp, s.base, wl.gs, out=self.a, coef1=self.coef1,
                                      workspace=self.conv_ws)
+            residual = x0 if i == 0 else self.x
             if i + 1 < nsites:
-                dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=self.x, out=self.x,
+                dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=residual, out=self.x,
                                     next_norm_w=self.sites[i + 1].norm_w, eps=wl.eps, next_n=self.n, next_row0=0)
             elif emit_h:
-                dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=self.x, out=self.x,
+                dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=residual, out=self.x,
                                     next_norm_w=self.final_norm_w, eps=wl.eps, next_n=self.h, next_row0=1)
             else:
-                dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=self.x, out=self.x)
+                dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=residual, out=self.x)
         return self.x
+
+    def launches_per_pass(self) -> int:
+        """Library kernels one full() pass launches: RMSNorm once, per site a GEMM + side-0 pass and a
+        side-1 pass, then the head GEMM + merge and the fused edge-score/walk kernel."""
+        return 1 + 3 * len(self.sites) + (3 if self.with_selector else 0)
 
     def selector(self, h: torch.Tensor, anchors: torch.Tensor, want_S: bool = True):
         wl = self.wl
