@@ -328,13 +328,9 @@ def our_arm(args, wl_name):
             e2e_ms.append(s.elapsed_time(e))
     e2e_total = sum(e2e_ms)
 
-    t = torch.tensor([total_ms, e2e_total], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_total = float(t[0]), float(t[1])
-    blocks_total = B * world * args.steps
-    value = blocks_total / (total_ms / 1e3)
-    e2e_value = blocks_total / (e2e_total / 1e3)
+    from dflash2_block_drafter_gb300.dist import aggregate_throughput
+    value, _, total_ms = aggregate_throughput(B * args.steps, total_ms, device=dev)
+    e2e_value, _, e2e_total = aggregate_throughput(B * args.steps, e2e_total, device=dev)
 
     pk = peaks()
     M = B * wl.steps
