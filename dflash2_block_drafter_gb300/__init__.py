@@ -20,7 +20,7 @@ __all__ = [
     "Dflash2Error", "library", "library_path", "dflash2_version", "dflash2_poll_error",
     "dflash2_conv_prepare_workspace_bytes", "dflash2_conv_prepare", "dflash2_conv_finish",
     "dflash2_head_topk_workspace_bytes", "dflash2_head_topk", "dflash2_score_edges",
-    "dflash2_select_path", "dflash2_selftest_bounded_wait", "DTYPE_CODES",
+    "dflash2_select_path", "dflash2_selftest_bounded_wait", "dflash2_head_topk_noalloc", "DTYPE_CODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -47,6 +47,7 @@ _SIGNATURES = {
     "dflash2_score_edges": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp]),
     "dflash2_select_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "dflash2_selftest_bounded_wait": (_i, [_i, _vp]),
+    "dflash2_head_topk_noalloc": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
 }
 
 
@@ -216,3 +217,31 @@ def dflash2_select_path(S, cand, path=None, stream=None):
 
 def dflash2_selftest_bounded_wait(limit_us: int, stream=None):
     _check(library().dflash2_selftest_bounded_wait(limit_us, _stream(stream)))
+
+
+def dflash2_head_topk_noalloc(h, w_head, K, bias=None, w_proj=None, cand=None, unary=None, z=None, logits=None,
+                              want_logits=False, stream=None):
+    """dflash2_head_topk with its scratch in the library's fixed device array instead of a workspace.
+
+    For callers that cannot allocate device memory while the head runs (inside a graph capture, a
+    serving loop, or a host that only passes input and output buffers). Outputs not passed in are
+    still allocated here by torch for convenience; pass them all to allocate nothing. Calls that
+    overlap on the GPU share the array and race; keep them on one stream.
+    """
+    M, H = h.shape
+    V = w_head.shape[0]
+    R = w_proj.shape[0] if w_proj is not None else 0
+    dt = h.dtype
+    dev = h.device
+    cand = torch.empty((M, K), dtype=torch.int32, device=dev) if cand is None else cand
+    unary = torch.empty((M, K), dtype=torch.float32, device=dev) if unary is None else unary
+    if w_proj is not None and z is None:
+        z = torch.empty((M, R), dtype=torch.float32, device=dev)
+    if want_logits and logits is None:
+        logits = torch.empty((M, V), dtype=torch.float32, device=dev)
+    _check(library().dflash2_head_topk_noalloc(
+        _dev(h, "h", dt), M, H, _dev(w_head, "w_head", dt), V, _dev(bias, "bias", torch.float32, True),
+        _dev(w_proj, "w_proj", dt, True), R, K, _code(h), _dev(cand, "cand", torch.int32),
+        _dev(unary, "unary", torch.float32), _dev(z, "z", torch.float32, True),
+        _dev(logits, "logits", torch.float32, True), _stream(stream)))
+    return cand, unary, z, logits

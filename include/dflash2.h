@@ -160,6 +160,25 @@ DFLASH2_API int dflash2_head_topk(const void* h, int M, int H, const void* w_hea
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Allocation-free variant of dflash2_head_topk. The pages describe no counterpart: this entry
+ * point exists for callers that cannot allocate device memory when they run the head — code
+ * inside a CUDA-graph capture or a latency-bound serving loop where cudaMalloc would stall or break
+ * the capture, host runtimes without a CUDA-aware allocator, and plug-in hosts that only hand over
+ * the input and output buffers. Arguments and results are those of dflash2_head_topk without the
+ * workspace: the top-K scratch lives in a fixed 8 MiB device array inside the library, held on
+ * every device that loads the library until the process exits.
+ *  - Calls whose scratch would exceed 8 MiB are rejected with DFLASH2_ERR_INVALID_ARG (960 rows
+ *    need about 4.7 MB on a 152-SM GB300).
+ *  - All calls on a device share the array and it keeps the last call's contents; nothing in it
+ *    needs to start at zero. Calls that overlap on the GPU race on it: keep them on one stream.
+ *  - The first call on a device looks up the array's address; make it before any stream capture.
+ *  - Never calls cudaMalloc, cudaFree or any allocating library routine.
+ * ---------------------------------------------------------------------------------- */
+DFLASH2_API int dflash2_head_topk_noalloc(const void* h, int M, int H, const void* w_head, int V, const float* bias,
+                                          const void* w_proj, int R, int K, int dtype, int32_t* cand, float* unary,
+                                          float* z, float* logits, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Edge scores, optionally fused with the greedy walk (MAX DFlash2CandidateSelector.score_edges
  * and select_path; dflash2.ts #select).
  *
