@@ -22,6 +22,10 @@ namespace cg = cooperative_groups;
 namespace dfl {
 namespace {
 
+constexpr int kApplyThreads = 128;            // threads per apply CTA (8 channels each)
+constexpr int kSlabCh = kApplyThreads * 8;    // channels per prepare CTA
+constexpr int kRowChunk = 4;                  // rows loaded ahead of the arithmetic
+
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -88,73 +92,108 @@ __global__ void __launch_bounds__(128) rmsnorm_kernel(const T* __restrict__ x, c
 
 // prepare's apply pass: out = side-0 conv of n; coef1 = side 1's deltas (no base); d_full = D.
 // part: [k_splits][B*G][4*groups] fp32 split-K partial sums of D, column (side*2+tap)*groups + g.
+// One CTA per (block, slab of 1024 channels). The block's D values for the slab's groups are
+// summed over the splits into shared memory first (coalesced along the group axis); then each
+// thread walks the block's rows for its 8 channels, loading four rows ahead of the arithmetic.
 template <typename T>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kApplyThreads)
     conv_side0_kernel(const T* __restrict__ n, const float* __restrict__ part, int k_splits,
                       const float* __restrict__ base, T* __restrict__ out, T* __restrict__ coef1,
                       float* __restrict__ d_full, int B, int G, int H, int gs, int groups) {
+  extern __shared__ float sD[];  // [G][4][gsl]
   const int b = blockIdx.y;
-  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
-  if (c >= H) return;
-  const int g = c / gs;
-  const bool leader = (c % gs) == 0;
+  const int c0 = blockIdx.x * kSlabCh;
+  const int cend = min(H, c0 + kSlabCh);
+  const int g0 = c0 / gs;
+  const int gsl = (cend - 1) / gs + 1 - g0;
   const int N = 4 * groups;
-  const int M = B * G;
+  const size_t MN = static_cast<size_t>(B) * G * N;
+  const size_t row0 = static_cast<size_t>(b) * G;
+  for (int i = threadIdx.x; i < G * 4 * gsl; i += kApplyThreads) {
+    const int g = i % gsl;
+    const int tk = i / gsl;
+    const float* p = part + (row0 + (tk >> 2)) * N + (tk & 3) * groups + g0 + g;
+    float acc = 0.f;
+    for (int s = 0; s < k_splits; ++s) acc += __ldg(p + s * MN);
+    sD[i] = acc;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * 2 * gsl; i += kApplyThreads) {
+    const int g = i % gsl;
+    const int tt = i / gsl;  // t*2 + tap
+    store1(coef1 + (row0 * 2 + tt) * groups + g0 + g, sD[((tt >> 1) * 4 + 2 + (tt & 1)) * gsl + g]);
+  }
+  if (d_full != nullptr) {
+    for (int i = threadIdx.x; i < G * 4 * gsl; i += kApplyThreads) {
+      const int g = i % gsl;
+      const int tk = i / gsl;
+      d_full[(row0 + (tk >> 2)) * N + (tk & 3) * groups + g0 + g] = sD[i];
+    }
+  }
+  const int c = c0 + threadIdx.x * 8;
+  if (c >= H) return;
+  const int gl = c / gs - g0;
   float b0[8], b1[8], prev[8];
-  load8(base + c, b0);          // base[0][0][c..]
-  load8(base + H + c, b1);      // base[0][1][c..]
+  load8(base + c, b0);      // base[0][0][c..]
+  load8(base + H + c, b1);  // base[0][1][c..]
 #pragma unroll
   for (int i = 0; i < 8; ++i) prev[i] = 0.f;
-  for (int t = 0; t < G; ++t) {
-    const int row = b * G + t;
-    float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-    for (int s = 0; s < k_splits; ++s) {
-      const float* pr = part + (static_cast<size_t>(s) * M + row) * N + g;
-      d0 += __ldg(pr);
-      d1 += __ldg(pr + groups);
-      d2 += __ldg(pr + 2 * groups);
-      d3 += __ldg(pr + 3 * groups);
-    }
-    float cur[8], o[8];
-    load8(n + static_cast<size_t>(row) * H + c, cur);
+  const T* np = n + row0 * H + c;
+  T* op = out + row0 * H + c;
+  for (int t0 = 0; t0 < G; t0 += kRowChunk) {
+    float cur[kRowChunk][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      o[i] = (b0[i] + d0) * cur[i] + (b1[i] + d1) * prev[i];
-      prev[i] = cur[i];
-    }
-    store8(out + static_cast<size_t>(row) * H + c, o);
-    if (leader) {
-      store1(coef1 + (static_cast<size_t>(row) * 2 + 0) * groups + g, d2);
-      store1(coef1 + (static_cast<size_t>(row) * 2 + 1) * groups + g, d3);
-      if (d_full != nullptr) {
-        float* df = d_full + static_cast<size_t>(row) * N + g;
-        df[0] = d0;
-        df[groups] = d1;
-        df[2 * groups] = d2;
-        df[3 * groups] = d3;
+    for (int j = 0; j < kRowChunk; ++j)
+      if (t0 + j < G) load8(np + static_cast<size_t>(t0 + j) * H, cur[j]);
+#pragma unroll
+    for (int j = 0; j < kRowChunk; ++j) {
+      const int t = t0 + j;
+      if (t < G) {
+        const float d0 = sD[(t * 4 + 0) * gsl + gl];
+        const float d1 = sD[(t * 4 + 1) * gsl + gl];
+        float o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[i] = (b0[i] + d0) * cur[j][i] + (b1[i] + d1) * prev[i];
+          prev[i] = cur[j][i];
+        }
+        store8(op + static_cast<size_t>(t) * H, o);
       }
     }
   }
 }
 
 // finish's apply pass: out = residual + side-1 conv of y (fp32 add, one rounding); optionally
-// next_n = rms(out) * next_w over rows [next_row0, G). With NORM the grid is one cluster per
-// block (cluster = gridDim.x CTAs) and the per-row sums of squares meet in DSMEM.
+// next_n = rms(out) * next_w over rows [next_row0, G). The block's side-1 deltas for the CTA's
+// groups are staged in shared memory first; rows are processed four at a time, loads first. With
+// NORM the grid is one cluster per block (cluster = gridDim.x CTAs) and the per-row sums of
+// squares meet through distributed shared memory.
 template <typename T, bool NORM>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kApplyThreads)
     conv_side1_kernel(const T* __restrict__ y, const T* __restrict__ coef1, const float* __restrict__ base,
                       const T* residual, T* out, const T* __restrict__ next_w, float eps, T* __restrict__ next_n,
                       int next_row0, int G, int H, int gs, int groups) {
+  extern __shared__ float sC[];  // [G][2][gsl]
   __shared__ float row_ss[64];
+  __shared__ float row_r[64];
   const int b = blockIdx.y;
-  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  const int c0 = blockIdx.x * blockDim.x * 8;
+  const int cend = min(H, c0 + static_cast<int>(blockDim.x) * 8);
+  const int g0 = c0 / gs;
+  const int gsl = (cend - 1) / gs + 1 - g0;
+  const size_t row0 = static_cast<size_t>(b) * G;
+  const int c = c0 + threadIdx.x * 8;
   const bool active = c < H;
   const int lane = threadIdx.x & 31;
-  if (NORM) {
-    for (int i = threadIdx.x; i < 64; i += blockDim.x) row_ss[i] = 0.f;
-    __syncthreads();
+  for (int i = threadIdx.x; i < G * 2 * gsl; i += blockDim.x) {
+    const int g = i % gsl;
+    const int tt = i / gsl;  // t*2 + tap
+    sC[i] = load1(coef1 + (row0 * 2 + tt) * groups + g0 + g);
   }
-  const int g = active ? c / gs : 0;
+  if (NORM)
+    for (int i = threadIdx.x; i < 64; i += blockDim.x) row_ss[i] = 0.f;
+  __syncthreads();
+  const int gl = active ? c / gs - g0 : 0;
   float b0[8], b1[8], prev[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -166,45 +205,52 @@ __global__ void __launch_bounds__(128)
     load8(base + 2 * H + c, b0);  // base[1][0][c..]
     load8(base + 3 * H + c, b1);  // base[1][1][c..]
   }
-  for (int t = 0; t < G; ++t) {
-    const size_t row = static_cast<size_t>(b) * G + t;
-    float ss = 0.f;
+  for (int t0 = 0; t0 < G; t0 += kRowChunk) {
+    float cur[kRowChunk][8], res[kRowChunk][8];
     if (active) {
-      const float d0 = load1(coef1 + (row * 2 + 0) * groups + g);
-      const float d1 = load1(coef1 + (row * 2 + 1) * groups + g);
-      float cur[8], o[8];
-      load8(y + row * H + c, cur);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        o[i] = (b0[i] + d0) * cur[i] + (b1[i] + d1) * prev[i];
-        prev[i] = cur[i];
-      }
-      if (residual != nullptr) {
-        float r[8];
-        load8(residual + row * H + c, r);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] += r[i];
-      }
-      store8(out + row * H + c, o);
-      if (NORM) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float sv = stored(o[i], out);
-          ss = fmaf(sv, sv, ss);
+      for (int j = 0; j < kRowChunk; ++j) {
+        if (t0 + j < G) {
+          load8(y + (row0 + t0 + j) * H + c, cur[j]);
+          if (residual != nullptr) load8(residual + (row0 + t0 + j) * H + c, res[j]);
         }
       }
     }
-    if (NORM && t >= next_row0) {  // every thread of the CTA takes part (inactive ones add 0)
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      if (lane == 0) atomicAdd(&row_ss[t], ss);
+    for (int j = 0; j < kRowChunk; ++j) {
+      const int t = t0 + j;
+      if (t >= G) break;
+      float ss = 0.f;
+      if (active) {
+        const float d0 = sC[(t * 2 + 0) * gsl + gl];
+        const float d1 = sC[(t * 2 + 1) * gsl + gl];
+        float o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[i] = (b0[i] + d0) * cur[j][i] + (b1[i] + d1) * prev[i];
+          prev[i] = cur[j][i];
+          if (residual != nullptr) o[i] += res[j][i];
+        }
+        store8(out + (row0 + t) * H + c, o);
+        if (NORM) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float sv = stored(o[i], out);
+            ss = fmaf(sv, sv, ss);
+          }
+        }
+      }
+      if (NORM && t >= next_row0) {  // every thread of the CTA takes part (inactive ones add 0)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) atomicAdd(&row_ss[t], ss);
+      }
     }
   }
   if (!NORM) return;
   cg::cluster_group cluster = cg::this_cluster();
   __syncthreads();
   cluster.sync();
-  __shared__ float row_r[64];
   const int ranks = static_cast<int>(cluster.num_blocks());
   for (int t = threadIdx.x; t < G; t += blockDim.x) {
     float tot = 0.f;
@@ -217,14 +263,21 @@ __global__ void __launch_bounds__(128)
   float w[8];
   load8(next_w + c, w);
   const int rows_out = G - next_row0;
-  for (int t = next_row0; t < G; ++t) {
-    const size_t row = static_cast<size_t>(b) * G + t;
-    float o[8];
-    load8(out + row * H + c, o);
-    const float r = row_r[t];
+  for (int t0 = next_row0; t0 < G; t0 += kRowChunk) {
+    float o[kRowChunk][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = o[i] * r * w[i];
-    store8(next_n + (static_cast<size_t>(b) * rows_out + (t - next_row0)) * H + c, o);
+    for (int j = 0; j < kRowChunk; ++j)
+      if (t0 + j < G) load8(out + (row0 + t0 + j) * H + c, o[j]);
+#pragma unroll
+    for (int j = 0; j < kRowChunk; ++j) {
+      const int t = t0 + j;
+      if (t < G) {
+        const float r = row_r[t];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[j][i] = o[j][i] * r * w[i];
+        store8(next_n + (static_cast<size_t>(b) * rows_out + (t - next_row0)) * H + c, o[j]);
+      }
+    }
   }
 }
 
@@ -277,19 +330,37 @@ int launch_rmsnorm(const void* x, const void* w, float eps, void* n, int rows, i
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "rmsnorm launch failed: %s", cudaGetErrorString(e));
 }
 
+// Largest number of groups one slab of `slab_ch` channels touches.
+static int slab_groups(int H, int gs, int slab_ch) {
+  int best = 0;
+  for (int c0 = 0; c0 < H; c0 += slab_ch) {
+    const int cend = std::min(H, c0 + slab_ch);
+    best = std::max(best, (cend - 1) / gs + 1 - c0 / gs);
+  }
+  return best;
+}
+
+// Upper bound of the apply passes' dynamic shared memory: G <= 64 rows x 4 deltas x 129 groups.
+constexpr int kApplySmemMax = 64 * 4 * 129 * 4;
+
 int launch_conv_side0(const ConvShape& s, const void* n, const float* part, int k_splits, const float* base,
                       void* out, void* coef1, float* d_full, cudaStream_t st) {
-  int threads, ctas;
-  apply_geometry(s.H, &threads, &ctas);
-  const dim3 grid(ctas, s.B);
-  if (s.dtype == DFLASH2_F32)
-    conv_side0_kernel<float><<<grid, threads, 0, st>>>(static_cast<const float*>(n), part, k_splits, base,
-                                                       static_cast<float*>(out), static_cast<float*>(coef1), d_full,
-                                                       s.B, s.G, s.H, s.gs, s.groups);
-  else
-    conv_side0_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
+  const dim3 grid((s.H + kSlabCh - 1) / kSlabCh, s.B);
+  const size_t smem = sizeof(float) * s.G * 4 * slab_groups(s.H, s.gs, kSlabCh);
+  static unsigned done_f32 = 0, done_bf16 = 0;
+  if (s.dtype == DFLASH2_F32) {
+    if (!ensure_smem_attr(conv_side0_kernel<float>, kApplySmemMax, &done_f32))
+      return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed (side0)");
+    conv_side0_kernel<float><<<grid, kApplyThreads, smem, st>>>(static_cast<const float*>(n), part, k_splits, base,
+                                                                static_cast<float*>(out), static_cast<float*>(coef1),
+                                                                d_full, s.B, s.G, s.H, s.gs, s.groups);
+  } else {
+    if (!ensure_smem_attr(conv_side0_kernel<__nv_bfloat16>, kApplySmemMax, &done_bf16))
+      return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed (side0)");
+    conv_side0_kernel<__nv_bfloat16><<<grid, kApplyThreads, smem, st>>>(
         static_cast<const __nv_bfloat16*>(n), part, k_splits, base, static_cast<__nv_bfloat16*>(out),
         static_cast<__nv_bfloat16*>(coef1), d_full, s.B, s.G, s.H, s.gs, s.groups);
+  }
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "conv side0 launch failed: %s", cudaGetErrorString(e));
 }
@@ -300,18 +371,23 @@ static int side1_typed(const ConvShape& s, const void* y, const void* coef1, con
   int threads, ctas;
   apply_geometry(s.H, &threads, &ctas);
   const dim3 grid(ctas, s.B);
+  const size_t smem = sizeof(float) * s.G * 2 * slab_groups(s.H, s.gs, threads * 8);
+  static unsigned done_plain = 0, done_norm = 0;
+  if (!ensure_smem_attr(conv_side1_kernel<T, false>, kApplySmemMax, &done_plain) ||
+      !ensure_smem_attr(conv_side1_kernel<T, true>, kApplySmemMax, &done_norm))
+    return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed (side1)");
   const T* yp = static_cast<const T*>(y);
   const T* cp = static_cast<const T*>(coef1);
   const T* rp = static_cast<const T*>(residual);
   T* op = static_cast<T*>(out);
   if (next_n == nullptr) {
-    conv_side1_kernel<T, false><<<grid, threads, 0, st>>>(yp, cp, base, rp, op, nullptr, eps, nullptr, 0, s.G, s.H,
-                                                          s.gs, s.groups);
+    conv_side1_kernel<T, false><<<grid, threads, smem, st>>>(yp, cp, base, rp, op, nullptr, eps, nullptr, 0, s.G,
+                                                             s.H, s.gs, s.groups);
   } else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
