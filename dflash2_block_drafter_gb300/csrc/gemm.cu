@@ -76,33 +76,6 @@ __device__ __forceinline__ bool next_tile(int& c, int c_end, int main_chunks, in
   return true;
 }
 
-// The (tile, k-block) steps of a CTA's work in load order; the producer runs a second cursor ahead
-// of its loads to prefetch weight chunks into L2.
-struct StepCursor {
-  int c, c_end, main_chunks, kb0, kb1, t0, nch, kb;
-  bool valid;
-  __device__ __forceinline__ void init(int c_begin, int c_end_, int main_, int kb0_, int kb1_) {
-    c = c_begin;
-    c_end = c_end_;
-    main_chunks = main_;
-    kb0 = kb0_;
-    kb1 = kb1_;
-    t0 = 0;
-    nch = 0;
-    valid = kb0 < kb1 && next_tile(c, c_end, main_chunks, t0, nch);
-    kb = kb0;
-  }
-  __device__ __forceinline__ void advance() {
-    if (!valid) return;
-    if (++kb == kb1) {
-      kb = kb0;
-      valid = next_tile(c, c_end, main_chunks, t0, nch);
-    }
-  }
-};
-
-constexpr int kPrefetchSteps = 8;  // k-blocks of weight chunks requested into L2 ahead of their TMA load
-
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* err) {
   *abort_flag = 1;
   if (err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_TIMEOUT));
@@ -196,25 +169,9 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      // Weight chunks go to L2 kPrefetchSteps k-blocks ahead, so that the TMA loads of the smem
-      // ring see L2 latency rather than DRAM latency. Each chunk is requested by one of the CTAs
-      // that share it (those with the same column range and different row groups).
-      StepCursor pf;
-      pf.init(c_begin, c_end, a.main_chunks, kb0, kb1);
-      auto prefetch_step = [&]() {
-        if (!pf.valid) return;
-        const int kx = pf.kb * (TF32 ? 32 : 64);
-        for (int j = 0; j < pf.nch; ++j) {
-          const int ch = pf.t0 + j;
-          if (ch < a.main_chunks && ch % a.m_groups == mg) tma_prefetch_l2_2d(&tmB, kx, ch * kChunk);
-        }
-        pf.advance();
-      };
-      for (int i = 0; i < kPrefetchSteps; ++i) prefetch_step();
       int c = c_begin, t0 = 0, nch = 0;
       while (ok && next_tile(c, c_end, a.main_chunks, t0, nch)) {
         for (int kb = kb0; kb < kb1; ++kb) {
-          prefetch_step();
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
@@ -363,32 +320,16 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
             }
           } else {
             float v[32];
-            if (col0 + 32 <= a.n_main) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-              if (a.bias != nullptr) {
-                const float4* bp = reinterpret_cast<const float4*>(a.bias + col0);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  const float4 b4 = __ldg(bp + q);
-                  v[4 * q] += b4.x;
-                  v[4 * q + 1] += b4.y;
-                  v[4 * q + 2] += b4.z;
-                  v[4 * q + 3] += b4.w;
-                }
+            for (int j = 0; j < 32; ++j) {
+              const int id = col0 + j;
+              float x = __uint_as_float(r[j]);
+              if (id < a.n_main) {
+                if (a.bias != nullptr) x += __ldg(a.bias + id);
+              } else {
+                x = -INFINITY;
               }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int id = col0 + j;
-                float x = __uint_as_float(r[j]);
-                if (id < a.n_main) {
-                  if (a.bias != nullptr) x += __ldg(a.bias + id);
-                } else {
-                  x = -INFINITY;
-                }
-                v[j] = x;
-              }
+              v[j] = x;
             }
             if (a.logits != nullptr && valid) {
               float* dst = a.logits + static_cast<size_t>(row) * a.n_main;
