@@ -185,7 +185,8 @@ int dflash2_head_topk(const void* h, int M, int H, const void* w_head, int V, co
   REQUIRE(h && w_head && cand && unary && workspace, "a required pointer is NULL");
   REQUIRE((w_proj == nullptr) == (z == nullptr), "w_proj and z must be both set or both NULL");
   if (w_proj != nullptr) REQUIRE(R >= 16 && R <= 256 && R % 16 == 0, "R=%d must be a multiple of 16 in [16, 256]", R);
-  REQUIRE(aligned16(h) && aligned16(w_head) && (!w_proj || aligned16(w_proj)), "h, w_head, w_proj must be 16-byte aligned");
+  REQUIRE(aligned16(h) && aligned16(w_head) && (!w_proj || aligned16(w_proj)) && (!bias || aligned16(bias)),
+          "h, w_head, w_proj and bias must be 16-byte aligned");
   REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "workspace must be 256-byte aligned");
   const int r_eff = w_proj != nullptr ? R : 0;
   const int sms = sm_count();

@@ -27,17 +27,25 @@
 namespace dfl {
 namespace {
 
+// Bytes of K per operand row in one pipeline stage: 128 (128-byte swizzle) or 64 (64-byte
+// swizzle, half-size stages, twice as many of them).
+#ifndef DFL_GEMM_ROW_BYTES
+#define DFL_GEMM_ROW_BYTES 128
+#endif
+constexpr int kRowBytes = DFL_GEMM_ROW_BYTES;
+static_assert(kRowBytes == 128 || kRowBytes == 64, "row bytes per stage must be 64 or 128");
+constexpr int kKSteps = kRowBytes / 32;            // 32-byte UMMA K steps per stage
 constexpr int kChunk = 64;                         // W rows per TMA box (one column chunk)
 constexpr int kMaxTileChunks = 4;                  // 256 accumulator columns per tile
-constexpr int kATile = 128 * 128;                  // bytes of one 128-row x 128-byte A tile
-constexpr int kBChunkBytes = kChunk * 128;         // 8 KB
-constexpr int kBTile = kMaxTileChunks * kBChunkBytes;  // 32 KB
+constexpr int kATile = 128 * kRowBytes;            // one 128-row A tile
+constexpr int kBChunkBytes = kChunk * kRowBytes;   // one 64-row W chunk
+constexpr int kBTile = kMaxTileChunks * kBChunkBytes;
 constexpr int kTopL = 16;                          // list length kept per row
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms
+constexpr int kSmemLimit = 232448;
 
 template <int MT>
 struct Cfg {
-  static constexpr int kStages = (MT == 1) ? 4 : 3;
   static constexpr int kStageBytes = MT * kATile + kBTile;
   static constexpr int kEpiWarps = 4 * MT;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
@@ -45,10 +53,12 @@ struct Cfg {
   static constexpr int kTmemCols = 256 * MT;
   static constexpr int kBarBytes = 256;
   static constexpr int kListBytes = kEpiThreads * kTopL * 8;
+  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes - kListBytes) / kStageBytes;
+  static constexpr int kStages = kFit > 8 ? 8 : kFit;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kListBytes;
 };
-static_assert(Cfg<2>::kSmem <= 232448, "shared memory budget");
-static_assert(Cfg<1>::kSmem <= 232448, "shared memory budget");
+static_assert(Cfg<2>::kStages >= 2 && Cfg<2>::kSmem <= kSmemLimit, "shared memory budget");
+static_assert(Cfg<1>::kStages >= 2 && Cfg<1>::kSmem <= kSmemLimit, "shared memory budget");
 
 struct GemmArgs {
   int M, K;
@@ -180,7 +190,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
           mbar_arrive_expect_tx(fb, static_cast<uint32_t>(mt_valid * kATile + nch * kBChunkBytes));
           uint8_t* sa = smem + stage * C::kStageBytes;
           uint8_t* sb = sa + MT * kATile;
-          const int kx = kb * (TF32 ? 32 : 64);
+          const int kx = kb * (kRowBytes / (TF32 ? 4 : 2));
           for (int mt = 0; mt < mt_valid; ++mt)
             tma_load_2d(smem_u32(sa + mt * kATile), &tmA, fb, kx, row0 + mt * 128, pol_keep);
           for (int j = 0; j < nch; ++j) {
@@ -236,11 +246,11 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
-          const uint64_t bdesc = desc_kmajor_sw128(sa + MT * kATile);
+          const uint64_t bdesc = desc_kmajor_swizzled<kRowBytes>(sa + MT * kATile);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte swizzle row
+          for (int k = 0; k < kKSteps; ++k) {  // 32-byte K steps along the swizzled row
             for (int mt = 0; mt < mt_valid; ++mt) {
-              const uint64_t adesc = desc_kmajor_sw128(sa + mt * kATile) + static_cast<uint64_t>(2 * k);
+              const uint64_t adesc = desc_kmajor_swizzled<kRowBytes>(sa + mt * kATile) + static_cast<uint64_t>(2 * k);
               const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
               if (TF32)
                 mma_tf32(tmem_base + static_cast<uint32_t>(mt * 256), adesc, bdesc + static_cast<uint64_t>(2 * k),
@@ -320,16 +330,32 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
             }
           } else {
             float v[32];
+            if (col0 + 32 <= a.n_main) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int id = col0 + j;
-              float x = __uint_as_float(r[j]);
-              if (id < a.n_main) {
-                if (a.bias != nullptr) x += __ldg(a.bias + id);
-              } else {
-                x = -INFINITY;
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+              if (a.bias != nullptr) {
+                const float4* bp = reinterpret_cast<const float4*>(a.bias + col0);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const float4 b4 = __ldg(bp + q);
+                  v[4 * q] += b4.x;
+                  v[4 * q + 1] += b4.y;
+                  v[4 * q + 2] += b4.z;
+                  v[4 * q + 3] += b4.w;
+                }
               }
-              v[j] = x;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int id = col0 + j;
+                float x = __uint_as_float(r[j]);
+                if (id < a.n_main) {
+                  if (a.bias != nullptr) x += __ldg(a.bias + id);
+                } else {
+                  x = -INFINITY;
+                }
+                v[j] = x;
+              }
             }
             if (a.logits != nullptr && valid) {
               float* dst = a.logits + static_cast<size_t>(row) * a.n_main;
@@ -471,18 +497,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major [rows, cols] operand, box = 128 bytes of K x box_rows rows, 128-byte swizzle.
+// Row-major [rows, cols] operand, box = kRowBytes of K x box_rows rows, swizzled to match.
 bool make_map(CUtensorMap* m, const void* ptr, int dtype, int rows, int cols, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const int es = dtype == DFLASH2_F32 ? 4 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * es};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kRowBytes / es), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(m, dtype == DFLASH2_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                          2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         kRowBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -519,7 +546,7 @@ int prepare_args(const GemmProblem& p, const GemmPlan& plan, CUtensorMap* mA, CU
   } else {
     *mE = *mB;
   }
-  const int bk = p.dtype == DFLASH2_F32 ? 32 : 64;
+  const int bk = kRowBytes / (p.dtype == DFLASH2_F32 ? 4 : 2);
   GemmArgs& a = *args;
   a = GemmArgs{};
   a.M = p.M;

@@ -73,9 +73,9 @@ extern "C" int dflash2_head_topk_noalloc(const void* h, int M, int H, const void
     return fail(DFLASH2_ERR_INVALID_ARG, "w_proj and z must be both set or both NULL");
   if (w_proj != nullptr && (R < 16 || R > 256 || R % 16 != 0))
     return fail(DFLASH2_ERR_INVALID_ARG, "R=%d must be a multiple of 16 in [16, 256]", R);
-  if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(w_head) |
-       reinterpret_cast<uintptr_t>(w_proj)) & 15u)
-    return fail(DFLASH2_ERR_INVALID_ARG, "h, w_head, w_proj must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(w_head) | reinterpret_cast<uintptr_t>(w_proj) |
+       reinterpret_cast<uintptr_t>(bias)) & 15u)
+    return fail(DFLASH2_ERR_INVALID_ARG, "h, w_head, w_proj and bias must be 16-byte aligned");
   const int r_eff = w_proj != nullptr ? R : 0;
   const int sms = sm_count();
   const size_t need = head_workspace(M, V, K, r_eff, sms);

@@ -155,6 +155,16 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
          (static_cast<uint64_t>(2) << 61);
 }
 
+// The same for 64-byte (RB = 64) or 128-byte (RB = 128) swizzled rows: stride byte offset
+// = 8 rows * RB, swizzle mode 4 (64B) or 2 (128B).
+template <int RB>
+__device__ __forceinline__ uint64_t desc_kmajor_swizzled(uint32_t saddr) {
+  static_assert(RB == 64 || RB == 128, "swizzle row bytes");
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>((8 * RB) >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(RB == 128 ? 2 : 4) << 61);
+}
+
 // Instruction descriptor: fp32 accumulator (bits 4-5 = 1), A/B format (bits 7-9, 10-12:
 // 1 = bf16 for kind::f16, 2 = tf32 for kind::tf32), both K-major (bits 15, 16 = 0),
 // N >> 3 (bits 17-22), M >> 4 (bits 24-28).

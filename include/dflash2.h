@@ -131,7 +131,7 @@ DFLASH2_API int dflash2_conv_prepare(const void* x, const void* norm_w, float ep
  *             t in [next_row0, G), i.e. a [B, G - next_row0, H] tensor. next_row0 = 0 feeds
  *             the next conv site's prepare (norm_w = NULL); next_row0 = 1 with the final
  *             norm gives the head's input h (rows 1..G-1, dflash2.ts #block).
- *             Requires H / 8 <= 1024 (the row reduction runs in one thread-block cluster).
+ *             Requires H <= 8192 (one thread per 8 channels of a row reduces the row).
  * ---------------------------------------------------------------------------------- */
 DFLASH2_API int dflash2_conv_finish(const void* y, const void* coef1, const float* base, int B, int G, int H,
                         int group_size, int taps, int dtype, const void* residual, void* out,
