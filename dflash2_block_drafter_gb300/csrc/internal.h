@@ -7,7 +7,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/dflash2.h"
+#include "dflash2.h"
 
 namespace dfl {
 
