@@ -52,10 +52,9 @@ struct Cfg {
   static constexpr int kThreads = 64 + kEpiThreads;
   static constexpr int kTmemCols = 256 * MT;
   static constexpr int kBarBytes = 256;
-  static constexpr int kListBytes = kEpiThreads * kTopL * 8;
-  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes - kListBytes) / kStageBytes;
+  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kListBytes;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
 };
 static_assert(Cfg<2>::kStages >= 2 && Cfg<2>::kSmem <= kSmemLimit, "shared memory budget");
 static_assert(Cfg<1>::kStages >= 2 && Cfg<1>::kSmem <= kSmemLimit, "shared memory budget");
@@ -91,19 +90,20 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* err) 
   if (err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_TIMEOUT));
 }
 
-// Insert (v, id) into a descending list held in shared memory (stride ne between entries);
-// equal values stay behind earlier (lower-id) entries.
-__device__ __forceinline__ void list_insert(float* lv, int* li, int et, int ne, float v, int id) {
-  int pos = kTopL - 1;
-  while (pos > 0) {
-    const float pv = lv[(pos - 1) * ne + et];
-    if (!(v > pv)) break;
-    lv[pos * ne + et] = pv;
-    li[pos * ne + et] = li[(pos - 1) * ne + et];
-    --pos;
+// Insert (x, id) into a descending 16-entry list held in registers, dropping the last entry.
+// Branch-free and fully unrolled; equal values stay behind earlier (lower-id) entries.
+__device__ __forceinline__ void list_insert(float (&tv)[kTopL], int (&ti)[kTopL], float x, int id) {
+#pragma unroll
+  for (int i = kTopL - 1; i >= 1; --i) {
+    const bool above = x > tv[i - 1];          // x lands before entry i-1: entry i-1 moves to i
+    const bool here = !above && (x > tv[i]);   // x lands exactly at i
+    tv[i] = above ? tv[i - 1] : (here ? x : tv[i]);
+    ti[i] = above ? ti[i - 1] : (here ? id : ti[i]);
   }
-  lv[pos * ne + et] = v;
-  li[pos * ne + et] = id;
+  if (x > tv[0]) {
+    tv[0] = x;
+    ti[0] = id;
+  }
 }
 
 template <int MT, bool TF32, int MODE>
@@ -122,8 +122,6 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* lv = reinterpret_cast<float*>(bar_area + C::kBarBytes);
-  int* li = reinterpret_cast<int*>(lv + kTopL * C::kEpiThreads);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -157,13 +155,6 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
-  }
-  if (MODE == 1 && warp >= 2) {
-    const int et = threadIdx.x - 64;
-    for (int i = 0; i < kTopL; ++i) {
-      lv[i * C::kEpiThreads + et] = -INFINITY;
-      li[i * C::kEpiThreads + et] = -1;
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -285,12 +276,17 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     const int e = warp - 2;
     const int q = warp & 3;
     const int mt = e >> 2;
-    const int et = threadIdx.x - 64;
     const int row = row0 + mt * 128 + q * 32 + lane;
     const bool tile_ok = mt < mt_valid;
     const bool valid = tile_ok && row < a.M;
     uint32_t acc_phase = 0;
-    float thr = -INFINITY;
+    float tv[kTopL];  // this row's running top-16 (descending), tv[15] is the admission threshold
+    int ti[kTopL];
+#pragma unroll
+    for (int i = 0; i < kTopL; ++i) {
+      tv[i] = -INFINITY;
+      ti[i] = -1;
+    }
     int c = c_begin, t0 = 0, nch = 0;
     while (next_tile(c, c_end, a.main_chunks, t0, nch)) {
       if (!mbar_wait_bounded(smem_u32(acc_full), acc_phase, abort_flag, kWaitLimitNs)) {
@@ -363,22 +359,23 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
               for (int j = 0; j < 32; ++j)
                 if (col0 + j < a.n_main) dst[col0 + j] = v[j];
             }
-            float mx = v[0];
+            // Candidates of this chunk: values above the row's current 16th. Each lane walks its
+            // own candidate bits; the warp loops while any lane has one left. A candidate is
+            // re-checked against the threshold, which rises as the list fills.
+            uint32_t cmask = 0u;
 #pragma unroll
-            for (int j = 1; j < 32; ++j) mx = fmaxf(mx, v[j]);
-            const bool want = valid && (mx > thr);
-            if (__any_sync(0xffffffffu, want)) {
-              if (want) {
+            for (int j = 0; j < 32; ++j) cmask |= (v[j] > tv[kTopL - 1] ? 1u : 0u) << j;
+            if (!valid) cmask = 0u;
+            while (__any_sync(0xffffffffu, cmask != 0u)) {
+              if (cmask != 0u) {
+                const int jj = __ffs(cmask) - 1;
+                cmask &= cmask - 1u;
+                float x = v[0];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  if (v[j] > thr) {
-                    list_insert(lv, li, et, C::kEpiThreads, v[j], col0 + j);
-                    thr = lv[(kTopL - 1) * C::kEpiThreads + et];
-                  }
-                }
+                for (int q = 1; q < 32; ++q) x = (jj == q) ? v[q] : x;
+                if (x > tv[kTopL - 1]) list_insert(tv, ti, x, col0 + jj);
               }
-            }
-          }
+            }          }
         }
       }
       tc_fence_before();
@@ -389,8 +386,8 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     if (MODE == 1 && valid && *abort_flag == 0) {
       const size_t o = (static_cast<size_t>(ns) * a.M + row) * kTopL;
       for (int i = 0; i < kTopL; ++i) {
-        a.list_val[o + i] = lv[i * C::kEpiThreads + et];
-        a.list_idx[o + i] = li[i * C::kEpiThreads + et];
+        a.list_val[o + i] = tv[i];
+        a.list_idx[o + i] = ti[i];
       }
     }
   }
