@@ -50,7 +50,10 @@ struct Cfg {
   static constexpr int kEpiWarps = 4 * MT;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kThreads = 64 + kEpiThreads;
-  static constexpr int kTmemCols = 256 * MT;
+  // One 128-row M tile fits twice in TMEM (2 x 256 columns): the accumulator is double-buffered
+  // and the MMA of the next tile overlaps the epilogue of this one. Two M tiles fill TMEM.
+  static constexpr int kAccBufs = MT == 1 ? 2 : 1;
+  static constexpr int kTmemCols = 512;
   static constexpr int kBarBytes = 256;
   static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
@@ -117,9 +120,9 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   uint8_t* bar_area = smem + C::kStages * C::kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(bar_area);
   uint64_t* empty = full + C::kStages;
-  uint64_t* acc_full = empty + C::kStages;
-  uint64_t* acc_empty = acc_full + 1;
-  uint64_t* drain = acc_empty + 1;
+  uint64_t* acc_full = empty + C::kStages;     // [kAccBufs]
+  uint64_t* acc_empty = acc_full + C::kAccBufs;  // [kAccBufs]
+  uint64_t* drain = acc_empty + C::kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -143,8 +146,10 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    mbar_init(smem_u32(acc_full), 1);
-    mbar_init(smem_u32(acc_empty), C::kEpiWarps);
+    for (int b = 0; b < C::kAccBufs; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), C::kEpiWarps);
+    }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -220,11 +225,15 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      uint32_t phase = 0;
+      int tile_i = 0;
       bool ok = true, any = false;
       int c = c_begin, t0 = 0, nch = 0;
       while (ok && next_tile(c, c_end, a.main_chunks, t0, nch)) {
-        if (!mbar_wait_bounded(smem_u32(acc_empty), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+        const int ab = tile_i % C::kAccBufs;                       // accumulator buffer of this tile
+        const uint32_t acc_par = static_cast<uint32_t>(tile_i / C::kAccBufs) & 1u;
+        const uint32_t acc_col = static_cast<uint32_t>(ab * 256);
+        if (!mbar_wait_bounded(smem_u32(&acc_empty[ab]), acc_par ^ 1u, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
         }
@@ -244,10 +253,10 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
               const uint64_t adesc = desc_kmajor_swizzled<kRowBytes>(sa + mt * kATile) + static_cast<uint64_t>(2 * k);
               const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
               if (TF32)
-                mma_tf32(tmem_base + static_cast<uint32_t>(mt * 256), adesc, bdesc + static_cast<uint64_t>(2 * k),
+                mma_tf32(tmem_base + acc_col + static_cast<uint32_t>(mt * 256), adesc, bdesc + static_cast<uint64_t>(2 * k),
                          idesc, acc);
               else
-                mma_f16(tmem_base + static_cast<uint32_t>(mt * 256), adesc, bdesc + static_cast<uint64_t>(2 * k),
+                mma_f16(tmem_base + acc_col + static_cast<uint32_t>(mt * 256), adesc, bdesc + static_cast<uint64_t>(2 * k),
                         idesc, acc);
             }
           }
@@ -259,8 +268,8 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(smem_u32(acc_full));  // accumulator complete
-        acc_phase ^= 1u;
+        mma_commit(smem_u32(&acc_full[ab]));  // accumulator complete
+        ++tile_i;
       }
       if (!ok) {
         raise_abort(abort_flag, a.err);
@@ -279,7 +288,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     const int row = row0 + mt * 128 + q * 32 + lane;
     const bool tile_ok = mt < mt_valid;
     const bool valid = tile_ok && row < a.M;
-    uint32_t acc_phase = 0;
+    int tile_i = 0;
     float tv[kTopL];  // this row's running top-16 (descending), tv[15] is the admission threshold
     int ti[kTopL];
 #pragma unroll
@@ -289,7 +298,10 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
     }
     int c = c_begin, t0 = 0, nch = 0;
     while (next_tile(c, c_end, a.main_chunks, t0, nch)) {
-      if (!mbar_wait_bounded(smem_u32(acc_full), acc_phase, abort_flag, kWaitLimitNs)) {
+      const int ab = tile_i % C::kAccBufs;
+      const uint32_t acc_par = static_cast<uint32_t>(tile_i / C::kAccBufs) & 1u;
+      const uint32_t acc_col = static_cast<uint32_t>(ab * 256);
+      if (!mbar_wait_bounded(smem_u32(&acc_full[ab]), acc_par, abort_flag, kWaitLimitNs)) {
         if (lane == 0) raise_abort(abort_flag, a.err);
         break;
       }
@@ -299,7 +311,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         for (int cc = 0; cc < nch * 2; ++cc) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(
-              tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mt * 256 + cc * 32), r);
+              tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_col + static_cast<uint32_t>(mt * 256 + cc * 32), r);
           tmem_ld_wait();
           const int col0 = t0 * kChunk + cc * 32;
           if (MODE == 0) {
@@ -380,8 +392,8 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(acc_empty));
-      acc_phase ^= 1u;
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
+      ++tile_i;
     }
     if (MODE == 1 && valid && *abort_flag == 0) {
       const size_t o = (static_cast<size_t>(ns) * a.M + row) * kTopL;
@@ -562,10 +574,16 @@ int prepare_args(const GemmProblem& p, const GemmPlan& plan, CUtensorMap* mA, CU
 
 }  // namespace
 
+// Largest M-tile count per CTA the head uses (2: one weight tile feeds 256 rows, single-buffered
+// accumulator; 1: 128 rows, double-buffered accumulator).
+#ifndef DFL_HEAD_MAX_MT
+#define DFL_HEAD_MAX_MT 2
+#endif
+
 GemmPlan head_plan(int M, int K, int n_main, int n_extra, int sms) {
   (void)K;
   GemmPlan p{};
-  p.mt = M > 128 ? 2 : 1;
+  p.mt = (M > 128 && DFL_HEAD_MAX_MT >= 2) ? 2 : 1;
   p.m_groups = (M + 128 * p.mt - 1) / (128 * p.mt);
   p.n_chunks = (n_main + kChunk - 1) / kChunk + (n_extra + kChunk - 1) / kChunk;
   p.n_splits = std::max(1, std::min(p.n_chunks, sms / p.m_groups));
