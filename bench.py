@@ -389,7 +389,14 @@ def our_arm(args, wl_name):
 
 # per-launch DRAM traffic (bytes) of the head kernel from an ncu capture, by workload; None until
 # measured for the current kernel
-TRAFFIC_PER_LAUNCH = {}
+TRAFFIC_PER_LAUNCH = {
+    # dram__bytes_read.sum + dram__bytes_write.sum of tc_gemm_kernel<2, bf16, TOPK> (960 rows),
+    # profiles/head_topk_selector-B64.md; the full tail runs the same head launch
+    "full-tail-B64": 2.559410e9 + 3.499264e6,
+    "selector-B64": 2.559410e9 + 3.499264e6,
+    # tc_gemm_kernel<1, bf16, TOPK> (15 rows), profiles/head_topk_selector-B1.md
+    "selector-B1": 2.543751e9 + 2.905344e6,
+}
 
 
 def main():
