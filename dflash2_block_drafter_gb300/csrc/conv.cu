@@ -50,6 +50,9 @@ __device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
   reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
   reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
+// Round to the storage type and back (the value a reader of the stored tensor sees).
+__device__ __forceinline__ float stored(float v, const __nv_bfloat16*) { return __bfloat162float(__float2bfloat16_rn(v)); }
+__device__ __forceinline__ float stored(float v, const float*) { return v; }
 __device__ __forceinline__ void store1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 __device__ __forceinline__ void store1(float* p, float v) { *p = v; }
 __device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -191,24 +194,113 @@ __global__ void __launch_bounds__(kApplyMaxThreads)
   store8(out + row * H + c, o);
 }
 
+// finish's apply pass fused with the next RMSNorm: one CTA per row (b, t), thread v owns
+// channels 8v..8v+7. out = residual + side-1 conv of y (rounded once); rows t >= next_row0 then
+// get next_n = rms(out) * next_w, computed from the rounded values the next reader sees.
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads)
+    conv_side1_norm_kernel(const T* __restrict__ y, const T* __restrict__ coef1, const float* __restrict__ base,
+                           const T* residual, T* out, const T* __restrict__ next_w, float eps, T* __restrict__ next_n,
+                           int next_row0, int G, int H, int gs, int groups) {
+  __shared__ float warp_ss[32];
+  __shared__ float row_r;
+  const size_t row = blockIdx.x;
+  const int t = static_cast<int>(row % G);
+  const size_t b = row / G;
+  const int c = threadIdx.x * 8;
+  const bool active = c < H;
+  float o[8];
+  if (active) {
+    const int g = c / gs;
+    const float d0 = load1(coef1 + (row * 2 + 0) * groups + g);
+    const float d1 = load1(coef1 + (row * 2 + 1) * groups + g);
+    float b0[8], b1[8], cur[8], prev[8], res[8];
+    load8(base + 2 * H + c, b0);  // base[1][0][c..]
+    load8(base + 3 * H + c, b1);  // base[1][1][c..]
+    load8(y + row * H + c, cur);
+    if (t > 0) {
+      load8(y + (row - 1) * H + c, prev);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) prev[i] = 0.f;
+    }
+    if (residual != nullptr) {
+      load8(residual + row * H + c, res);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) res[i] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = (b0[i] + d0) * cur[i] + (b1[i] + d1) * prev[i] + res[i];
+    store8(out + row * H + c, o);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = stored(o[i], out);
+  }
+  if (t < next_row0) return;  // the whole CTA leaves together
+  float ss = 0.f;
+  if (active) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(o[i], o[i], ss);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) warp_ss[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? warp_ss[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (threadIdx.x == 0) row_r = rsqrtf(v / static_cast<float>(H) + eps);
+  }
+  __syncthreads();
+  if (!active) return;
+  const float r = row_r;
+  float w[8];
+  load8(next_w + c, w);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = o[i] * r * w[i];
+  store8(next_n + (b * (G - next_row0) + (t - next_row0)) * H + c, o);
+}
+
 }  // namespace
 
-// Split-K plan of kernel_projection. Small M: 64-column tiles, K split until ~all SMs stream the
-// weight. Large M: 256-row groups x 128-column tiles (A and W tiles both reused) with a few K
-// splits, keeping the fp32 partials (summed by the side-0 pass) small.
+// Split-K plan of kernel_projection: 128-row M tiles; the N tile (64, 128 or 256 columns) and the
+// number of K splits are picked by a small cost model, so that the weight stream is spread over
+// the SMs at small M and the tensor pipe is used efficiently at large M:
+//   issue:    k-blocks per CTA x 4 MMAs x ~145 cycles (a tcgen05.mma of any N up to 256 takes about
+//             that long to issue, so wide tiles do more work per instruction)
+//   stream:   weight bytes / (CTAs x ~40 GB/s per SM)
+//   partials: fp32 split-K partials written and read back by the side-0 pass (~5 TB/s)
+// cost = max(issue, stream) + partials.
 GemmPlan kp_plan(const ConvShape& s, int sms) {
   const int M = s.rows();
   const int N = 4 * s.groups;
   const int bk = 64;  // elements of K per pipeline stage at most (fewer with 64-byte rows)
   const int k_blocks = (s.H + bk - 1) / bk;
-  GemmPlan p{};
-  p.mt = M > 128 ? 2 : 1;
-  p.m_groups = (M + 128 * p.mt - 1) / (128 * p.mt);
-  p.n_chunks = (N + 63) / 64;
-  p.n_splits = p.m_groups >= 2 ? (p.n_chunks + 1) / 2 : p.n_chunks;
-  const int units = p.m_groups * p.n_splits;
-  p.k_splits = std::max(1, std::min(std::min(k_blocks, 16), sms / std::max(1, units)));
-  return p;
+  const double w_bytes = 2.0 * N * s.H;
+  GemmPlan best{};
+  double best_cost = 1e30;
+  for (int tile_chunks = 4; tile_chunks >= 1; tile_chunks /= 2) {
+    GemmPlan p{};
+    p.mt = 1;
+    p.m_groups = (M + 127) / 128;
+    p.n_chunks = (N + 63) / 64;
+    p.n_splits = (p.n_chunks + tile_chunks - 1) / tile_chunks;
+    const int units = p.m_groups * p.n_splits;
+    p.k_splits = std::max(1, std::min(std::min(k_blocks, 32), sms / std::max(1, units)));
+    const int ctas = units * p.k_splits;
+    const int waves = (ctas + sms - 1) / sms;
+    const double kb_per_cta = static_cast<double>(k_blocks) / p.k_splits;
+    const double t_issue = waves * kb_per_cta * 4.0 * 145.0 / 1.9e9;
+    const double t_stream = w_bytes / (std::min(ctas, sms) * 40e9);
+    const double t_part = p.k_splits > 1 ? p.k_splits * static_cast<double>(M) * N * 8.0 / 5e12 : 0.0;
+    const double cost = std::max(t_issue, t_stream) + t_part;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = p;
+    }
+  }
+  return best;
 }
 
 size_t conv_prepare_workspace(const ConvShape& s, int sms) {
@@ -257,8 +349,27 @@ int launch_conv_side0(const ConvShape& s, const void* n, const float* part, int 
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "conv side0 launch failed: %s", cudaGetErrorString(e));
 }
 
+template <typename T>
+static int side1_norm_typed(const ConvShape& s, const void* y, const void* coef1, const float* base,
+                            const void* residual, void* out, const void* next_w, float eps, void* next_n, int next_row0,
+                            cudaStream_t st) {
+  const int threads = std::min(kNormThreads, ((s.H / 8 + 31) / 32) * 32);
+  conv_side1_norm_kernel<T><<<s.B * s.G, threads, 0, st>>>(
+      static_cast<const T*>(y), static_cast<const T*>(coef1), base, static_cast<const T*>(residual),
+      static_cast<T*>(out), static_cast<const T*>(next_w), eps, static_cast<T*>(next_n), next_row0, s.G, s.H, s.gs,
+      s.groups);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DFLASH2_OK
+                          : fail(DFLASH2_ERR_CUDA, "conv side1+norm launch failed: %s", cudaGetErrorString(e));
+}
+
 int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, const float* base, const void* residual,
                       void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st) {
+  if (next_n != nullptr) {
+    if (s.dtype == DFLASH2_F32)
+      return side1_norm_typed<float>(s, y, coef1, base, residual, out, next_w, eps, next_n, next_row0, st);
+    return side1_norm_typed<__nv_bfloat16>(s, y, coef1, base, residual, out, next_w, eps, next_n, next_row0, st);
+  }
   const int vpc = vectors_per_cta(s.G);
   const dim3 grid((s.H / 8 + vpc - 1) / vpc, s.B);
   const int threads = s.G * vpc;
@@ -270,10 +381,8 @@ int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, cons
     conv_side1_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
         static_cast<const __nv_bfloat16*>(y), static_cast<const __nv_bfloat16*>(coef1), base,
         static_cast<const __nv_bfloat16*>(residual), static_cast<__nv_bfloat16*>(out), s.G, s.H, s.gs, s.groups, vpc);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "conv side1 launch failed: %s", cudaGetErrorString(e));
-  if (next_n == nullptr) return DFLASH2_OK;
-  return launch_rmsnorm_rows(out, next_w, eps, next_n, s.B, s.G, next_row0, s.H, s.dtype, st);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "conv side1 launch failed: %s", cudaGetErrorString(e));
 }
 
 }  // namespace dfl

@@ -433,9 +433,19 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict
   }
   for (int s = lane; s < n_splits; s += 32) {
     const size_t o = (static_cast<size_t>(s) * M + row) * kTopL;
+    float lvv[kTopL];
+    int liv[kTopL];
+#pragma unroll
+    for (int q = 0; q < kTopL / 4; ++q) {  // the whole sorted list in 8 vector loads
+      const float4 f = __ldg(reinterpret_cast<const float4*>(lv + o) + q);
+      const int4 n = __ldg(reinterpret_cast<const int4*>(li + o) + q);
+      lvv[4 * q] = f.x; lvv[4 * q + 1] = f.y; lvv[4 * q + 2] = f.z; lvv[4 * q + 3] = f.w;
+      liv[4 * q] = n.x; liv[4 * q + 1] = n.y; liv[4 * q + 2] = n.z; liv[4 * q + 3] = n.w;
+    }
+#pragma unroll
     for (int i = 0; i < kTopL; ++i) {
-      float cv = lv[o + i];
-      int ci = li[o + i];
+      float cv = lvv[i];
+      int ci = liv[i];
       if (ci < 0 || !better(cv, ci, tv[kTopL - 1], ti[kTopL - 1])) break;  // lists are sorted
 #pragma unroll
       for (int j = 0; j < kTopL; ++j) {
