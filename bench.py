@@ -239,42 +239,31 @@ def our_arm(args, wl_name):
             run.selector(h_in, anchors)
 
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    head_ev = []
+    hs_ev = torch.cuda.Event(enable_timing=True)
+    he_ev = torch.cuda.Event(enable_timing=True)
 
-    def timed_step(record_head):
-        """One step between events; the head call also gets its own events."""
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        if record_head and run.with_selector:
-            hs = torch.cuda.Event(enable_timing=True)
-            he = torch.cuda.Event(enable_timing=True)
-            s.record(stream)
-            if wl.sites:
-                run.conv_chain(x0, ys, emit_h=True)
-                h = run.h
-            else:
-                h = h_in
-            hs.record(stream)
-            M = h.shape[0] * h.shape[1]
-            d.dflash2_head_topk(h.view(M, wl.H), run.w_head, wl.K, bias=run.bias, w_proj=run.w_proj, cand=run.cand,
-                                unary=run.unary, z=run.z, workspace=run.head_ws)
-            he.record(stream)
-            d.dflash2_score_edges(run.cand.view(h.shape[0], wl.steps, wl.K), run.unary.view(h.shape[0], wl.steps, wl.K),
-                                  run.z.view(h.shape[0], wl.steps, wl.R), anchors, run.pred, run.succ, S=run.S,
-                                  path=run.path)
-            e.record(stream)
-            head_ev.append((hs, he))
+    def step_marked():
+        """One step with events around the head call (the dominant kernel)."""
+        if wl.sites:
+            run.conv_chain(x0, ys, emit_h=run.with_selector)
+            h = run.h if run.with_selector else None
         else:
-            s.record(stream)
-            step()
-            e.record(stream)
-        return s, e
+            h = h_in
+        if run.with_selector:
+            Bh = h.shape[0]
+            hs_ev.record()
+            d.dflash2_head_topk(h.view(Bh * wl.steps, wl.H), run.w_head, wl.K, bias=run.bias, w_proj=run.w_proj,
+                                cand=run.cand, unary=run.unary, z=run.z, workspace=run.head_ws)
+            he_ev.record()
+            d.dflash2_score_edges(run.cand.view(Bh, wl.steps, wl.K), run.unary.view(Bh, wl.steps, wl.K),
+                                  run.z.view(Bh, wl.steps, wl.R), anchors, run.pred, run.succ, S=run.S, path=run.path)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
-        step()
+        step_marked()
     torch.cuda.synchronize()
     assert d.dflash2_poll_error() == 0, "device error word set during warm-up"
+    graph = run.capture(step_marked) if args.graph else None
 
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     smi_id = visible[torch.cuda.current_device()].strip() if visible and visible[0].strip() else \
@@ -284,17 +273,26 @@ def our_arm(args, wl_name):
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
-    evs = []
+    step_ms, head_ms = [], []
+    s_ev = torch.cuda.Event(enable_timing=True)
+    e_ev = torch.cuda.Event(enable_timing=True)
     for _ in range(args.steps):
         flush.zero_()
-        evs.append(timed_step(True))
+        s_ev.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            step_marked()
+        e_ev.record(stream)
+        e_ev.synchronize()
+        step_ms.append(s_ev.elapsed_time(e_ev))
+        if run.with_selector:
+            head_ms.append(hs_ev.elapsed_time(he_ev))
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    step_ms = [s.elapsed_time(e) for s, e in evs]
     total_ms = sum(step_ms)
-    head_ms = [a.elapsed_time(b) for a, b in head_ev]
     assert d.dflash2_poll_error() == 0, "device error word set during the timed steps"
 
     # ---------------------------------------------------------------- e2e: host buffers through the C ABI
@@ -372,6 +370,7 @@ def our_arm(args, wl_name):
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": "blocks/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * args.steps,
+        "cuda_graph": bool(args.graph),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -409,6 +408,9 @@ def main():
     ap.add_argument("--cpu-blocks", type=int, default=2)
     ap.add_argument("--ref-blocks", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", dest="graph", action="store_true", default=True,
+                    help="replay each timed step as one CUDA graph (default)")
+    ap.add_argument("--no-graph", dest="graph", action="store_false")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args, args.workload)

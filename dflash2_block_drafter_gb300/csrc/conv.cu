@@ -50,9 +50,6 @@ __device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
   reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
   reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
-// Round to the storage type and back (the value a reader of the stored tensor sees).
-__device__ __forceinline__ float stored(float v, const __nv_bfloat16*) { return __bfloat162float(__float2bfloat16_rn(v)); }
-__device__ __forceinline__ float stored(float v, const float*) { return v; }
 __device__ __forceinline__ void store1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 __device__ __forceinline__ void store1(float* p, float v) { *p = v; }
 __device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -194,74 +191,6 @@ __global__ void __launch_bounds__(kApplyMaxThreads)
   store8(out + row * H + c, o);
 }
 
-// finish's apply pass fused with the next RMSNorm: one CTA per row (b, t), thread v owns
-// channels 8v..8v+7. out = residual + side-1 conv of y (rounded once); rows t >= next_row0 then
-// get next_n = rms(out) * next_w, computed from the rounded values the next reader sees.
-template <typename T>
-__global__ void __launch_bounds__(kNormThreads)
-    conv_side1_norm_kernel(const T* __restrict__ y, const T* __restrict__ coef1, const float* __restrict__ base,
-                           const T* residual, T* out, const T* __restrict__ next_w, float eps, T* __restrict__ next_n,
-                           int next_row0, int G, int H, int gs, int groups) {
-  __shared__ float warp_ss[32];
-  __shared__ float row_r;
-  const size_t row = blockIdx.x;
-  const int t = static_cast<int>(row % G);
-  const size_t b = row / G;
-  const int c = threadIdx.x * 8;
-  const bool active = c < H;
-  float o[8];
-  if (active) {
-    const int g = c / gs;
-    const float d0 = load1(coef1 + (row * 2 + 0) * groups + g);
-    const float d1 = load1(coef1 + (row * 2 + 1) * groups + g);
-    float b0[8], b1[8], cur[8], prev[8], res[8];
-    load8(base + 2 * H + c, b0);  // base[1][0][c..]
-    load8(base + 3 * H + c, b1);  // base[1][1][c..]
-    load8(y + row * H + c, cur);
-    if (t > 0) {
-      load8(y + (row - 1) * H + c, prev);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) prev[i] = 0.f;
-    }
-    if (residual != nullptr) {
-      load8(residual + row * H + c, res);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) res[i] = 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = (b0[i] + d0) * cur[i] + (b1[i] + d1) * prev[i] + res[i];
-    store8(out + row * H + c, o);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = stored(o[i], out);
-  }
-  if (t < next_row0) return;  // the whole CTA leaves together
-  float ss = 0.f;
-  if (active) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(o[i], o[i], ss);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  if ((threadIdx.x & 31) == 0) warp_ss[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? warp_ss[threadIdx.x] : 0.f;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    if (threadIdx.x == 0) row_r = rsqrtf(v / static_cast<float>(H) + eps);
-  }
-  __syncthreads();
-  if (!active) return;
-  const float r = row_r;
-  float w[8];
-  load8(next_w + c, w);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = o[i] * r * w[i];
-  store8(next_n + (b * (G - next_row0) + (t - next_row0)) * H + c, o);
-}
-
 }  // namespace
 
 // Split-K plan of kernel_projection: 128-row M tiles; the N tile (64, 128 or 256 columns) and the
@@ -349,27 +278,8 @@ int launch_conv_side0(const ConvShape& s, const void* n, const float* part, int 
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "conv side0 launch failed: %s", cudaGetErrorString(e));
 }
 
-template <typename T>
-static int side1_norm_typed(const ConvShape& s, const void* y, const void* coef1, const float* base,
-                            const void* residual, void* out, const void* next_w, float eps, void* next_n, int next_row0,
-                            cudaStream_t st) {
-  const int threads = std::min(kNormThreads, ((s.H / 8 + 31) / 32) * 32);
-  conv_side1_norm_kernel<T><<<s.B * s.G, threads, 0, st>>>(
-      static_cast<const T*>(y), static_cast<const T*>(coef1), base, static_cast<const T*>(residual),
-      static_cast<T*>(out), static_cast<const T*>(next_w), eps, static_cast<T*>(next_n), next_row0, s.G, s.H, s.gs,
-      s.groups);
-  const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? DFLASH2_OK
-                          : fail(DFLASH2_ERR_CUDA, "conv side1+norm launch failed: %s", cudaGetErrorString(e));
-}
-
 int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, const float* base, const void* residual,
                       void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st) {
-  if (next_n != nullptr) {
-    if (s.dtype == DFLASH2_F32)
-      return side1_norm_typed<float>(s, y, coef1, base, residual, out, next_w, eps, next_n, next_row0, st);
-    return side1_norm_typed<__nv_bfloat16>(s, y, coef1, base, residual, out, next_w, eps, next_n, next_row0, st);
-  }
   const int vpc = vectors_per_cta(s.G);
   const dim3 grid((s.H / 8 + vpc - 1) / vpc, s.B);
   const int threads = s.G * vpc;
@@ -382,7 +292,11 @@ int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, cons
         static_cast<const __nv_bfloat16*>(y), static_cast<const __nv_bfloat16*>(coef1), base,
         static_cast<const __nv_bfloat16*>(residual), static_cast<__nv_bfloat16*>(out), s.G, s.H, s.gs, s.groups, vpc);
   const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "conv side1 launch failed: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "conv side1 launch failed: %s", cudaGetErrorString(e));
+  if (next_n == nullptr) return DFLASH2_OK;
+  // The next RMSNorm as its own row-per-CTA pass: measured faster than fusing it into the
+  // apply pass, whose row-per-CTA layout loses the L1 reuse of the previous row.
+  return launch_rmsnorm_rows(out, next_w, eps, next_n, s.B, s.G, next_row0, s.H, s.dtype, st);
 }
 
 }  // namespace dfl

@@ -55,9 +55,10 @@ struct Cfg {
   static constexpr int kAccBufs = MT == 1 ? 2 : 1;
   static constexpr int kTmemCols = 512;
   static constexpr int kBarBytes = 256;
-  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes) / kStageBytes;
+  static constexpr int kBiasBytes = kEpiWarps * 256 * 4;  // one tile's bias per epilogue warp
+  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes - kBiasBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kBiasBytes;
 };
 static_assert(Cfg<2>::kStages >= 2 && Cfg<2>::kSmem <= kSmemLimit, "shared memory budget");
 static_assert(Cfg<1>::kStages >= 2 && Cfg<1>::kSmem <= kSmemLimit, "shared memory budget");
@@ -125,6 +126,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   uint64_t* drain = acc_empty + C::kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* sbias_all = reinterpret_cast<float*>(bar_area + C::kBarBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -296,11 +298,32 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       tv[i] = -INFINITY;
       ti[i] = -1;
     }
+    float* sbias = sbias_all + e * 256;  // this warp's copy of the tile's bias
     int c = c_begin, t0 = 0, nch = 0;
     while (next_tile(c, c_end, a.main_chunks, t0, nch)) {
       const int ab = tile_i % C::kAccBufs;
       const uint32_t acc_par = static_cast<uint32_t>(tile_i / C::kAccBufs) & 1u;
       const uint32_t acc_col = static_cast<uint32_t>(ab * 256);
+      // Stage the tile's bias in shared memory before waiting for the accumulator, so its global
+      // load latency hides behind the mainloop (each 32-column chunk would otherwise miss L1).
+      if (MODE == 1 && a.bias != nullptr && t0 < a.main_chunks) {
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i4 = lane + 32 * h;  // float4 index within the tile
+          const int col = t0 * kChunk + 4 * i4;
+          float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (col + 4 <= a.n_main) {
+            b4 = __ldg(reinterpret_cast<const float4*>(a.bias + col));
+          } else {
+            if (col < a.n_main) b4.x = __ldg(a.bias + col);
+            if (col + 1 < a.n_main) b4.y = __ldg(a.bias + col + 1);
+            if (col + 2 < a.n_main) b4.z = __ldg(a.bias + col + 2);
+          }
+          reinterpret_cast<float4*>(sbias)[i4] = b4;
+        }
+        __syncwarp();
+      }
       if (!mbar_wait_bounded(smem_u32(&acc_full[ab]), acc_par, abort_flag, kWaitLimitNs)) {
         if (lane == 0) raise_abort(abort_flag, a.err);
         break;
@@ -342,10 +365,10 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
               if (a.bias != nullptr) {
-                const float4* bp = reinterpret_cast<const float4*>(a.bias + col0);
+                const float4* bp = reinterpret_cast<const float4*>(sbias + cc * 32);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                  const float4 b4 = __ldg(bp + q);
+                  const float4 b4 = bp[q];
                   v[4 * q] += b4.x;
                   v[4 * q + 1] += b4.y;
                   v[4 * q + 2] += b4.z;

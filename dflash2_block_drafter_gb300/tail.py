@@ -125,3 +125,22 @@ class TailRunner:
         """The whole block tail; returns path [B, steps] int32 (device)."""
         self.conv_chain(x0, ys, emit_h=True)
         return self.selector(self.h, anchors, want_S=want_S)
+
+    def capture(self, fn, *args, **kwargs) -> "torch.cuda.CUDAGraph":
+        """Record one pass of ``fn`` (e.g. ``self.full``) into a CUDA graph over the runner's fixed
+        buffers; ``graph.replay()`` then re-launches every kernel of the pass with one call.
+
+        The pass runs once eagerly first, so that every kernel's attributes are set outside the
+        capture. Inputs are read from the tensors passed here at replay time: refresh them in place.
+        """
+        fn(*args, **kwargs)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                fn(*args, **kwargs)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        return graph

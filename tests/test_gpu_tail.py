@@ -66,3 +66,25 @@ def test_full_tail_b64_sampled(torch):
     _check_tail(run, wl, [0, 31, 63])
     path = run.path.cpu().numpy()
     assert path.shape == (64, 15) and np.all((path >= 0) & (path < wl.V))
+
+
+def test_graph_replay_matches_eager(torch):
+    """The tail captured into a CUDA graph and replayed gives the eager pass's results exactly."""
+    from dflash2_block_drafter_gb300.tail import TailRunner, to_device
+    import dflash2_block_drafter_gb300 as d
+    wl = I.make_config(0)
+    run = TailRunner(wl)
+    x0 = to_device(wl.x0)
+    ys = [to_device(s.y) for s in wl.sites]
+    anchors = to_device(wl.anchors)
+    run.full(x0, ys, anchors)
+    eager = (run.path.clone(), run.S.clone(), run.h.clone())
+    graph = run.capture(run.full, x0, ys, anchors)
+    run.path.zero_()
+    run.S.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert d.dflash2_poll_error() == 0
+    assert torch.equal(run.path, eager[0])
+    assert torch.equal(run.S, eager[1])
+    assert torch.equal(run.h, eager[2])
