@@ -56,9 +56,12 @@ struct Cfg {
   static constexpr int kTmemCols = 512;
   static constexpr int kBarBytes = 256;
   static constexpr int kBiasBytes = kEpiWarps * 256 * 4;  // one tile's bias per epilogue warp
-  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes - kBiasBytes) / kStageBytes;
+  // STORE epilogue with one M tile: a 32x33 fp32 transpose tile per epilogue warp, so that partial
+  // sums leave as full 128-byte row segments rather than 16-byte pieces of 32 different rows.
+  static constexpr int kTransBytes = MT == 1 ? kEpiWarps * 32 * 33 * 4 : 0;
+  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes - kBiasBytes - kTransBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kBiasBytes;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kBiasBytes + kTransBytes;
 };
 static_assert(Cfg<2>::kStages >= 2 && Cfg<2>::kSmem <= kSmemLimit, "shared memory budget");
 static_assert(Cfg<1>::kStages >= 2 && Cfg<1>::kSmem <= kSmemLimit, "shared memory budget");
@@ -127,6 +130,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sbias_all = reinterpret_cast<float*>(bar_area + C::kBarBytes);
+  float* strans_all = reinterpret_cast<float*>(bar_area + C::kBarBytes + C::kBiasBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -337,7 +341,24 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
               tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_col + static_cast<uint32_t>(mt * 256 + cc * 32), r);
           tmem_ld_wait();
           const int col0 = t0 * kChunk + cc * 32;
-          if (MODE == 0) {
+          if (MODE == 0 && MT == 1) {
+            // lane l holds row (row - lane + l); transpose through shared memory and write each
+            // row's 32 columns as one 128-byte segment
+            float* tr = strans_all + e * (32 * 33);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) tr[lane * 33 + j] = __uint_as_float(r[j]);
+            __syncwarp();
+            const int rbase = row - lane;
+            const int col = col0 + lane;
+            float* base_ptr = a.part + static_cast<size_t>(ks) * a.M * a.n_main;
+#pragma unroll 8
+            for (int rr = 0; rr < 32; ++rr) {
+              const int rrow = rbase + rr;
+              if (tile_ok && rrow < a.M && col < a.n_main)
+                base_ptr[static_cast<size_t>(rrow) * a.n_main + col] = tr[rr * 33 + lane];
+            }
+            __syncwarp();
+          } else if (MODE == 0) {
             if (valid) {
               float* dst = a.part + (static_cast<size_t>(ks) * a.M + row) * a.n_main + col0;
               if (col0 + 32 <= a.n_main && (a.n_main & 3) == 0) {
@@ -397,10 +418,16 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
             // Candidates of this chunk: values above the row's current 16th. Each lane walks its
             // own candidate bits; the warp loops while any lane has one left. A candidate is
             // re-checked against the threshold, which rises as the list fills.
-            uint32_t cmask = 0u;
+            float mx = fmaxf(v[0], v[1]);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) cmask |= (v[j] > tv[kTopL - 1] ? 1u : 0u) << j;
-            if (!valid) cmask = 0u;
+            for (int j = 2; j < 32; ++j) mx = fmaxf(mx, v[j]);
+            const bool any_cand = valid && mx > tv[kTopL - 1];
+            if (!__any_sync(0xffffffffu, any_cand)) continue;  // the common case once lists fill
+            uint32_t cmask = 0u;
+            if (any_cand) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) cmask |= (v[j] > tv[kTopL - 1] ? 1u : 0u) << j;
+            }
             while (__any_sync(0xffffffffu, cmask != 0u)) {
               if (cmask != 0u) {
                 const int jj = __ffs(cmask) - 1;
@@ -410,7 +437,8 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
                 for (int q = 1; q < 32; ++q) x = (jj == q) ? v[q] : x;
                 if (x > tv[kTopL - 1]) list_insert(tv, ti, x, col0 + jj);
               }
-            }          }
+            }
+          }
         }
       }
       tc_fence_before();
