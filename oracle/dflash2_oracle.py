@@ -177,6 +177,17 @@ def top_k(logits, K: int):
     return ids.reshape(L.shape[:-1] + (K,)), vals.reshape(L.shape[:-1] + (K,))
 
 
+def listed_candidates(cols, ids) -> np.ndarray:
+    """Token ids of top-K columns taken over a draft vocabulary: ids[cols].
+
+    [ts] ``#block`` (a target that declares a draft vocabulary projects the head onto those rows
+    only) and ``#select`` (``ids`` maps the columns of logits over the draft vocabulary to token
+    ids before the codebook gathers). The top-K itself runs over the listed columns with the same
+    rule as ``top_k`` (equal values: lower column, i.e. earlier listed row, first).
+    """
+    return np.asarray(ids, dtype=np.int64)[np.asarray(cols, dtype=np.int64)]
+
+
 def kth_margin(logits, K: int) -> np.ndarray:
     """Per row: (K-th largest) - ((K+1)-th largest) logit; the gap that decides top-K membership."""
     L = _f64(logits)

@@ -169,6 +169,12 @@ def uniform_ids(config_seed: int, name: str, n: int, high: int) -> np.ndarray:
     return g.integers(0, high, size=n, dtype=np.int64).astype(np.int32)
 
 
+def draft_vocabulary(config_seed: int, V: int, n: int) -> np.ndarray:
+    """A seeded draft vocabulary: n distinct token ids in [0, V), ascending (int32)."""
+    g = np.random.Generator(np.random.PCG64(_seed_for(config_seed, "draft_vocabulary")))
+    return np.sort(g.choice(V, size=n, replace=False)).astype(np.int32)
+
+
 def ones(shape, dtype: str) -> np.ndarray:
     return _store(np.ones(shape, dtype=np.float32), dtype)
 

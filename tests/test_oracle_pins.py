@@ -400,3 +400,31 @@ def test_block_tail_composition_shapes_and_zero_codebooks():
     assert out["S"].shape == (B, G - 1, K, K)
     h = O.rms_norm(out["x"][:, 1:], np.ones(H), 1e-6)
     assert np.array_equal(out["path"], np.argmax(h @ W.T + bias, axis=-1))
+
+
+def test_listed_vocabulary_equals_masked_full_head():
+    # Top-K over a sorted draft vocabulary S (head rows W[S]) mapped through ids equals the full
+    # head's top-K with every unlisted logit removed (same tie rule: the listed order is id order).
+    M, H, V, K = 6, 12, 200, 8
+    h = _rand(M, H)
+    W = _rand(V, H)
+    bias = RNG.integers(-2, 3, size=V).astype(np.float64)   # integer bias makes ties likely
+    W[5] = W[7]                                             # two identical rows: an exact tie
+    S = np.sort(RNG.choice(V, size=60, replace=False))
+    S = np.union1d(S, [5, 7])
+    cols, vals = O.top_k(O.head_logits(h, W[S], bias[S]), K)
+    got = O.listed_candidates(cols, S)
+    full = O.head_logits(h, W, bias)
+    masked = np.full_like(full, -np.inf)
+    masked[:, S] = full[:, S]
+    ref_ids, ref_vals = O.top_k(masked, K)
+    assert np.array_equal(got, ref_ids)
+    np.testing.assert_array_equal(vals, ref_vals)
+
+
+def test_listed_vocabulary_identity_map():
+    M, H, V, K = 4, 8, 50, 5
+    h = _rand(M, H)
+    W = _rand(V, H)
+    cols, _ = O.top_k(O.head_logits(h, W), K)
+    assert np.array_equal(O.listed_candidates(cols, np.arange(V)), cols)
