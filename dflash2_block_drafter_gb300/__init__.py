@@ -20,7 +20,7 @@ __all__ = [
     "Dflash2Error", "library", "library_path", "dflash2_version", "dflash2_poll_error",
     "dflash2_conv_prepare_workspace_bytes", "dflash2_conv_prepare", "dflash2_conv_finish",
     "dflash2_head_topk_workspace_bytes", "dflash2_head_topk", "dflash2_score_edges",
-    "dflash2_select_path", "dflash2_selftest_bounded_wait", "dflash2_head_topk_noalloc", "DTYPE_CODES",
+    "dflash2_select_path", "dflash2_selftest_bounded_wait", "dflash2_head_topk_noalloc", "dflash2_head_topk_vocab", "DTYPE_CODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -48,6 +48,8 @@ _SIGNATURES = {
     "dflash2_select_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "dflash2_selftest_bounded_wait": (_i, [_i, _vp]),
     "dflash2_head_topk_noalloc": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
+    "dflash2_head_topk_vocab": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz,
+                                     _vp]),
 }
 
 
@@ -184,6 +186,32 @@ def dflash2_head_topk(h, w_head, K, bias=None, w_proj=None, cand=None, unary=Non
         _dev(w_proj, "w_proj", dt, True), R, K, _code(h), _dev(cand, "cand", torch.int32),
         _dev(unary, "unary", torch.float32), _dev(z, "z", torch.float32, True),
         _dev(logits, "logits", torch.float32, True), _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+    return cand, unary, z, logits
+
+
+def dflash2_head_topk_vocab(h, w_listed, vocab_ids, K, bias_listed=None, w_proj=None, cand=None, unary=None, z=None,
+                            logits=None, want_logits=False, workspace=None, stream=None):
+    """Head GEMM + fused top-K over a draft vocabulary: rows of w_listed are the listed tokens
+    vocab_ids (int32). Returns (cand [M,K] token ids, unary, z or None, logits [M,V_listed] or None)."""
+    M, H = h.shape
+    V = w_listed.shape[0]
+    R = w_proj.shape[0] if w_proj is not None else 0
+    dt = h.dtype
+    dev = h.device
+    cand = torch.empty((M, K), dtype=torch.int32, device=dev) if cand is None else cand
+    unary = torch.empty((M, K), dtype=torch.float32, device=dev) if unary is None else unary
+    if w_proj is not None and z is None:
+        z = torch.empty((M, R), dtype=torch.float32, device=dev)
+    if want_logits and logits is None:
+        logits = torch.empty((M, V), dtype=torch.float32, device=dev)
+    nbytes = library().dflash2_head_topk_workspace_bytes(M, H, V, K, R)
+    workspace = _workspace(nbytes, dev, workspace)
+    _check(library().dflash2_head_topk_vocab(
+        _dev(h, "h", dt), M, H, _dev(w_listed, "w_listed", dt), V, _dev(vocab_ids, "vocab_ids", torch.int32),
+        _dev(bias_listed, "bias_listed", torch.float32, True), _dev(w_proj, "w_proj", dt, True), R, K, _code(h),
+        _dev(cand, "cand", torch.int32), _dev(unary, "unary", torch.float32), _dev(z, "z", torch.float32, True),
+        _dev(logits, "logits", torch.float32, True), _dev(workspace, "workspace"), workspace.numel(),
+        _stream(stream)))
     return cand, unary, z, logits
 
 

@@ -199,6 +199,33 @@ int dflash2_head_topk(const void* h, int M, int H, const void* w_head, int V, co
   return launch_head_topk(gp, plan, bias, K, cand, unary, z, logits, workspace, static_cast<cudaStream_t>(stream));
 }
 
+int dflash2_head_topk_vocab(const void* h, int M, int H, const void* w_listed, int V_listed, const int32_t* vocab_ids,
+                            const float* bias_listed, const void* w_proj, int R, int K, int dtype, int32_t* cand,
+                            float* unary, float* z, float* logits, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  REQUIRE(vocab_ids != nullptr, "vocab_ids is NULL (use dflash2_head_topk for the full vocabulary)");
+  REQUIRE(dtype == DFLASH2_BF16 || dtype == DFLASH2_F32, "dtype=%d is not DFLASH2_BF16 or DFLASH2_F32", dtype);
+  REQUIRE(M >= 1, "M=%d must be >= 1", M);
+  REQUIRE(H >= 64 && H % 64 == 0, "H=%d must be a positive multiple of 64", H);
+  REQUIRE(K >= 1 && K <= 16 && K <= V_listed, "K=%d must be in [1, min(16, V_listed)]", K);
+  REQUIRE(h && w_listed && cand && unary && workspace, "a required pointer is NULL");
+  REQUIRE((w_proj == nullptr) == (z == nullptr), "w_proj and z must be both set or both NULL");
+  if (w_proj != nullptr) REQUIRE(R >= 16 && R <= 256 && R % 16 == 0, "R=%d must be a multiple of 16 in [16, 256]", R);
+  REQUIRE(aligned16(h) && aligned16(w_listed) && (!w_proj || aligned16(w_proj)) && (!bias_listed || aligned16(bias_listed)),
+          "h, w_listed, w_proj and bias_listed must be 16-byte aligned");
+  REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "workspace must be 256-byte aligned");
+  const int r_eff = w_proj != nullptr ? R : 0;
+  const int sms = sm_count();
+  const size_t need = head_workspace(M, V_listed, K, r_eff, sms);
+  if (workspace_bytes < need)
+    return fail(DFLASH2_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", workspace_bytes,
+                need);
+  const GemmPlan plan = head_plan(M, H, V_listed, r_eff, sms);
+  const GemmProblem gp{h, w_listed, w_proj, M, H, V_listed, r_eff, dtype};
+  return launch_head_topk(gp, plan, bias_listed, K, cand, unary, z, logits, workspace,
+                          static_cast<cudaStream_t>(stream), vocab_ids);
+}
+
 int dflash2_score_edges(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
                         const void* pred_book, const void* succ_book, int B, int steps, int K, int R, int V, int dtype,
                         float* S, int32_t* path, void* stream) {

@@ -469,9 +469,10 @@ __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
 }
 
 // One warp per row: merge the per-split sorted lists into the row's top-K (value desc, id asc).
+// `ids_map` (nullable): token id of each column when the head ran over a draft vocabulary.
 __global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict__ lv, const int* __restrict__ li,
-                                                         int n_splits, int M, int K, int32_t* __restrict__ cand,
-                                                         float* __restrict__ unary) {
+                                                         int n_splits, int M, int K, const int32_t* __restrict__ ids_map,
+                                                         int32_t* __restrict__ cand, float* __restrict__ unary) {
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
@@ -524,7 +525,7 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict
       }
     }
     if (lane == 0) {
-      cand[static_cast<size_t>(row) * K + k] = bi;
+      cand[static_cast<size_t>(row) * K + k] = ids_map != nullptr ? __ldg(ids_map + bi) : bi;
       unary[static_cast<size_t>(row) * K + k] = bv;
     }
     if (ti[0] == bi) {  // ids are unique across lanes: the owner pops its head
@@ -670,7 +671,7 @@ int launch_gemm_store(const GemmProblem& p, const GemmPlan& plan, float* part, c
 }
 
 int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bias, int K, int32_t* cand,
-                     float* unary, float* z, float* logits, void* workspace, cudaStream_t st) {
+                     float* unary, float* z, float* logits, void* workspace, cudaStream_t st, const int32_t* ids_map) {
   CUtensorMap mA, mB, mE;
   GemmArgs a;
   int rc = prepare_args(p, plan, &mA, &mB, &mE, &a);
@@ -686,7 +687,7 @@ int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bi
   if (rc != DFLASH2_OK) return rc;
   const int rows_per_block = 8;
   topk_merge_kernel<<<(p.M + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0, st>>>(
-      a.list_val, a.list_idx, plan.n_splits, p.M, K, cand, unary);
+      a.list_val, a.list_idx, plan.n_splits, p.M, K, ids_map, cand, unary);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "topk_merge launch failed: %s", cudaGetErrorString(e));
   return DFLASH2_OK;

@@ -74,8 +74,10 @@ size_t head_workspace(int M, int V, int K, int R, int sms);
 int launch_gemm_store(const GemmProblem& p, const GemmPlan& plan, float* part, cudaStream_t st);
 // mode 1: per-row running top-16 over the main columns (+bias), z for the extra columns,
 // optional full logits; then a merge into cand/unary.
+// ids_map (nullable): token id of each weight row when the head runs over a draft vocabulary.
 int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bias, int K, int32_t* cand,
-                     float* unary, float* z, float* logits, void* workspace, cudaStream_t st);
+                     float* unary, float* z, float* logits, void* workspace, cudaStream_t st,
+                     const int32_t* ids_map = nullptr);
 int launch_wait_selftest(int limit_us, cudaStream_t st);
 
 // ---------------------------------------------------------------- selector (selector.cu)

@@ -160,6 +160,24 @@ DFLASH2_API int dflash2_head_topk(const void* h, int M, int H, const void* w_hea
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------------------
+ * Head + top-K over a draft vocabulary (dflash2.ts #block: a target that declares its draft
+ * vocabulary projects the head onto those rows only; #select: `ids` maps the columns of the
+ * logits over the draft vocabulary to token ids before the codebook gathers).
+ *
+ *   w_listed   [V_listed, H] dtype   the head rows of the listed vocabulary, in listed order.
+ *   vocab_ids  [V_listed] int32      the token id of each listed row (required).
+ *   bias_listed [V_listed] fp32 or NULL.
+ *   cand       [M, K] int32          TOKEN ids (vocab_ids of the chosen rows), ordered by value
+ *                                    descending; equal values keep the earlier listed row first.
+ *   Everything else (h, w_proj/z, unary, logits [M, V_listed], workspace sized by
+ *   dflash2_head_topk_workspace_bytes(M, H, V_listed, K, R)) is as for dflash2_head_topk.
+ * ---------------------------------------------------------------------------------- */
+DFLASH2_API int dflash2_head_topk_vocab(const void* h, int M, int H, const void* w_listed, int V_listed,
+                                        const int32_t* vocab_ids, const float* bias_listed, const void* w_proj, int R,
+                                        int K, int dtype, int32_t* cand, float* unary, float* z, float* logits,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------
  * Allocation-free variant of dflash2_head_topk. The pages describe no counterpart: this entry
  * point exists for callers that cannot allocate device memory when they run the head — code
  * inside a CUDA-graph capture or a latency-bound serving loop where cudaMalloc would stall or break

@@ -131,3 +131,11 @@ def test_binding_requires_cuda_tensors(lib):
     x = torch.zeros(1, 16, 64, dtype=torch.bfloat16)
     with pytest.raises((ValueError, RuntimeError)):
         d.dflash2_conv_finish(x, torch.zeros(1, 16, 2, 4, dtype=torch.bfloat16), torch.zeros(2, 2, 64), 16)
+
+
+def test_head_topk_vocab_rejects_bad_arguments(lib):
+    f = lib.dflash2_head_topk_vocab
+    #          h    M   H     w    V     ids   bias  wp    R   K   dt cand  un    z     lg    ws   wsb st
+    assert f(FAKE, 15, 5120, FAKE, 1000, None, None, FAKE, 64, 16, 0, FAKE, FAKE, FAKE, None, FAKE, 0, None) == -1
+    assert f(FAKE, 15, 5120, FAKE, 8, FAKE, None, FAKE, 64, 16, 0, FAKE, FAKE, FAKE, None, FAKE, 0, None) == -1
+    assert f(FAKE, 15, 5120, FAKE, 1000, FAKE, None, FAKE, 64, 16, 0, FAKE, FAKE, FAKE, None, FAKE, 0, None) == -4
