@@ -197,8 +197,7 @@ __global__ void __launch_bounds__(kApplyMaxThreads)
 // 2 x 128 rows), the N tile (64, 128 or 256 columns) and the number of K splits:
 //   issue:  k-blocks per CTA x MMAs per k-block x ~145 cycles (a tcgen05.mma of any N up to 256
 //           takes about that long, so wide tiles do more work per instruction)
-//   ingest: bytes each CTA pulls through TMA at ~100 GB/s per SM (measured: with a ~200 KB stage
-//           ring the in-flight bytes, not L2 bandwidth, cap what one SM can pull)
+//   ingest: bytes each CTA pulls through TMA at ~150 GB/s per SM
 //   stream: weight bytes / (CTAs x ~40 GB/s per SM)   (small M: spread the weight over the SMs)
 //   output: with 2..8 K splits the splits of a tile form a cluster and reduce through distributed
 //           shared memory (the sum is written once); otherwise each split stores fp32 partials
@@ -228,7 +227,7 @@ GemmPlan kp_plan(const ConvShape& s, int sms) {
       const double cols = 64.0 * tile_chunks;
       const double rows = std::min(M, 128 * mt);
       const double t_issue = waves * kb_per_cta * 4.0 * mt * 145.0 / 1.9e9;
-      const double t_ingest = waves * kb_per_cta * (mt * 16384.0 + tile_chunks * 8192.0) / 100e9;
+      const double t_ingest = waves * kb_per_cta * (mt * 16384.0 + tile_chunks * 8192.0) / 150e9;
       const double t_stream = w_bytes / (std::min(ctas, sms) * 40e9);
       double t_out;
       if (p.cluster_reduce)
