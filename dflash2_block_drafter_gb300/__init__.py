@@ -20,7 +20,7 @@ __all__ = [
     "Dflash2Error", "library", "library_path", "dflash2_version", "dflash2_poll_error",
     "dflash2_conv_prepare_workspace_bytes", "dflash2_conv_prepare", "dflash2_conv_finish",
     "dflash2_head_topk_workspace_bytes", "dflash2_head_topk", "dflash2_score_edges",
-    "dflash2_select_path", "dflash2_selftest_bounded_wait", "dflash2_head_topk_noalloc", "dflash2_head_topk_vocab", "dflash2_prefetch_l2", "DTYPE_CODES",
+    "dflash2_select_path", "dflash2_selftest_bounded_wait", "dflash2_head_topk_noalloc", "dflash2_head_topk_vocab", "DTYPE_CODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -48,7 +48,6 @@ _SIGNATURES = {
     "dflash2_select_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "dflash2_selftest_bounded_wait": (_i, [_i, _vp]),
     "dflash2_head_topk_noalloc": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
-    "dflash2_prefetch_l2": (_i, [_vp, _sz, _vp]),
     "dflash2_head_topk_vocab": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz,
                                      _vp]),
 }
@@ -242,11 +241,6 @@ def dflash2_select_path(S, cand, path=None, stream=None):
     _check(library().dflash2_select_path(_dev(S, "S", torch.float32), _dev(cand, "cand", torch.int32), B, steps, K,
                                          _dev(path, "path", torch.int32), _stream(stream)))
     return path
-
-
-def dflash2_prefetch_l2(t, stream=None):
-    """Ask L2 to fetch a device tensor's bytes (asynchronous; returns at once)."""
-    _check(library().dflash2_prefetch_l2(_dev(t, "tensor"), t.numel() * t.element_size(), _stream(stream)))
 
 
 def dflash2_selftest_bounded_wait(limit_us: int, stream=None):

@@ -248,13 +248,6 @@ int dflash2_select_path(const float* S, const int32_t* cand, int B, int steps, i
   return launch_select_path(S, cand, B, steps, K, path, static_cast<cudaStream_t>(stream));
 }
 
-int dflash2_prefetch_l2(const void* ptr, size_t bytes, void* stream) {
-  REQUIRE(ptr != nullptr, "ptr is NULL");
-  REQUIRE((reinterpret_cast<uintptr_t>(ptr) & 15u) == 0, "ptr must be 16-byte aligned");
-  if (bytes == 0) return DFLASH2_OK;
-  return launch_l2_prefetch(ptr, bytes, static_cast<cudaStream_t>(stream));
-}
-
 int dflash2_selftest_bounded_wait(int limit_us, void* stream) {
   REQUIRE(limit_us >= 1 && limit_us <= 1000000, "limit_us=%d must be in [1, 1000000]", limit_us);
   return launch_wait_selftest(limit_us, static_cast<cudaStream_t>(stream));

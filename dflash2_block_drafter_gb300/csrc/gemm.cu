@@ -609,18 +609,6 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict
   }
 }
 
-// L2 prefetch of a byte range: each thread asks L2 for one 64 KB piece (bulk prefetch, no data
-// returned to the SM). Fire and forget: the kernel ends as soon as the requests are issued.
-__global__ void __launch_bounds__(128) l2_prefetch_kernel(const uint8_t* base, size_t bytes) {
-  const size_t piece = 65536;
-  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const size_t off = i * piece;
-  if (off >= bytes) return;
-  const uint32_t len = static_cast<uint32_t>(((bytes - off < piece ? bytes - off : piece) + 15) & ~static_cast<size_t>(15));
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(base + off)), "r"(len)
-               : "memory");
-}
-
 // One thread waits on an mbarrier that nothing completes; the bounded wait gives up.
 __global__ void wait_selftest_kernel(uint64_t limit_ns, int* err) {
   __shared__ __align__(8) uint64_t bar;
@@ -789,15 +777,6 @@ int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bi
       a.list_val, a.list_idx, plan.n_splits, p.M, K, ids_map, cand, unary);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "topk_merge launch failed: %s", cudaGetErrorString(e));
-  return DFLASH2_OK;
-}
-
-int launch_l2_prefetch(const void* ptr, size_t bytes, cudaStream_t st) {
-  const size_t pieces = (bytes + 65535) / 65536;
-  const unsigned grid = static_cast<unsigned>((pieces + 127) / 128);
-  l2_prefetch_kernel<<<grid, 128, 0, st>>>(static_cast<const uint8_t*>(ptr), bytes);
-  const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "l2 prefetch launch failed: %s", cudaGetErrorString(e));
   return DFLASH2_OK;
 }
 

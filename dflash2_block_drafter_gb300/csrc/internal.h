@@ -83,7 +83,6 @@ int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bi
                      float* unary, float* z, float* logits, void* workspace, cudaStream_t st,
                      const int32_t* ids_map = nullptr);
 int launch_wait_selftest(int limit_us, cudaStream_t st);
-int launch_l2_prefetch(const void* ptr, size_t bytes, cudaStream_t st);
 
 // ---------------------------------------------------------------- selector (selector.cu)
 int launch_score_edges(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,

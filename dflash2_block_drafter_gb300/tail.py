@@ -20,7 +20,7 @@ import numpy as np
 import torch
 
 from . import (dflash2_conv_finish, dflash2_conv_prepare, dflash2_conv_prepare_workspace_bytes, dflash2_head_topk,
-               dflash2_head_topk_workspace_bytes, dflash2_prefetch_l2, dflash2_score_edges)
+               dflash2_head_topk_workspace_bytes, dflash2_score_edges)
 
 
 def to_device(a: np.ndarray, device="cuda") -> torch.Tensor:
@@ -50,9 +50,8 @@ class SiteWeights:
 class TailRunner:
     """One drafter tail (conv sites -> final norm -> selector) with preallocated buffers."""
 
-    def __init__(self, wl, device="cuda", with_selector: bool = True, prefetch_weights: bool = True):
+    def __init__(self, wl, device="cuda", with_selector: bool = True):
         self.wl = wl
-        self.prefetch_weights = prefetch_weights
         self.device = device
         self.dtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
         B, G, H = wl.B, wl.G, wl.H
@@ -88,8 +87,6 @@ class TailRunner:
         """Every site in order, starting from x0 (left unchanged); returns the final residual stream (self.x)."""
         wl = self.wl
         nsites = len(self.sites)
-        if nsites and self.prefetch_weights:
-            dflash2_prefetch_l2(self.sites[0].w_kp)
         for i, s in enumerate(self.sites):
             if i == 0:
                 dflash2_conv_prepare(x0, s.norm_w, wl.eps, s.w_kp, s.base, wl.gs, out=self.a, coef1=self.coef1,
@@ -97,9 +94,6 @@ class TailRunner:
             else:
                 dflash2_conv_prepare(self.n, None, wl.eps, s.w_kp, s.base, wl.gs, out=self.a, coef1=self.coef1,
                                      workspace=self.conv_ws)
-            if i + 1 < nsites and self.prefetch_weights:
-                # the next site's weight streams into L2 while this site's apply passes run
-                dflash2_prefetch_l2(self.sites[i + 1].w_kp)
             residual = x0 if i == 0 else self.x
             if i + 1 < nsites:
                 dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=residual, out=self.x,
@@ -111,18 +105,10 @@ class TailRunner:
                 dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=residual, out=self.x)
         return self.x
 
-    def launches_per_pass(self, conv: bool = True, selector: bool = True, emit_h: bool = True) -> int:
-        """Library kernels one pass launches: the first site's RMSNorm; per site a kernel_projection
-        GEMM, a side-0 pass, a side-1 pass, the next RMSNorm (not after the last site of a chain
-        that emits no h) and an L2 prefetch of its weight; then the head GEMM + top-K merge and the
-        fused edge-score/walk kernel."""
-        n = 0
-        ns = len(self.sites)
-        if conv and ns:
-            n += 1 + 3 * ns + (ns if emit_h else ns - 1) + (ns if self.prefetch_weights else 0)
-        if selector and self.with_selector:
-            n += 3
-        return n
+    def launches_per_pass(self) -> int:
+        """Library kernels one full() pass launches: RMSNorm once, per site a GEMM + side-0 pass and a
+        side-1 pass, then the head GEMM + merge and the fused edge-score/walk kernel."""
+        return 1 + 3 * len(self.sites) + (3 if self.with_selector else 0)
 
     def selector(self, h: torch.Tensor, anchors: torch.Tensor, want_S: bool = True):
         wl = self.wl

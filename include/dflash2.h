@@ -221,12 +221,6 @@ DFLASH2_API int dflash2_score_edges(const int32_t* cand, const float* unary, con
  * 1 <= steps, 1 <= K <= 32. */
 DFLASH2_API int dflash2_select_path(const float* S, const int32_t* cand, int B, int steps, int K, int32_t* path, void* stream);
 
-/* Asks L2 to fetch `bytes` of device memory starting at `ptr` (16-byte aligned), asynchronously on
- * `stream`: the launch only issues bulk L2 prefetch requests and returns. Used to bring the next
- * conv site's kernel_projection weight into L2 while the current site's apply passes run, so that
- * the next GEMM's short mainloop streams from L2 instead of DRAM. Has no counterpart on the pages. */
-DFLASH2_API int dflash2_prefetch_l2(const void* ptr, size_t bytes, void* stream);
-
 /* Self-test of the bounded-wait machinery: launches one block that waits on an mbarrier that
  * nothing completes, with a limit of `limit_us` microseconds (1..1000000). The wait gives up,
  * records DFLASH2_ERR_TIMEOUT in the device error word and the kernel returns; read it with
