@@ -148,7 +148,7 @@ int dflash2_conv_prepare(const void* x, const void* norm_w, float eps, const voi
   const GemmProblem gp{n, w_kp, nullptr, s.rows(), H, 4 * s.groups, 0, dtype};
   rc = launch_gemm_store(gp, plan, part, st);
   if (rc != DFLASH2_OK) return rc;
-  return launch_conv_side0(s, n, part, plan.cluster_reduce ? 1 : plan.k_splits, base, out, coef1, d_full, st);
+  return launch_conv_side0(s, n, part, plan.k_splits, base, out, coef1, d_full, st);
 }
 
 int dflash2_conv_finish(const void* y, const void* coef1, const float* base, int B, int G, int H, int group_size,

@@ -1,8 +1,5 @@
 // Tensor-core GEMM for sm_103a (tcgen05 + TMEM + TMA), with two epilogues:
 //   * STORE: fp32 split-K partial sums (kernel_projection of the grouped conv);
-//   * REDUCE: the K splits of one tile form a thread-block cluster; each CTA stages its partial
-//            accumulator in shared memory and the CTAs sum disjoint row ranges across the cluster
-//            through distributed shared memory, so the result is written to memory once;
 //   * TOPK : per-row running top-16 of the logits (+bias), the extra columns written as z
 //            (hidden_projection folded in as 64-row chunks after the vocabulary), optional
 //            full logits. Full-vocabulary logits never reach memory unless asked for.
@@ -138,21 +135,11 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Grid order: (mg fastest, ns, ks), or (ks fastest, mg, ns) for REDUCE, where the k_splits CTAs
-  // of one tile are consecutive and form one cluster (cluster rank = ks).
   int bid = blockIdx.x;
-  int mg, ns, ks;
-  if (MODE == 2) {
-    ks = bid % a.k_splits;
-    bid /= a.k_splits;
-    mg = bid % a.m_groups;
-    ns = bid / a.m_groups;
-  } else {
-    mg = bid % a.m_groups;
-    bid /= a.m_groups;
-    ns = bid % a.n_splits;
-    ks = bid / a.n_splits;
-  }
+  const int mg = bid % a.m_groups;
+  bid /= a.m_groups;
+  const int ns = bid % a.n_splits;
+  const int ks = bid / a.n_splits;
   const int c_begin = static_cast<int>((static_cast<long long>(a.n_chunks) * ns) / a.n_splits);
   const int c_end = static_cast<int>((static_cast<long long>(a.n_chunks) * (ns + 1)) / a.n_splits);
   const int kb0 = static_cast<int>((static_cast<long long>(a.k_blocks) * ks) / a.k_splits);
@@ -346,7 +333,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
         break;
       }
       tc_fence_after();
-      if (MODE != 2 && tile_ok) {
+      if (tile_ok) {
         const bool extra = t0 >= a.main_chunks;
         for (int cc = 0; cc < nch * 2; ++cc) {
           uint32_t r[32];
@@ -470,62 +457,6 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (MODE == 2) {
-    // Split-K reduction across the cluster, one 128-row M tile at a time. The stage ring is idle
-    // (the CTA's single tile is fully consumed), so it holds the staged partial tile:
-    // red[128][ncols + 4] fp32, rows padded against bank conflicts.
-    tc_fence_after();
-    int c = c_begin, t0 = 0, nch = 0;
-    next_tile(c, c_end, a.main_chunks, t0, nch);
-    const int ncols = nch * kChunk;
-    const int rstride = ncols + 4;
-    float* red = reinterpret_cast<float*>(smem);
-    const uint32_t red_s = smem_u32(red);
-    const int kc = a.k_splits;
-    const int rows_per = (128 + kc - 1) / kc;
-    const int r_lo = min(128, ks * rows_per);
-    const int r_hi = min(128, r_lo + rows_per);
-    for (int mt = 0; mt < MT; ++mt) {
-      if (warp >= 2 && ((warp - 2) >> 2) == mt && mt < mt_valid) {
-        const int q = warp & 3;
-        float* my = red + (q * 32 + lane) * rstride;
-        for (int cc = 0; cc < nch * 2; ++cc) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(mt * 256 + cc * 32),
-                             r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(my + cc * 32 + j) =
-                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                            __uint_as_float(r[j + 3]));
-        }
-      }
-      cluster_sync_all();  // every CTA's partial tile is staged
-      if (warp >= 2 && mt < mt_valid) {
-        const int et = threadIdx.x - 64;
-        const int c4n = ncols / 4;
-        for (int idx = et; idx < (r_hi - r_lo) * c4n; idx += C::kEpiThreads) {
-          const int rr = r_lo + idx / c4n;
-          const int c4 = idx - (idx / c4n) * c4n;
-          const uint32_t off = static_cast<uint32_t>((rr * rstride + c4 * 4) * 4);
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int pr = 0; pr < kc; ++pr) {  // fixed order: the sum is deterministic
-            const float4 v = ld_shared_cluster_f4(mapa_shared(red_s + off, static_cast<uint32_t>(pr)));
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-          }
-          const int grow = row0 + mt * 128 + rr;
-          const int gcol = t0 * kChunk + c4 * 4;
-          if (grow < a.M && gcol < a.n_main)
-            *reinterpret_cast<float4*>(a.part + static_cast<size_t>(grow) * a.n_main + gcol) = acc;
-        }
-      }
-      cluster_sync_all();  // peers are done reading this CTA's staged tile
-    }
-  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
@@ -661,23 +592,6 @@ int launch_tc(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& m
   auto kern = tc_gemm_kernel<MT, TF32, MODE>;
   if (!ensure_smem_attr(kern, Cfg<MT>::kSmem, &done))
     return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(cudaGetLastError()));
-  if (MODE == 2) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(Cfg<MT>::kThreads);
-    cfg.dynamicSmemBytes = Cfg<MT>::kSmem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = args.k_splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, mA, mB, mE, args);
-    if (le != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "tc_gemm (cluster) launch failed: %s", cudaGetErrorString(le));
-    return DFLASH2_OK;
-  }
   kern<<<grid, Cfg<MT>::kThreads, Cfg<MT>::kSmem, st>>>(mA, mB, mE, args);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "tc_gemm launch failed: %s", cudaGetErrorString(e));
@@ -753,7 +667,6 @@ int launch_gemm_store(const GemmProblem& p, const GemmPlan& plan, float* part, c
   if (rc != DFLASH2_OK) return rc;
   a.part = part;
   const int grid = plan.m_groups * plan.n_splits * plan.k_splits;
-  if (plan.cluster_reduce) return dispatch_tc<2>(plan.mt, p.dtype == DFLASH2_F32, mA, mB, mE, a, grid, st);
   return dispatch_tc<0>(plan.mt, p.dtype == DFLASH2_F32, mA, mB, mE, a, grid, st);
 }
 

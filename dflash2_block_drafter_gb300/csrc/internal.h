@@ -65,16 +65,12 @@ struct GemmPlan {
   int n_splits;  // column ranges (balanced over 64-column chunks)
   int k_splits;  // reduction ranges (STORE mode only)
   int n_chunks;  // 64-column chunks over the virtual range
-  // STORE only: the k_splits CTAs of a tile form a cluster and reduce through distributed shared
-  // memory, writing the summed result once ([M][n_main]) instead of k_splits partials.
-  bool cluster_reduce;
 };
 // Split-K plan of the kernel_projection GEMM; shared by the workspace query and the launch.
 GemmPlan kp_plan(const ConvShape& s, int sms);
 GemmPlan head_plan(int M, int K, int n_main, int n_extra, int sms);
 size_t head_workspace(int M, int V, int K, int R, int sms);
-// mode 0: write fp32 partial sums part[k_split][M][n_main]; with plan.cluster_reduce the sum
-// part[M][n_main] itself.
+// mode 0: write fp32 partial sums part[k_split][M][n_main].
 int launch_gemm_store(const GemmProblem& p, const GemmPlan& plan, float* part, cudaStream_t st);
 // mode 1: per-row running top-16 over the main columns (+bias), z for the extra columns,
 // optional full logits; then a merge into cand/unary.
