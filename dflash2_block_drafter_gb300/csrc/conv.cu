@@ -193,14 +193,16 @@ __global__ void __launch_bounds__(kApplyMaxThreads)
 
 }  // namespace
 
-// Split-K plan of kernel_projection: 128-row M tiles; the N tile (64, 128 or 256 columns) and the
-// number of K splits are picked by a small cost model, so that the weight stream is spread over
-// the SMs at small M and the tensor pipe is used efficiently at large M:
-//   issue:    k-blocks per CTA x 4 MMAs x ~145 cycles (a tcgen05.mma of any N up to 256 takes about
-//             that long to issue, so wide tiles do more work per instruction)
-//   stream:   weight bytes / (CTAs x ~40 GB/s per SM)
-//   partials: fp32 split-K partials written and read back by the side-0 pass (~5 TB/s)
-// cost = max(issue, stream) + partials.
+// Split-K plan of kernel_projection, picked by a small cost model over the M tiles per CTA (1 or
+// 2 x 128 rows), the N tile (64, 128 or 256 columns) and the number of K splits:
+//   issue:   k-blocks per CTA x MMAs per k-block x ~145 cycles (a tcgen05.mma of any N up to 256
+//            takes about that long, so wide tiles do more work per instruction)
+//   ingest:  bytes each CTA pulls through TMA at ~100 GB/s per SM (measured: with a ~200 KB stage
+//            ring the bytes in flight, not L2 bandwidth, cap what one SM can pull)
+//   stream:  weight bytes / (CTAs x ~40 GB/s per SM)   (small M: spread the weight over the SMs)
+//   output:  each CTA's fp32 tile leaves at ~16 GB/s per SM (measured), and with K splits the
+//            partials are read back by the side-0 pass (~5 TB/s)
+// cost = max(issue, ingest, stream) + output.
 GemmPlan kp_plan(const ConvShape& s, int sms) {
   const int M = s.rows();
   const int N = 4 * s.groups;
@@ -209,24 +211,30 @@ GemmPlan kp_plan(const ConvShape& s, int sms) {
   const double w_bytes = 2.0 * N * s.H;
   GemmPlan best{};
   double best_cost = 1e30;
-  for (int tile_chunks = 4; tile_chunks >= 1; tile_chunks /= 2) {
-    GemmPlan p{};
-    p.mt = 1;
-    p.m_groups = (M + 127) / 128;
-    p.n_chunks = (N + 63) / 64;
-    p.n_splits = (p.n_chunks + tile_chunks - 1) / tile_chunks;
-    const int units = p.m_groups * p.n_splits;
-    p.k_splits = std::max(1, std::min(std::min(k_blocks, 32), sms / std::max(1, units)));
-    const int ctas = units * p.k_splits;
-    const int waves = (ctas + sms - 1) / sms;
-    const double kb_per_cta = static_cast<double>(k_blocks) / p.k_splits;
-    const double t_issue = waves * kb_per_cta * 4.0 * 145.0 / 1.9e9;
-    const double t_stream = w_bytes / (std::min(ctas, sms) * 40e9);
-    const double t_part = p.k_splits > 1 ? p.k_splits * static_cast<double>(M) * N * 8.0 / 5e12 : 0.0;
-    const double cost = std::max(t_issue, t_stream) + t_part;
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = p;
+  for (int mt = 1; mt <= (M > 128 ? 2 : 1); ++mt) {
+    for (int tile_chunks = 4; tile_chunks >= 1; tile_chunks /= 2) {
+      GemmPlan p{};
+      p.mt = mt;
+      p.m_groups = (M + 128 * mt - 1) / (128 * mt);
+      p.n_chunks = (N + 63) / 64;
+      p.n_splits = (p.n_chunks + tile_chunks - 1) / tile_chunks;
+      const int units = p.m_groups * p.n_splits;
+      p.k_splits = std::max(1, std::min(std::min(k_blocks, 32), sms / std::max(1, units)));
+      const int ctas = units * p.k_splits;
+      const int waves = (ctas + sms - 1) / sms;
+      const double kb_per_cta = static_cast<double>(k_blocks) / p.k_splits;
+      const double cols = 64.0 * tile_chunks;
+      const double rows = std::min(M, 128 * mt);
+      const double t_issue = waves * kb_per_cta * 4.0 * mt * 145.0 / 1.9e9;
+      const double t_ingest = waves * kb_per_cta * (mt * 16384.0 + tile_chunks * 8192.0) / 100e9;
+      const double t_stream = w_bytes / (std::min(ctas, sms) * 40e9);
+      const double t_out = waves * rows * cols * 4.0 / 16e9 +
+                           (p.k_splits > 1 ? p.k_splits * static_cast<double>(M) * N * 8.0 / 5e12 : 0.0);
+      const double cost = std::max(std::max(t_issue, t_ingest), t_stream) + t_out;
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = p;
+      }
     }
   }
   return best;
