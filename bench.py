@@ -362,8 +362,8 @@ def our_arm(args, wl_name):
         if traffic is not None:
             roofline["traffic"] = traffic
 
-    launches = run.launches_per_pass() if full_tail else (
-        (1 + 3 * len(wl.sites)) if wl.sites else 3)
+    launches = run.launches_per_pass(conv=bool(wl.sites), selector=run.with_selector,
+                                     emit_h=run.with_selector)
     line = {
         "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",

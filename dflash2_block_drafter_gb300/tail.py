@@ -105,10 +105,17 @@ class TailRunner:
                 dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=residual, out=self.x)
         return self.x
 
-    def launches_per_pass(self) -> int:
-        """Library kernels one full() pass launches: RMSNorm once, per site a GEMM + side-0 pass and a
-        side-1 pass, then the head GEMM + merge and the fused edge-score/walk kernel."""
-        return 1 + 3 * len(self.sites) + (3 if self.with_selector else 0)
+    def launches_per_pass(self, conv: bool = True, selector: bool = True, emit_h: bool = True) -> int:
+        """Library kernels one pass launches: the first site's RMSNorm; per site a kernel_projection
+        GEMM, a side-0 pass, a side-1 pass and the next RMSNorm (not after the last site of a chain
+        that emits no h); then the head GEMM + top-K merge and the fused edge-score/walk kernel."""
+        n = 0
+        ns = len(self.sites)
+        if conv and ns:
+            n += 1 + 3 * ns + (ns if emit_h else ns - 1)
+        if selector and self.with_selector:
+            n += 3
+        return n
 
     def selector(self, h: torch.Tensor, anchors: torch.Tensor, want_S: bool = True):
         wl = self.wl
