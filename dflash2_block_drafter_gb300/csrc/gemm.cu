@@ -97,6 +97,21 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* err) 
   if (err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_TIMEOUT));
 }
 
+// v[j] for a run-time j in [0, 32) without local memory: a 5-level select tree on the bits of j
+// (depth 5 instead of a 31-long dependent chain).
+__device__ __forceinline__ float select32(const float (&v)[32], int j) {
+  float a[16], b[8], c[4], d[2];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) a[k] = (j & 1) ? v[2 * k + 1] : v[2 * k];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) b[k] = (j & 2) ? a[2 * k + 1] : a[2 * k];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) c[k] = (j & 4) ? b[2 * k + 1] : b[2 * k];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) d[k] = (j & 8) ? c[2 * k + 1] : c[2 * k];
+  return (j & 16) ? d[1] : d[0];
+}
+
 // Insert (x, id) into a descending 16-entry list held in registers, dropping the last entry.
 // Branch-free and fully unrolled; equal values stay behind earlier (lower-id) entries.
 __device__ __forceinline__ void list_insert(float (&tv)[kTopL], int (&ti)[kTopL], float x, int id) {
@@ -432,9 +447,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
               if (cmask != 0u) {
                 const int jj = __ffs(cmask) - 1;
                 cmask &= cmask - 1u;
-                float x = v[0];
-#pragma unroll
-                for (int q = 1; q < 32; ++q) x = (jj == q) ? v[q] : x;
+                const float x = select32(v, jj);
                 if (x > tv[kTopL - 1]) list_insert(tv, ti, x, col0 + jj);
               }
             }
