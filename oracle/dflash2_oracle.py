@@ -250,6 +250,31 @@ def select_path(S, cand, seed_index: int = 0):
     return path, pos
 
 
+def select_path_depths(S, cand, depths):
+    """The greedy walk of blocks that draft different numbers of tokens in one batch.
+
+    [ts] ``blockColumns`` / ``#block`` (a block runs over ``columns = min(G, depth + 1)`` rows: the
+    anchor and ``depth`` mask rows, so it drafts ``depth`` tokens). Block b walks only its first
+    ``depths[b]`` slots; the slots after them hold -1 (no token). Rows past a block's depth are
+    padding in a dense [B, G, ...] batch.
+    Returns (path ids [B, steps] with -1 padding, chosen positions [B, steps] with -1 padding).
+    """
+    S = _f64(S)
+    cand = np.asarray(cand)
+    B, steps, K, _ = S.shape
+    pos = np.full((B, steps), -1, dtype=np.int64)
+    path = np.full((B, steps), -1, dtype=np.int64)
+    for b in range(B):
+        d = int(depths[b])
+        p = 0
+        for l in range(d):
+            c = int(np.argmax(S[b, l, p, :]))
+            pos[b, l] = c
+            path[b, l] = cand[b, l, c]
+            p = c
+    return path, pos
+
+
 def walk_margins(S, pos) -> np.ndarray:
     """Per (b, l): best minus second-best of the row the walk read at slot l (its tie margin)."""
     S = _f64(S)

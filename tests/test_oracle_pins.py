@@ -428,3 +428,40 @@ def test_listed_vocabulary_identity_map():
     W = _rand(V, H)
     cols, _ = O.top_k(O.head_logits(h, W), K)
     assert np.array_equal(O.listed_candidates(cols, np.arange(V)), cols)
+
+
+def test_mixed_depth_walk_is_prefix_of_full_walk():
+    # The walk is causal: a block that drafts d tokens chooses exactly the first d tokens of the
+    # full-depth walk, followed by -1 padding; d = steps reproduces the full walk.
+    B, steps, K, R, V = 6, 7, 5, 8, 60
+    cand = RNG.integers(0, V, size=(B, steps, K))
+    unary = _rand(B, steps, K)
+    z = _rand(B, steps, R)
+    anchors = RNG.integers(0, V, size=B)
+    S = O.score_edges(cand, unary, z, anchors, _rand(V, R), _rand(V, R))
+    full, full_pos = O.select_path(S, cand)
+    depths = np.array([1, 7, 3, 0, 5, 2])
+    path, pos = O.select_path_depths(S, cand, depths)
+    for b in range(B):
+        d = depths[b]
+        assert np.array_equal(path[b, :d], full[b, :d])
+        assert np.array_equal(pos[b, :d], full_pos[b, :d])
+        assert np.all(path[b, d:] == -1) and np.all(pos[b, d:] == -1)
+    p2, _ = O.select_path_depths(S, cand, np.full(B, steps))
+    assert np.array_equal(p2, full)
+
+
+def test_conv_rows_past_depth_do_not_reach_earlier_rows():
+    # A block of G rows whose rows past d+1 are arbitrary padding gives, on its first d+1 rows,
+    # exactly the conv of the (d+1)-row block: the conv only looks back one row.
+    B, G, H, gs, d = 3, 9, 32, 16, 4
+    x = _rand(B, G, H)
+    y = _rand(B, G, H)
+    w = _rand(4 * H // gs, H, scale=0.2)
+    base = _rand(2, 2, H)
+    out, d1, _ = O.conv_prepare(x, np.ones(H), 1e-6, w, base, gs)
+    fin = O.conv_finish(y, d1, base, gs, residual=x)
+    out_s, d1_s, _ = O.conv_prepare(x[:, :d + 1], np.ones(H), 1e-6, w, base, gs)
+    fin_s = O.conv_finish(y[:, :d + 1], d1_s, base, gs, residual=x[:, :d + 1])
+    assert np.array_equal(out[:, :d + 1], out_s)
+    assert np.array_equal(fin[:, :d + 1], fin_s)
