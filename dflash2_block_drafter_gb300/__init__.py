@@ -20,7 +20,8 @@ __all__ = [
     "Dflash2Error", "library", "library_path", "dflash2_version", "dflash2_poll_error",
     "dflash2_conv_prepare_workspace_bytes", "dflash2_conv_prepare", "dflash2_conv_finish",
     "dflash2_head_topk_workspace_bytes", "dflash2_head_topk", "dflash2_score_edges",
-    "dflash2_select_path", "dflash2_selftest_bounded_wait", "dflash2_head_topk_noalloc", "dflash2_head_topk_vocab", "DTYPE_CODES",
+    "dflash2_select_path", "dflash2_selftest_bounded_wait", "dflash2_head_topk_noalloc", "dflash2_head_topk_vocab", "dflash2_score_edges_depths", "dflash2_select_path_depths",
+    "DTYPE_CODES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -48,6 +49,8 @@ _SIGNATURES = {
     "dflash2_select_path": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "dflash2_selftest_bounded_wait": (_i, [_i, _vp]),
     "dflash2_head_topk_noalloc": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
+    "dflash2_score_edges_depths": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp]),
+    "dflash2_select_path_depths": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
     "dflash2_head_topk_vocab": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz,
                                      _vp]),
 }
@@ -273,3 +276,32 @@ def dflash2_head_topk_noalloc(h, w_head, K, bias=None, w_proj=None, cand=None, u
         _dev(unary, "unary", torch.float32), _dev(z, "z", torch.float32, True),
         _dev(logits, "logits", torch.float32, True), _stream(stream)))
     return cand, unary, z, logits
+
+
+def dflash2_score_edges_depths(cand, unary, z, anchors, pred_book, succ_book, depths, want_S=True, S=None, path=None,
+                               stream=None):
+    """Edge scores + the greedy walk for a mixed-depth batch: block b walks depths[b] (int32) slots,
+    later path entries are -1. Returns (S or None, path)."""
+    B, steps, K = cand.shape
+    R = z.shape[-1]
+    V = pred_book.shape[0]
+    dev = cand.device
+    if want_S and S is None:
+        S = torch.empty((B, steps, K, K), dtype=torch.float32, device=dev)
+    path = torch.empty((B, steps), dtype=torch.int32, device=dev) if path is None else path
+    _check(library().dflash2_score_edges_depths(
+        _dev(cand, "cand", torch.int32), _dev(unary, "unary", torch.float32), _dev(z, "z", torch.float32),
+        _dev(anchors, "anchors", torch.int32), _dev(pred_book, "pred_book", pred_book.dtype),
+        _dev(succ_book, "succ_book", pred_book.dtype), _dev(depths, "depths", torch.int32), B, steps, K, R, V,
+        _code(pred_book), _dev(S, "S", torch.float32, True), _dev(path, "path", torch.int32), _stream(stream)))
+    return S, path
+
+
+def dflash2_select_path_depths(S, cand, depths, path=None, stream=None):
+    """Greedy walk over S for a mixed-depth batch; returns path [B, steps] with -1 padding."""
+    B, steps, K, _ = S.shape
+    path = torch.empty((B, steps), dtype=torch.int32, device=S.device) if path is None else path
+    _check(library().dflash2_select_path_depths(_dev(S, "S", torch.float32), _dev(cand, "cand", torch.int32),
+                                                _dev(depths, "depths", torch.int32), B, steps, K,
+                                                _dev(path, "path", torch.int32), _stream(stream)))
+    return path

@@ -241,6 +241,30 @@ int dflash2_score_edges(const int32_t* cand, const float* unary, const float* z,
                             static_cast<cudaStream_t>(stream));
 }
 
+int dflash2_score_edges_depths(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
+                               const void* pred_book, const void* succ_book, const int32_t* depths, int B, int steps,
+                               int K, int R, int V, int dtype, float* S, int32_t* path, void* stream) {
+  REQUIRE(depths != nullptr, "depths is NULL (use dflash2_score_edges for full-depth blocks)");
+  REQUIRE(dtype == DFLASH2_BF16 || dtype == DFLASH2_F32, "dtype=%d is not DFLASH2_BF16 or DFLASH2_F32", dtype);
+  REQUIRE(B >= 1 && steps >= 1 && steps <= 63, "B=%d, steps=%d: need B >= 1 and 1 <= steps <= 63", B, steps);
+  REQUIRE(K >= 1 && K <= 32, "K=%d must be in [1, 32]", K);
+  REQUIRE(R >= 8 && R <= 128 && R % 8 == 0, "R=%d must be a multiple of 8 in [8, 128]", R);
+  REQUIRE(V >= 1, "V=%d must be >= 1", V);
+  REQUIRE(cand && unary && z && anchors && pred_book && succ_book && path, "a required pointer is NULL");
+  REQUIRE(aligned16(z) && aligned16(pred_book) && aligned16(succ_book), "z and the codebooks must be 16-byte aligned");
+  return launch_score_edges(cand, unary, z, anchors, pred_book, succ_book, B, steps, K, R, V, dtype, S, path,
+                            static_cast<cudaStream_t>(stream), depths);
+}
+
+int dflash2_select_path_depths(const float* S, const int32_t* cand, const int32_t* depths, int B, int steps, int K,
+                               int32_t* path, void* stream) {
+  REQUIRE(depths != nullptr, "depths is NULL (use dflash2_select_path for full-depth blocks)");
+  REQUIRE(B >= 1 && steps >= 1, "B=%d, steps=%d must be >= 1", B, steps);
+  REQUIRE(K >= 1 && K <= 32, "K=%d must be in [1, 32]", K);
+  REQUIRE(S && cand && path, "a required pointer is NULL");
+  return launch_select_path(S, cand, B, steps, K, path, static_cast<cudaStream_t>(stream), depths);
+}
+
 int dflash2_select_path(const float* S, const int32_t* cand, int B, int steps, int K, int32_t* path, void* stream) {
   REQUIRE(B >= 1 && steps >= 1, "B=%d, steps=%d must be >= 1", B, steps);
   REQUIRE(K >= 1 && K <= 32, "K=%d must be in [1, 32]", K);

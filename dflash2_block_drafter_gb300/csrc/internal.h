@@ -81,10 +81,11 @@ int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bi
 int launch_wait_selftest(int limit_us, cudaStream_t st);
 
 // ---------------------------------------------------------------- selector (selector.cu)
+// depths (nullable): per-block draft length of a mixed-depth batch; slots past it get path -1.
 int launch_score_edges(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
                        const void* pred, const void* succ, int B, int steps, int K, int R, int V, int dtype,
-                       float* S, int32_t* path, cudaStream_t st);
+                       float* S, int32_t* path, cudaStream_t st, const int32_t* depths = nullptr);
 int launch_select_path(const float* S, const int32_t* cand, int B, int steps, int K, int32_t* path,
-                       cudaStream_t st);
+                       cudaStream_t st, const int32_t* depths = nullptr);
 
 }  // namespace dfl

@@ -54,13 +54,26 @@ __device__ __forceinline__ int warp_argmax(float v, int K) {
   return bi;
 }
 
+// Draft length of block b: depths[b] slots (the rest of the block's rows are padding of a
+// mixed-depth batch; dflash2.ts blockColumns), all `steps` without a depths array. A value
+// outside [0, steps] records DFLASH2_ERR_INVALID_ARG in the error word and is clamped.
+__device__ __forceinline__ int block_depth(const int32_t* depths, int b, int steps, int* err) {
+  if (depths == nullptr) return steps;
+  const int d = depths[b];
+  if (d < 0 || d > steps) {
+    if (err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_INVALID_ARG));
+    return d < 0 ? 0 : steps;
+  }
+  return d;
+}
+
 // Slots are processed in chunks of `lchunk` (all of them at once at the drafter's shape).
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
     score_edges_kernel(const int32_t* __restrict__ cand, const float* __restrict__ unary, const float* __restrict__ z,
                        const int32_t* __restrict__ anchors, const T* __restrict__ pred, const T* __restrict__ succ,
                        int steps, int K, int R, int V, int lchunk, float* __restrict__ S, int32_t* __restrict__ path,
-                       int* err) {
+                       const int32_t* __restrict__ depths, int* err) {
   extern __shared__ float sm[];
   const int b = blockIdx.x;
   const int RP = R + 1;  // padded row: the K successor rows of a slot fall in distinct banks
@@ -123,24 +136,29 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
   }
   if (path != nullptr && tid < 32) {
+    const int d = block_depth(depths, b, steps, err);
     int p = 0;
-    for (int l = 0; l < steps; ++l) {
+    for (int l = 0; l < d; ++l) {
       const float v = tid < K ? sS[(l * K + p) * K + tid] : -INFINITY;
       const int c = warp_argmax(v, K);
       if (tid == 0) path[static_cast<size_t>(b) * steps + l] = sid[l * K + c];
       p = c;
     }
+    for (int l = d + tid; l < steps; l += 32) path[static_cast<size_t>(b) * steps + l] = -1;
   }
 }
 
 // The walk alone over a given S: one warp per block.
 __global__ void __launch_bounds__(128) select_path_kernel(const float* __restrict__ S, const int32_t* __restrict__ cand,
-                                                          int B, int steps, int K, int32_t* __restrict__ path) {
+                                                          int B, int steps, int K, int32_t* __restrict__ path,
+                                                          const int32_t* __restrict__ depths, int* err) {
   const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
+  const int d = block_depth(depths, b, steps, err);
+  for (int l = d + lane; l < steps; l += 32) path[static_cast<size_t>(b) * steps + l] = -1;
   int p = 0;
-  for (int l = 0; l < steps; ++l) {
+  for (int l = 0; l < d; ++l) {
     const size_t rowoff = ((static_cast<size_t>(b) * steps + l) * K + p) * K;
     const float v = lane < K ? S[rowoff + lane] : -INFINITY;
     const int c = warp_argmax(v, K);
@@ -158,7 +176,7 @@ size_t edges_smem(int steps, int K, int R, int lchunk) {
 
 int launch_score_edges(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
                        const void* pred, const void* succ, int B, int steps, int K, int R, int V, int dtype,
-                       float* S, int32_t* path, cudaStream_t st) {
+                       float* S, int32_t* path, cudaStream_t st, const int32_t* depths) {
   int lchunk = steps;
   while (lchunk > 1 && edges_smem(steps, K, R, lchunk) > static_cast<size_t>(kSmemBudget)) --lchunk;
   const size_t smem = edges_smem(steps, K, R, lchunk);
@@ -171,21 +189,21 @@ int launch_score_edges(const int32_t* cand, const float* unary, const float* z, 
     if (e == cudaSuccess)
       score_edges_kernel<float><<<B, kThreads, smem, st>>>(cand, unary, z, anchors, static_cast<const float*>(pred),
                                                            static_cast<const float*>(succ), steps, K, R, V, lchunk, S,
-                                                           path, device_error_word());
+                                                           path, depths, device_error_word());
   } else {
     if (!ensure_smem_attr(score_edges_kernel<__nv_bfloat16>, kSmemBudget, &done_bf16)) e = cudaErrorInvalidValue;
     if (e == cudaSuccess)
       score_edges_kernel<__nv_bfloat16><<<B, kThreads, smem, st>>>(
           cand, unary, z, anchors, static_cast<const __nv_bfloat16*>(pred), static_cast<const __nv_bfloat16*>(succ),
-          steps, K, R, V, lchunk, S, path, device_error_word());
+          steps, K, R, V, lchunk, S, path, depths, device_error_word());
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "score_edges launch failed: %s", cudaGetErrorString(e));
 }
 
 int launch_select_path(const float* S, const int32_t* cand, int B, int steps, int K, int32_t* path,
-                       cudaStream_t st) {
-  select_path_kernel<<<(B + 3) / 4, 128, 0, st>>>(S, cand, B, steps, K, path);
+                       cudaStream_t st, const int32_t* depths) {
+  select_path_kernel<<<(B + 3) / 4, 128, 0, st>>>(S, cand, B, steps, K, path, depths, device_error_word());
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "select_path launch failed: %s", cudaGetErrorString(e));
 }

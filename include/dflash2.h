@@ -221,6 +221,21 @@ DFLASH2_API int dflash2_score_edges(const int32_t* cand, const float* unary, con
  * 1 <= steps, 1 <= K <= 32. */
 DFLASH2_API int dflash2_select_path(const float* S, const int32_t* cand, int B, int steps, int K, int32_t* path, void* stream);
 
+/* Mixed-depth batches (dflash2.ts blockColumns / #block: a block drafting `depth` tokens runs over
+ * its anchor and `depth` mask rows). In a dense [B, G, ...] batch block b may draft only
+ * depths[b] <= G-1 tokens; its rows past depths[b] + 1 are padding. The conv and the head need no
+ * change for that (the conv only looks one row back, and the head works row by row), so only the
+ * walk honours the depths: block b walks slots [0, depths[b]) and path[b, l] = -1 for later slots.
+ *   depths [B] int32 in [0, steps] (device; a value outside records DFLASH2_ERR_INVALID_ARG in the
+ *   device error word and is clamped). Other arguments as for dflash2_score_edges /
+ *   dflash2_select_path; path is required. S (if requested) is computed for every slot. */
+DFLASH2_API int dflash2_score_edges_depths(const int32_t* cand, const float* unary, const float* z,
+                                           const int32_t* anchors, const void* pred_book, const void* succ_book,
+                                           const int32_t* depths, int B, int steps, int K, int R, int V, int dtype,
+                                           float* S, int32_t* path, void* stream);
+DFLASH2_API int dflash2_select_path_depths(const float* S, const int32_t* cand, const int32_t* depths, int B, int steps,
+                                           int K, int32_t* path, void* stream);
+
 /* Self-test of the bounded-wait machinery: launches one block that waits on an mbarrier that
  * nothing completes, with a limit of `limit_us` microseconds (1..1000000). The wait gives up,
  * records DFLASH2_ERR_TIMEOUT in the device error word and the kernel returns; read it with

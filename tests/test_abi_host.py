@@ -139,3 +139,15 @@ def test_head_topk_vocab_rejects_bad_arguments(lib):
     assert f(FAKE, 15, 5120, FAKE, 1000, None, None, FAKE, 64, 16, 0, FAKE, FAKE, FAKE, None, FAKE, 0, None) == -1
     assert f(FAKE, 15, 5120, FAKE, 8, FAKE, None, FAKE, 64, 16, 0, FAKE, FAKE, FAKE, None, FAKE, 0, None) == -1
     assert f(FAKE, 15, 5120, FAKE, 1000, FAKE, None, FAKE, 64, 16, 0, FAKE, FAKE, FAKE, None, FAKE, 0, None) == -4
+
+
+def test_mixed_depth_walk_rejects_bad_arguments(lib):
+    f = lib.dflash2_score_edges_depths
+    #        cand  un    z     anch  pred  succ  depths B  st  K   R   V     dt S     path  stream
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 15, 16, 64, 1000, 0, None, FAKE, None) == -1  # no depths
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 15, 16, 64, 1000, 0, FAKE, None, None) == -1  # no path
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 16, 64, 1000, 0, None, FAKE, None) == -1  # steps > 63
+    assert b"depths" in lib.dflash2_last_error_message() or b"steps" in lib.dflash2_last_error_message()
+    g = lib.dflash2_select_path_depths
+    assert g(FAKE, FAKE, None, 1, 15, 16, FAKE, None) == -1
+    assert g(FAKE, FAKE, FAKE, 1, 15, 33, FAKE, None) == -1
