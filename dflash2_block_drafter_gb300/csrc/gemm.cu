@@ -70,6 +70,7 @@ struct GemmArgs {
   int M, K;
   int n_main, n_extra;
   int main_chunks, n_chunks;
+  int main_units, n_units;  // pair head: 128-column units of the vocabulary / of all columns
   int m_groups, n_splits, k_splits, k_blocks;
   float* part;            // STORE: [k_splits][M][n_main]
   const float* bias;      // TOPK: [n_main] or null
@@ -125,6 +126,93 @@ __device__ __forceinline__ void list_insert(float (&tv)[kTopL], int (&ti)[kTopL]
   if (x > tv[0]) {
     tv[0] = x;
     ti[0] = id;
+  }
+}
+// The hidden_projection columns r0..r0+31 of one row, written to z.
+__device__ __forceinline__ void store_z32(const uint32_t (&r)[32], int r0, const GemmArgs& a, bool valid, int row) {
+  if (valid && a.z != nullptr) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (r0 + j < a.n_extra) a.z[static_cast<size_t>(row) * a.n_extra + r0 + j] = __uint_as_float(r[j]);
+  }
+}
+
+// Logits of the vocabulary columns col0..col0+31 of one row (accumulator + bias; columns past the
+// vocabulary are -inf) into the row's running top-16 (tv, ti); optionally the full logits.
+// `sb` holds the bias of these 32 columns in shared memory when col0 + 32 <= n_main.
+// Candidates are the values above the row's current 16th: each lane walks its own candidate bits
+// while any lane of the warp has one left, re-checking against the threshold as the list fills.
+__device__ __forceinline__ void topk_cols32(const uint32_t (&r)[32], int col0, const float* sb, const GemmArgs& a,
+                                            bool valid, int row, float (&tv)[kTopL], int (&ti)[kTopL]) {
+  float v[32];
+  if (col0 + 32 <= a.n_main) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    if (a.bias != nullptr) {
+      const float4* bp = reinterpret_cast<const float4*>(sb);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 b4 = bp[q];
+        v[4 * q] += b4.x;
+        v[4 * q + 1] += b4.y;
+        v[4 * q + 2] += b4.z;
+        v[4 * q + 3] += b4.w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int id = col0 + j;
+      float x = __uint_as_float(r[j]);
+      if (id < a.n_main) {
+        if (a.bias != nullptr) x += __ldg(a.bias + id);
+      } else {
+        x = -INFINITY;
+      }
+      v[j] = x;
+    }
+  }
+  if (a.logits != nullptr && valid) {
+    float* dst = a.logits + static_cast<size_t>(row) * a.n_main;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (col0 + j < a.n_main) dst[col0 + j] = v[j];
+  }
+  float mx = fmaxf(v[0], v[1]);
+#pragma unroll
+  for (int j = 2; j < 32; ++j) mx = fmaxf(mx, v[j]);
+  const bool any_cand = valid && mx > tv[kTopL - 1];
+  if (!__any_sync(0xffffffffu, any_cand)) return;  // the common case once lists fill
+  uint32_t cmask = 0u;
+  if (any_cand) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cmask |= (v[j] > tv[kTopL - 1] ? 1u : 0u) << j;
+  }
+  while (__any_sync(0xffffffffu, cmask != 0u)) {
+    if (cmask != 0u) {
+      const int jj = __ffs(cmask) - 1;
+      cmask &= cmask - 1u;
+      const float x = select32(v, jj);
+      if (x > tv[kTopL - 1]) list_insert(tv, ti, x, col0 + jj);
+    }
+  }
+}
+
+// Stages the bias of the 256 columns from col0 in shared memory (one warp; zero past n_main).
+__device__ __forceinline__ void stage_bias256(float* sb, const float* bias, int col0, int n_main, int lane) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i4 = lane + 32 * h;  // float4 index within the tile
+    const int col = col0 + 4 * i4;
+    float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (col + 4 <= n_main) {
+      b4 = __ldg(reinterpret_cast<const float4*>(bias + col));
+    } else {
+      if (col < n_main) b4.x = __ldg(bias + col);
+      if (col + 1 < n_main) b4.y = __ldg(bias + col + 1);
+      if (col + 2 < n_main) b4.z = __ldg(bias + col + 2);
+    }
+    reinterpret_cast<float4*>(sb)[i4] = b4;
   }
 }
 
@@ -327,20 +415,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       // load latency hides behind the mainloop (each 32-column chunk would otherwise miss L1).
       if (MODE == 1 && a.bias != nullptr && t0 < a.main_chunks) {
         __syncwarp();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int i4 = lane + 32 * h;  // float4 index within the tile
-          const int col = t0 * kChunk + 4 * i4;
-          float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (col + 4 <= a.n_main) {
-            b4 = __ldg(reinterpret_cast<const float4*>(a.bias + col));
-          } else {
-            if (col < a.n_main) b4.x = __ldg(a.bias + col);
-            if (col + 1 < a.n_main) b4.y = __ldg(a.bias + col + 1);
-            if (col + 2 < a.n_main) b4.z = __ldg(a.bias + col + 2);
-          }
-          reinterpret_cast<float4*>(sbias)[i4] = b4;
-        }
+        stage_bias256(sbias, a.bias, t0 * kChunk, a.n_main, lane);
         __syncwarp();
       }
       if (!mbar_wait_bounded(smem_u32(&acc_full[ab]), acc_par, abort_flag, kWaitLimitNs)) {
@@ -389,68 +464,9 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
               }
             }
           } else if (extra) {
-            const int r0 = col0 - a.main_chunks * kChunk;
-            if (valid && a.z != nullptr) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (r0 + j < a.n_extra) a.z[static_cast<size_t>(row) * a.n_extra + r0 + j] = __uint_as_float(r[j]);
-            }
+            store_z32(r, col0 - a.main_chunks * kChunk, a, valid, row);
           } else {
-            float v[32];
-            if (col0 + 32 <= a.n_main) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-              if (a.bias != nullptr) {
-                const float4* bp = reinterpret_cast<const float4*>(sbias + cc * 32);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  const float4 b4 = bp[q];
-                  v[4 * q] += b4.x;
-                  v[4 * q + 1] += b4.y;
-                  v[4 * q + 2] += b4.z;
-                  v[4 * q + 3] += b4.w;
-                }
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int id = col0 + j;
-                float x = __uint_as_float(r[j]);
-                if (id < a.n_main) {
-                  if (a.bias != nullptr) x += __ldg(a.bias + id);
-                } else {
-                  x = -INFINITY;
-                }
-                v[j] = x;
-              }
-            }
-            if (a.logits != nullptr && valid) {
-              float* dst = a.logits + static_cast<size_t>(row) * a.n_main;
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (col0 + j < a.n_main) dst[col0 + j] = v[j];
-            }
-            // Candidates of this chunk: values above the row's current 16th. Each lane walks its
-            // own candidate bits; the warp loops while any lane has one left. A candidate is
-            // re-checked against the threshold, which rises as the list fills.
-            float mx = fmaxf(v[0], v[1]);
-#pragma unroll
-            for (int j = 2; j < 32; ++j) mx = fmaxf(mx, v[j]);
-            const bool any_cand = valid && mx > tv[kTopL - 1];
-            if (!__any_sync(0xffffffffu, any_cand)) continue;  // the common case once lists fill
-            uint32_t cmask = 0u;
-            if (any_cand) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) cmask |= (v[j] > tv[kTopL - 1] ? 1u : 0u) << j;
-            }
-            while (__any_sync(0xffffffffu, cmask != 0u)) {
-              if (cmask != 0u) {
-                const int jj = __ffs(cmask) - 1;
-                cmask &= cmask - 1u;
-                const float x = select32(v, jj);
-                if (x > tv[kTopL - 1]) list_insert(tv, ti, x, col0 + jj);
-              }
-            }
+            topk_cols32(r, col0, sbias + cc * 32, a, valid, row, tv, ti);
           }
         }
       }
@@ -473,6 +489,298 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------ head on CTA pairs
+// The head (TOPK epilogue) on pairs of CTAs: a two-CTA cluster computes 256 rows x up to 256
+// columns per tile with one pair MMA (cta_group::2, M = 256). Each CTA stages its own 128
+// activation rows and half of the tile's weight rows, so a 32 KB stage per SM feeds the work a
+// 64 KB stage fed a two-M-tile CTA, and each CTA's accumulator (its 128 rows x 256 columns) fits in
+// TMEM twice: the epilogue of one tile overlaps the MMAs of the next.
+//
+// Columns go in 128-column units (two 64-row TMA chunks of one operand); a tile is one or two
+// units of the same operand. Of a tile of n units the leader loads the first n chunks and the
+// peer the next n (the pair MMA takes B's first half from the leader, the second from the peer).
+//
+// Barriers: full[s] is the leader's (armed by the leader with both CTAs' bytes; the peer's copies
+// complete on it across the cluster); empty[s] and acc_full[b] exist in both CTAs (the leader's
+// commits arrive on both); acc_empty[b] is the leader's (4 epilogue warps from each CTA).
+struct PairCfg {
+  static constexpr int kStageBytes = kATile + 2 * kBChunkBytes;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kBiasBytes = kEpiWarps * 256 * 4;
+  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes - kBiasBytes) / kStageBytes;
+  static constexpr int kStages = kFit > 8 ? 8 : kFit;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kBiasBytes;
+};
+static_assert(PairCfg::kStages >= 2 && PairCfg::kSmem <= kSmemLimit, "shared memory budget (pair)");
+static_assert((2 * PairCfg::kStages + 2 * PairCfg::kAccBufs + 1) * 8 + 8 <= PairCfg::kBarBytes, "barrier area");
+
+// Next tile of the unit range [u, u_end): up to 2 units, never straddling the operand boundary.
+__device__ __forceinline__ bool next_unit_tile(int& u, int u_end, int main_units, int& u0, int& nu) {
+  if (u >= u_end) return false;
+  u0 = u;
+  int e = min(u + 2, u_end);
+  if (u0 < main_units && e > main_units) e = main_units;
+  nu = e - u0;
+  u = e;
+  return true;
+}
+
+__device__ __forceinline__ void raise_abort_pair(volatile int* abort_flag, uint32_t peer_flag, int* err) {
+  *abort_flag = 1;
+  st_shared_cluster_u32(peer_flag, 1u);
+  if (err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_TIMEOUT));
+}
+
+template <bool TF32>
+__global__ void __launch_bounds__(PairCfg::kThreads, 1)
+    tc_head_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmE, const GemmArgs a) {
+  using C = PairCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* bar_area = smem + C::kStages * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(bar_area);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* acc_full = empty + C::kStages;
+  uint64_t* acc_empty = acc_full + C::kAccBufs;
+  uint64_t* drain = acc_empty + C::kAccBufs;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* sbias_all = reinterpret_cast<float*>(bar_area + C::kBarBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: leader (issues the MMAs), 1: peer
+  const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int mg = pair % a.m_groups;
+  const int ns = pair / a.m_groups;
+  const int u_begin = static_cast<int>((static_cast<long long>(a.n_units) * ns) / a.n_splits);
+  const int u_end = static_cast<int>((static_cast<long long>(a.n_units) * (ns + 1)) / a.n_splits);
+  const int rowA = mg * 256 + static_cast<int>(rank) * 128;  // this CTA's 128 activation rows
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < C::kAccBufs; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 2 * C::kEpiWarps);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (a.n_extra > 0) prefetch_tmap(&tmE);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers are initialised before anything arrives on them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol_keep = policy_evict_last();    // activations: re-read by every column tile
+      const uint64_t pol_stream = policy_evict_first(); // weights: streamed
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      int u = u_begin, u0 = 0, nu = 0;
+      while (ok && next_unit_tile(u, u_end, a.main_units, u0, nu)) {
+        const bool extra = u0 >= a.main_units;
+        const CUtensorMap* mw = extra ? &tmE : &tmB;
+        const uint64_t pol_w = extra ? pol_keep : pol_stream;
+        const int wrow0 = (extra ? u0 - a.main_units : u0) * 128 + static_cast<int>(rank) * nu * kChunk;
+        const uint32_t cta_bytes = static_cast<uint32_t>(kATile + nu * kBChunkBytes);
+        for (int kb = 0; kb < a.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb_own = smem_u32(&full[stage]);
+          const uint32_t fb = mapa_shared(fb_own, 0);  // the leader's full barrier
+          if (rank == 0) mbar_arrive_expect_tx(fb_own, 2 * cta_bytes);
+          uint8_t* sa = smem + stage * C::kStageBytes;
+          uint8_t* sb = sa + kATile;
+          const int kx = kb * (kRowBytes / (TF32 ? 4 : 2));
+          tma_load_2d_pair(smem_u32(sa), &tmA, fb, kx, rowA, pol_keep);
+          for (int j = 0; j < nu; ++j)
+            tma_load_2d_pair(smem_u32(sb + j * kBChunkBytes), mw, fb, kx, wrow0 + j * kChunk, pol_w);
+          ++issued;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every stage released: all of the leader's commits towards this CTA have landed.
+      for (int i = 0; ok && i < C::kStages; ++i) {
+        if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) ok = false;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        raise_abort_pair(abort_flag, peer_abort, a.err);
+        if (rank == 0) {
+          // Wait for the fills still in flight (they count both CTAs' bytes).
+          int s = stage;
+          uint32_t ph = phase;
+          const int n = min(issued, C::kStages);
+          for (int i = 0; i < n; ++i) {
+            if (s == 0) {
+              s = C::kStages - 1;
+              ph ^= 1u;
+            } else {
+              --s;
+            }
+            mbar_wait_bounded(smem_u32(&full[s]), ph, nullptr, kDrainLimitNs);
+          }
+        } else {
+          // The peer's copies complete on the leader's barriers: give them a fixed bounded time.
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 2000000ull) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ pair MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int tile_i = 0;
+      bool ok = true, any = false;
+      int u = u_begin, u0 = 0, nu = 0;
+      while (ok && next_unit_tile(u, u_end, a.main_units, u0, nu)) {
+        const int ab = tile_i & 1;
+        const uint32_t acc_par = static_cast<uint32_t>(tile_i >> 1) & 1u;
+        const uint32_t acc_col = static_cast<uint32_t>(ab * 256);
+        if (!mbar_wait_bounded(smem_u32(&acc_empty[ab]), acc_par ^ 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t idesc = make_idesc(TF32, 256, nu * 128);
+        for (int kb = 0; kb < a.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
+          const uint64_t adesc = desc_kmajor_swizzled<kRowBytes>(sa);
+          const uint64_t bdesc = desc_kmajor_swizzled<kRowBytes>(sa + kATile);
+#pragma unroll
+          for (int k = 0; k < kKSteps; ++k) {  // 32-byte K steps along the swizzled row
+            const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+            if (TF32)
+              mma_tf32_pair(tmem_base + acc_col, adesc + static_cast<uint64_t>(2 * k),
+                            bdesc + static_cast<uint64_t>(2 * k), idesc, acc);
+            else
+              mma_f16_pair(tmem_base + acc_col, adesc + static_cast<uint64_t>(2 * k),
+                           bdesc + static_cast<uint64_t>(2 * k), idesc, acc);
+          }
+          mma_commit_pair(smem_u32(&empty[stage]), 0x3);  // frees the stage in both CTAs
+          any = true;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(smem_u32(&acc_full[ab]), 0x3);  // accumulator complete in both CTAs
+        ++tile_i;
+      }
+      if (!ok) {
+        raise_abort_pair(abort_flag, peer_abort, a.err);
+        if (any) {
+          mma_commit_pair(smem_u32(drain), 0x1);
+          mbar_wait_bounded(smem_u32(drain), 0, nullptr, kDrainLimitNs);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int e = warp - 2;
+    const int q = warp & 3;
+    const int row = rowA + q * 32 + lane;
+    const bool valid = row < a.M;
+    float tv[kTopL];
+    int ti[kTopL];
+#pragma unroll
+    for (int i = 0; i < kTopL; ++i) {
+      tv[i] = -INFINITY;
+      ti[i] = -1;
+    }
+    float* sbias = sbias_all + e * 256;
+    int tile_i = 0;
+    int u = u_begin, u0 = 0, nu = 0;
+    while (next_unit_tile(u, u_end, a.main_units, u0, nu)) {
+      const int ab = tile_i & 1;
+      const uint32_t acc_par = static_cast<uint32_t>(tile_i >> 1) & 1u;
+      const uint32_t acc_col = static_cast<uint32_t>(ab * 256);
+      const bool extra = u0 >= a.main_units;
+      if (a.bias != nullptr && !extra) {
+        __syncwarp();
+        stage_bias256(sbias, a.bias, u0 * 128, a.n_main, lane);
+        __syncwarp();
+      }
+      if (!mbar_wait_bounded(smem_u32(&acc_full[ab]), acc_par, abort_flag, kWaitLimitNs)) {
+        if (lane == 0) raise_abort_pair(abort_flag, peer_abort, a.err);
+        break;
+      }
+      tc_fence_after();
+      for (int cc = 0; cc < nu * 4; ++cc) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_col + static_cast<uint32_t>(cc * 32),
+                           r);
+        tmem_ld_wait();
+        if (extra)
+          store_z32(r, (u0 - a.main_units) * 128 + cc * 32, a, valid, row);
+        else
+          topk_cols32(r, u0 * 128 + cc * 32, sbias + cc * 32, a, valid, row, tv, ti);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[ab]), 0));
+      ++tile_i;
+    }
+    if (valid && *abort_flag == 0) {
+      const size_t o = (static_cast<size_t>(ns) * a.M + row) * kTopL;
+      for (int i = 0; i < kTopL; ++i) {
+        a.list_val[o + i] = tv[i];
+        a.list_idx[o + i] = ti[i];
+      }
+    }
+  }
+
+  // Nothing is in flight towards either CTA past this point (stages released, accumulators read,
+  // remote arrivals made before the barrier), so the pair can free TMEM and exit.
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, C::kTmemCols);
   }
 }
 
@@ -611,6 +919,62 @@ int launch_tc(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& m
   return DFLASH2_OK;
 }
 
+template <bool TF32>
+int launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mE, const GemmArgs& args, int pairs,
+                cudaStream_t st) {
+  static unsigned done = 0;
+  auto kern = tc_head_pair_kernel<TF32>;
+  if (!ensure_smem_attr(kern, PairCfg::kSmem, &done))
+    return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(cudaGetLastError()));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.blockDim = dim3(PairCfg::kThreads);
+  cfg.dynamicSmemBytes = PairCfg::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mE, args);
+  if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "pair head launch failed: %s", cudaGetErrorString(e));
+  return DFLASH2_OK;
+}
+
+// Two-CTA clusters of the pair head that can be resident at once on the current device (0 if
+// the query fails: the head then runs on single CTAs).
+int pair_capacity() {
+  constexpr int kMaxDev = 64;
+  static int cached[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] != 0) return cached[dev] > 0 ? cached[dev] : 0;
+  static unsigned done = 0;
+  auto kern = tc_head_pair_kernel<false>;
+  int n = 0;
+  if (ensure_smem_attr(kern, PairCfg::kSmem, &done)) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(PairCfg::kThreads);
+    cfg.dynamicSmemBytes = PairCfg::kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();
+  cached[dev] = n > 0 ? n : -1;
+  return n > 0 ? n : 0;
+}
+
 template <int MODE>
 int dispatch_tc(int mt, bool tf32, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mE,
                 const GemmArgs& args, int grid, cudaStream_t st) {
@@ -639,6 +1003,8 @@ int prepare_args(const GemmProblem& p, const GemmPlan& plan, CUtensorMap* mA, CU
   a.n_extra = (p.E != nullptr) ? p.n_extra : 0;
   a.main_chunks = (p.n_main + kChunk - 1) / kChunk;
   a.n_chunks = plan.n_chunks;
+  a.main_units = (p.n_main + 127) / 128;
+  a.n_units = plan.n_chunks;
   a.m_groups = plan.m_groups;
   a.n_splits = plan.n_splits;
   a.k_splits = plan.k_splits;
@@ -655,9 +1021,24 @@ int prepare_args(const GemmProblem& p, const GemmPlan& plan, CUtensorMap* mA, CU
 #define DFL_HEAD_MAX_MT 2
 #endif
 
+// 1: heads of more than 128 rows run on CTA pairs (cta_group::2) when the device can host them.
+#ifndef DFL_HEAD_PAIR
+#define DFL_HEAD_PAIR 1
+#endif
+
 GemmPlan head_plan(int M, int K, int n_main, int n_extra, int sms) {
   (void)K;
   GemmPlan p{};
+  const int pairs = (DFL_HEAD_PAIR && M > 128) ? std::min(pair_capacity(), sms / 2) : 0;
+  if (pairs > 0) {
+    p.pair = 1;
+    p.mt = 2;
+    p.m_groups = (M + 255) / 256;
+    p.n_chunks = (n_main + 127) / 128 + (n_extra + 127) / 128;  // 128-column units
+    p.n_splits = std::max(1, std::min(p.n_chunks, pairs / p.m_groups));
+    p.k_splits = 1;
+    return p;
+  }
   p.mt = (M > 128 && DFL_HEAD_MAX_MT >= 2) ? 2 : 1;
   p.m_groups = (M + 128 * p.mt - 1) / (128 * p.mt);
   p.n_chunks = (n_main + kChunk - 1) / kChunk + (n_extra + kChunk - 1) / kChunk;
@@ -696,7 +1077,10 @@ int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bi
   a.z = z;
   a.logits = logits;
   const int grid = plan.m_groups * plan.n_splits;
-  rc = dispatch_tc<1>(plan.mt, p.dtype == DFLASH2_F32, mA, mB, mE, a, grid, st);
+  if (plan.pair)
+    rc = p.dtype == DFLASH2_F32 ? launch_pair<true>(mA, mB, mE, a, grid, st) : launch_pair<false>(mA, mB, mE, a, grid, st);
+  else
+    rc = dispatch_tc<1>(plan.mt, p.dtype == DFLASH2_F32, mA, mB, mE, a, grid, st);
   if (rc != DFLASH2_OK) return rc;
   const int rows_per_block = 8;
   topk_merge_kernel<<<(p.M + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0, st>>>(

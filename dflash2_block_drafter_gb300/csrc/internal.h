@@ -60,11 +60,12 @@ struct GemmProblem {
   int M, K, n_main, n_extra, dtype;
 };
 struct GemmPlan {
-  int mt;        // 128-row M tiles per CTA (1 or 2)
+  int mt;        // 128-row M tiles per CTA (1 or 2); per CTA pair when `pair`
   int m_groups;  // ceil(M / (128 * mt))
-  int n_splits;  // column ranges (balanced over 64-column chunks)
+  int n_splits;  // column ranges (balanced over 64-column chunks, or 128-column units when `pair`)
   int k_splits;  // reduction ranges (STORE mode only)
-  int n_chunks;  // 64-column chunks over the virtual range
+  int n_chunks;  // 64-column chunks (128-column units when `pair`) over the virtual range
+  int pair;      // head on two-CTA clusters (cta_group::2): grid = 2 * m_groups * n_splits CTAs
 };
 // Split-K plan of the kernel_projection GEMM; shared by the workspace query and the launch.
 GemmPlan kp_plan(const ConvShape& s, int sms);

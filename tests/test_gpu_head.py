@@ -41,6 +41,25 @@ def _run(wl, want_logits=False, K=None):
 ])
 def test_head_topk_parity(torch, dtype, B, G, H, V, R, bias):
     wl = I.selector_case(11 + B + V, B=B, G=G, H=H, V=V, K=16, R=R, dtype=dtype, bias=bias)
+    _check_head(wl, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("M,V,R", [
+    (129, 3001, 128),   # one row past a 128-row tile; vocabulary ends inside a 128-column unit
+    (257, 1000, 192),   # one row past a 256-row group; fewer column units than CTA pairs; 1.5 units of z
+    (513, 9000, 16),    # ragged third group; z narrower than a chunk
+    (1024, 2500, 64),   # four full groups; units not a multiple of the column ranges
+])
+def test_head_topk_row_and_column_edges(torch, dtype, M, V, R):
+    """Row counts just past the 128- and 256-row boundaries of the head's tiles (some CTAs hold a
+    single valid row or none), ragged vocabularies and hidden_projection widths."""
+    wl = I.selector_case(40 + M, B=M, G=2, H=256, V=V, K=16, R=R, dtype=dtype, bias=True)
+    _check_head(wl, dtype)
+
+
+def _check_head(wl, dtype):
+    H = wl.H
     cand, unary, z, logits = _run(wl, want_logits=True)
     h = I.to_f64(wl.h).reshape(-1, H)
     W = I.to_f64(wl.w_head)
