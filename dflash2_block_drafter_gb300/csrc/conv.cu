@@ -203,6 +203,11 @@ __global__ void __launch_bounds__(kApplyMaxThreads)
 //   output:  each CTA's fp32 tile leaves at ~16 GB/s per SM (measured), and with K splits the
 //            partials are read back by the side-0 pass (~5 TB/s)
 // cost = max(issue, ingest, stream) + output.
+// CTA-pair plans (above 128 rows): 256-row pair tiles, each SM ingesting its 128 rows and half of
+// the tile's weight rows, partials leaving by TMA store (~50 GB/s per SM assumed).
+#ifndef DFL_KP_PAIR
+#define DFL_KP_PAIR 1
+#endif
 GemmPlan kp_plan(const ConvShape& s, int sms) {
   const int M = s.rows();
   const int N = 4 * s.groups;
@@ -235,6 +240,32 @@ GemmPlan kp_plan(const ConvShape& s, int sms) {
         best_cost = cost;
         best = p;
       }
+    }
+  }
+  const int pairs = (DFL_KP_PAIR && M > 128 && N % 4 == 0) ? std::min(gemm_pair_capacity(), sms / 2) : 0;
+  for (int tile_units = 2; pairs > 0 && tile_units >= 1; --tile_units) {
+    GemmPlan p{};
+    p.pair = 1;
+    p.mt = 2;
+    p.m_groups = (M + 255) / 256;
+    p.n_chunks = (N + 127) / 128;  // 128-column units
+    p.n_splits = (p.n_chunks + tile_units - 1) / tile_units;
+    const int tiles = p.m_groups * p.n_splits;
+    p.k_splits = std::max(1, std::min(std::min(k_blocks, 32), pairs / std::max(1, tiles)));
+    const int used = tiles * p.k_splits;
+    const int waves = (used + pairs - 1) / pairs;
+    const int units_per_pair = (p.n_chunks + p.n_splits - 1) / p.n_splits;
+    const int tiles_per_pair = (units_per_pair + 1) / 2;
+    const double kb_per_cta = static_cast<double>(k_blocks) / p.k_splits * tiles_per_pair;
+    const double t_issue = waves * kb_per_cta * 4.0 * 145.0 / 1.9e9;
+    const double t_ingest = waves * kb_per_cta * (16384.0 + std::min(units_per_pair, 2) * 8192.0) / 100e9;
+    const double t_stream = w_bytes / (std::min(2 * used, sms) * 40e9);
+    const double t_out = waves * 128.0 * 128.0 * units_per_pair * 4.0 / 50e9 +
+                         (p.k_splits > 1 ? p.k_splits * static_cast<double>(M) * N * 8.0 / 5e12 : 0.0);
+    const double cost = std::max(std::max(t_issue, t_ingest), t_stream) + t_out;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = p;
     }
   }
   return best;

@@ -492,12 +492,14 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   }
 }
 
-// ------------------------------------------------------------------------------ head on CTA pairs
-// The head (TOPK epilogue) on pairs of CTAs: a two-CTA cluster computes 256 rows x up to 256
-// columns per tile with one pair MMA (cta_group::2, M = 256). Each CTA stages its own 128
-// activation rows and half of the tile's weight rows, so a 32 KB stage per SM feeds the work a
-// 64 KB stage fed a two-M-tile CTA, and each CTA's accumulator (its 128 rows x 256 columns) fits in
-// TMEM twice: the epilogue of one tile overlaps the MMAs of the next.
+// ------------------------------------------------------------------------------ CTA-pair GEMM
+// The GEMM on pairs of CTAs: a two-CTA cluster computes 256 rows x up to 256 columns per tile
+// with one pair MMA (cta_group::2, M = 256). Each CTA stages its own 128 activation rows and half
+// of the tile's weight rows, so a 32 KB stage per SM feeds the work a 64 KB stage fed a
+// two-M-tile CTA, and each CTA's accumulator (its 128 rows x 256 columns) fits in TMEM twice: the
+// epilogue of one tile overlaps the MMAs of the next. Epilogues as in tc_gemm_kernel: TOPK (the
+// head) and STORE (split-K fp32 partials of kernel_projection, written by TMA from swizzled
+// shared-memory tiles).
 //
 // Columns go in 128-column units (two 64-row TMA chunks of one operand); a tile is one or two
 // units of the same operand. Of a tile of n units the leader loads the first n chunks and the
@@ -506,6 +508,18 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
 // Barriers: full[s] is the leader's (armed by the leader with both CTAs' bytes; the peer's copies
 // complete on it across the cluster); empty[s] and acc_full[b] exist in both CTAs (the leader's
 // commits arrive on both); acc_empty[b] is the leader's (4 epilogue warps from each CTA).
+
+// L2 policy of the weight stream (0: evict_first, 1: evict_normal, 2: evict_last) and where the
+// head epilogue reads the bias from (1: a per-warp copy in shared memory, 0: global memory
+// through L1, which leaves room for a seventh stage).
+#ifndef DFL_PAIR_WPOL
+#define DFL_PAIR_WPOL 1
+#endif
+#ifndef DFL_PAIR_SMEM_BIAS
+#define DFL_PAIR_SMEM_BIAS 1
+#endif
+
+template <int MODE>
 struct PairCfg {
   static constexpr int kStageBytes = kATile + 2 * kBChunkBytes;
   static constexpr int kEpiWarps = 4;
@@ -513,13 +527,19 @@ struct PairCfg {
   static constexpr int kAccBufs = 2;
   static constexpr int kTmemCols = 512;
   static constexpr int kBarBytes = 256;
-  static constexpr int kBiasBytes = kEpiWarps * 256 * 4;
-  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes - kBiasBytes) / kStageBytes;
+  static constexpr int kBiasBytes = (MODE == 1 && DFL_PAIR_SMEM_BIAS) ? kEpiWarps * 256 * 4 : 0;
+  // STORE: two 32x32 fp32 staging tiles (128-byte swizzled rows) per epilogue warp
+  static constexpr int kOutTile = 32 * 32 * 4;
+  static constexpr int kOutBytes = MODE == 0 ? kEpiWarps * 2 * kOutTile : 0;
+  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes - kBiasBytes - kOutBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kBiasBytes;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kBiasBytes + kOutBytes;
 };
-static_assert(PairCfg::kStages >= 2 && PairCfg::kSmem <= kSmemLimit, "shared memory budget (pair)");
-static_assert((2 * PairCfg::kStages + 2 * PairCfg::kAccBufs + 1) * 8 + 8 <= PairCfg::kBarBytes, "barrier area");
+static_assert(PairCfg<1>::kStages >= 2 && PairCfg<1>::kSmem <= kSmemLimit, "shared memory budget (pair, head)");
+static_assert(PairCfg<0>::kStageBytes % 1024 == 0 && PairCfg<0>::kOutTile % 1024 == 0, "staging tile alignment");
+static_assert(PairCfg<0>::kStages >= 2 && PairCfg<0>::kSmem <= kSmemLimit, "shared memory budget (pair, store)");
+static_assert((2 * PairCfg<1>::kStages + 2 * PairCfg<1>::kAccBufs + 1) * 8 + 8 <= PairCfg<1>::kBarBytes, "barriers");
+static_assert((2 * PairCfg<0>::kStages + 2 * PairCfg<0>::kAccBufs + 1) * 8 + 8 <= PairCfg<0>::kBarBytes, "barriers");
 
 // Next tile of the unit range [u, u_end): up to 2 units, never straddling the operand boundary.
 __device__ __forceinline__ bool next_unit_tile(int& u, int u_end, int main_units, int& u0, int& nu) {
@@ -538,15 +558,17 @@ __device__ __forceinline__ void raise_abort_pair(volatile int* abort_flag, uint3
   if (err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_TIMEOUT));
 }
 
-template <bool TF32>
-__global__ void __launch_bounds__(PairCfg::kThreads, 1)
-    tc_head_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmE, const GemmArgs a) {
-  using C = PairCfg;
+template <bool TF32, int MODE>
+__global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
+    tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmD, const GemmArgs a) {
+  using C = PairCfg<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* bar_area = smem + C::kStages * C::kStageBytes;
+  // layout: stages | STORE staging tiles (1024-aligned, as the 128-byte swizzle needs) | barriers | bias
+  uint8_t* sout_all = smem + C::kStages * C::kStageBytes;
+  uint8_t* bar_area = sout_all + C::kOutBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(bar_area);
   uint64_t* empty = full + C::kStages;
   uint64_t* acc_full = empty + C::kStages;
@@ -560,11 +582,15 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: leader (issues the MMAs), 1: peer
   const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
-  const int pair = static_cast<int>(blockIdx.x >> 1);
+  int pair = static_cast<int>(blockIdx.x >> 1);
   const int mg = pair % a.m_groups;
-  const int ns = pair / a.m_groups;
+  pair /= a.m_groups;
+  const int ns = pair % a.n_splits;
+  const int ks = pair / a.n_splits;
   const int u_begin = static_cast<int>((static_cast<long long>(a.n_units) * ns) / a.n_splits);
   const int u_end = static_cast<int>((static_cast<long long>(a.n_units) * (ns + 1)) / a.n_splits);
+  const int kb0 = static_cast<int>((static_cast<long long>(a.k_blocks) * ks) / a.k_splits);
+  const int kb1 = static_cast<int>((static_cast<long long>(a.k_blocks) * (ks + 1)) / a.k_splits);
   const int rowA = mg * 256 + static_cast<int>(rank) * 128;  // this CTA's 128 activation rows
 
   if (threadIdx.x == 0) {
@@ -582,6 +608,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (a.n_extra > 0) prefetch_tmap(&tmE);
+    if (MODE == 0) prefetch_tmap(&tmD);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
@@ -595,8 +622,10 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      const uint64_t pol_keep = policy_evict_last();    // activations: re-read by every column tile
-      const uint64_t pol_stream = policy_evict_first(); // weights: streamed
+      const uint64_t pol_keep = policy_evict_last();  // activations: re-read by every column tile
+      // weights: streamed, but read by the pairs of every row group
+      const uint64_t pol_stream = DFL_PAIR_WPOL == 0 ? policy_evict_first()
+                                  : DFL_PAIR_WPOL == 1 ? policy_evict_normal() : policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -608,7 +637,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         const uint64_t pol_w = extra ? pol_keep : pol_stream;
         const int wrow0 = (extra ? u0 - a.main_units : u0) * 128 + static_cast<int>(rank) * nu * kChunk;
         const uint32_t cta_bytes = static_cast<uint32_t>(kATile + nu * kBChunkBytes);
-        for (int kb = 0; kb < a.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
@@ -680,7 +709,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         }
         tc_fence_after();
         const uint32_t idesc = make_idesc(TF32, 256, nu * 128);
-        for (int kb = 0; kb < a.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
@@ -691,7 +720,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
           const uint64_t bdesc = desc_kmajor_swizzled<kRowBytes>(sa + kATile);
 #pragma unroll
           for (int k = 0; k < kKSteps; ++k) {  // 32-byte K steps along the swizzled row
-            const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+            const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
             if (TF32)
               mma_tf32_pair(tmem_base + acc_col, adesc + static_cast<uint64_t>(2 * k),
                             bdesc + static_cast<uint64_t>(2 * k), idesc, acc);
@@ -733,6 +762,8 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       ti[i] = -1;
     }
     float* sbias = sbias_all + e * 256;
+    uint8_t* sout = sout_all + e * 2 * C::kOutTile;  // STORE: this warp's two staging tiles
+    int n_out = 0;                                  // STORE: tiles handed to TMA so far
     int tile_i = 0;
     int u = u_begin, u0 = 0, nu = 0;
     while (next_unit_tile(u, u_end, a.main_units, u0, nu)) {
@@ -740,7 +771,7 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
       const uint32_t acc_par = static_cast<uint32_t>(tile_i >> 1) & 1u;
       const uint32_t acc_col = static_cast<uint32_t>(ab * 256);
       const bool extra = u0 >= a.main_units;
-      if (a.bias != nullptr && !extra) {
+      if (MODE == 1 && DFL_PAIR_SMEM_BIAS && a.bias != nullptr && !extra) {
         __syncwarp();
         stage_bias256(sbias, a.bias, u0 * 128, a.n_main, lane);
         __syncwarp();
@@ -755,17 +786,51 @@ __global__ void __launch_bounds__(PairCfg::kThreads, 1)
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_col + static_cast<uint32_t>(cc * 32),
                            r);
         tmem_ld_wait();
-        if (extra)
+        if (MODE == 0) {
+          // This warp's 32 rows x 32 columns of the partial sum: into a staging tile laid out as
+          // the tensor map's 128-byte swizzle expects (16-byte unit j of row i at unit j ^ (i % 8),
+          // so the eight lanes of a store phase hit eight different units), then one TMA store.
+          // Boxes that start past the last row or column are not stored (warp-uniform test), and
+          // every stored box is one bulk group, so "at most one group still reading" below means
+          // the store that last used this staging tile is done with it.
+          const int col0 = u0 * 128 + cc * 32;
+          const int row0 = rowA + q * 32;
+          if (row0 < a.M && col0 < a.n_main) {
+            uint8_t* tile = sout + (n_out & 1) * C::kOutTile;
+            if (n_out >= 2) {
+              if (lane == 0) bulk_wait_group_read<1>();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<float4*>(tile + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                  make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmD, smem_u32(tile), col0, row0, ks);
+              bulk_commit_group();
+            }
+            ++n_out;
+          }
+        } else if (extra) {
           store_z32(r, (u0 - a.main_units) * 128 + cc * 32, a, valid, row);
-        else
-          topk_cols32(r, u0 * 128 + cc * 32, sbias + cc * 32, a, valid, row, tv, ti);
+        } else {
+          topk_cols32(r, u0 * 128 + cc * 32, DFL_PAIR_SMEM_BIAS ? sbias + cc * 32 : a.bias + u0 * 128 + cc * 32, a,
+                      valid, row, tv, ti);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[ab]), 0));
       ++tile_i;
     }
-    if (valid && *abort_flag == 0) {
+    if (MODE == 0) {
+      if (lane == 0) bulk_wait_group_all();  // partial sums written before the CTA retires
+      __syncwarp();
+    }
+    if (MODE == 1 && valid && *abort_flag == 0) {
       const size_t o = (static_cast<size_t>(ns) * a.M + row) * kTopL;
       for (int i = 0; i < kTopL; ++i) {
         a.list_val[o + i] = tv[i];
@@ -906,6 +971,23 @@ bool make_map(CUtensorMap* m, const void* ptr, int dtype, int rows, int cols, in
   return r == CUDA_SUCCESS;
 }
 
+// Split-K partial sums [k_splits][rows][cols] fp32 as a 3D map for TMA stores of 32 x 32 boxes
+// with 128-byte swizzle (the pair GEMM's STORE epilogue). Rows past `rows` in a box are clipped
+// per split.
+bool make_part_map(CUtensorMap* m, float* part, int k_splits, int rows, int cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(k_splits)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 4, static_cast<cuuint64_t>(rows) * cols * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, part, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int MT, bool TF32, int MODE>
 int launch_tc(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mE, const GemmArgs& args, int grid,
               cudaStream_t st) {
@@ -919,32 +1001,38 @@ int launch_tc(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& m
   return DFLASH2_OK;
 }
 
-template <bool TF32>
-int launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mE, const GemmArgs& args, int pairs,
-                cudaStream_t st) {
-  static unsigned done = 0;
-  auto kern = tc_head_pair_kernel<TF32>;
-  if (!ensure_smem_attr(kern, PairCfg::kSmem, &done))
-    return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(cudaGetLastError()));
+template <bool TF32, int MODE>
+cudaLaunchConfig_t pair_config(int pairs, cudaStream_t st, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-  cfg.blockDim = dim3(PairCfg::kThreads);
-  cfg.dynamicSmemBytes = PairCfg::kSmem;
+  cfg.blockDim = dim3(PairCfg<MODE>::kThreads);
+  cfg.dynamicSmemBytes = PairCfg<MODE>::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mE, args);
-  if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "pair head launch failed: %s", cudaGetErrorString(e));
+  return cfg;
+}
+
+template <bool TF32, int MODE>
+int launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mE, const CUtensorMap& mD,
+                const GemmArgs& args, int pairs, cudaStream_t st) {
+  static unsigned done = 0;
+  auto kern = tc_pair_kernel<TF32, MODE>;
+  if (!ensure_smem_attr(kern, PairCfg<MODE>::kSmem, &done))
+    return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(cudaGetLastError()));
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pair_config<TF32, MODE>(pairs, st, attr);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mE, mD, args);
+  if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "pair GEMM launch failed: %s", cudaGetErrorString(e));
   return DFLASH2_OK;
 }
 
-// Two-CTA clusters of the pair head that can be resident at once on the current device (0 if
-// the query fails: the head then runs on single CTAs).
+// Two-CTA clusters of the pair GEMM that can be resident at once on the current device (0 if the
+// query fails: the GEMMs then run on single CTAs). Both epilogues fit one CTA per SM.
 int pair_capacity() {
   constexpr int kMaxDev = 64;
   static int cached[kMaxDev] = {};
@@ -953,22 +1041,18 @@ int pair_capacity() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (cached[dev] != 0) return cached[dev] > 0 ? cached[dev] : 0;
-  static unsigned done = 0;
-  auto kern = tc_head_pair_kernel<false>;
   int n = 0;
-  if (ensure_smem_attr(kern, PairCfg::kSmem, &done)) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(PairCfg::kThreads);
-    cfg.dynamicSmemBytes = PairCfg::kSmem;
+  static unsigned done1 = 0, done0 = 0;
+  auto k1 = tc_pair_kernel<false, 1>;
+  auto k0 = tc_pair_kernel<false, 0>;
+  if (ensure_smem_attr(k1, PairCfg<1>::kSmem, &done1) && ensure_smem_attr(k0, PairCfg<0>::kSmem, &done0)) {
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    int n1 = 0, n0 = 0;
+    cudaLaunchConfig_t cfg = pair_config<false, 1>(1, nullptr, attr);
+    if (cudaOccupancyMaxActiveClusters(&n1, k1, &cfg) != cudaSuccess) n1 = 0;
+    cfg = pair_config<false, 0>(1, nullptr, attr);
+    if (cudaOccupancyMaxActiveClusters(&n0, k0, &cfg) != cudaSuccess) n0 = 0;
+    n = std::min(n1, n0);
   }
   (void)cudaGetLastError();
   cached[dev] = n > 0 ? n : -1;
@@ -1054,6 +1138,8 @@ size_t head_workspace(int M, int V, int K, int R, int sms) {
   return lists * (sizeof(float) + sizeof(int)) + 256;
 }
 
+int gemm_pair_capacity() { return pair_capacity(); }
+
 int launch_gemm_store(const GemmProblem& p, const GemmPlan& plan, float* part, cudaStream_t st) {
   CUtensorMap mA, mB, mE;
   GemmArgs a;
@@ -1061,6 +1147,14 @@ int launch_gemm_store(const GemmProblem& p, const GemmPlan& plan, float* part, c
   if (rc != DFLASH2_OK) return rc;
   a.part = part;
   const int grid = plan.m_groups * plan.n_splits * plan.k_splits;
+  if (plan.pair) {
+    if (p.n_main % 4 != 0) return fail(DFLASH2_ERR_INVALID_ARG, "pair GEMM store needs N %% 4 == 0 (N=%d)", p.n_main);
+    CUtensorMap mD;
+    if (!make_part_map(&mD, part, plan.k_splits, p.M, p.n_main))
+      return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (partials)");
+    return p.dtype == DFLASH2_F32 ? launch_pair<true, 0>(mA, mB, mE, mD, a, grid, st)
+                                  : launch_pair<false, 0>(mA, mB, mE, mD, a, grid, st);
+  }
   return dispatch_tc<0>(plan.mt, p.dtype == DFLASH2_F32, mA, mB, mE, a, grid, st);
 }
 
@@ -1078,7 +1172,8 @@ int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bi
   a.logits = logits;
   const int grid = plan.m_groups * plan.n_splits;
   if (plan.pair)
-    rc = p.dtype == DFLASH2_F32 ? launch_pair<true>(mA, mB, mE, a, grid, st) : launch_pair<false>(mA, mB, mE, a, grid, st);
+    rc = p.dtype == DFLASH2_F32 ? launch_pair<true, 1>(mA, mB, mE, mA, a, grid, st)
+                                : launch_pair<false, 1>(mA, mB, mE, mA, a, grid, st);
   else
     rc = dispatch_tc<1>(plan.mt, p.dtype == DFLASH2_F32, mA, mB, mE, a, grid, st);
   if (rc != DFLASH2_OK) return rc;

@@ -70,6 +70,8 @@ struct GemmPlan {
 // Split-K plan of the kernel_projection GEMM; shared by the workspace query and the launch.
 GemmPlan kp_plan(const ConvShape& s, int sms);
 GemmPlan head_plan(int M, int K, int n_main, int n_extra, int sms);
+// Two-CTA clusters of the pair GEMM that fit the current device at once (0: pairs unavailable).
+int gemm_pair_capacity();
 size_t head_workspace(int M, int V, int K, int R, int sms);
 // mode 0: write fp32 partial sums part[k_split][M][n_main].
 int launch_gemm_store(const GemmProblem& p, const GemmPlan& plan, float* part, cudaStream_t st);

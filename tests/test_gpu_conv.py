@@ -25,7 +25,11 @@ def _site_dev(torch, s):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("B,G,H,gs", [(1, 8, 256, 16), (3, 16, 512, 16), (5, 7, 320, 16), (2, 16, 1024, 32)])
+@pytest.mark.parametrize("B,G,H,gs", [
+    (1, 8, 256, 16), (3, 16, 512, 16), (5, 7, 320, 16), (2, 16, 1024, 32),
+    # above 128 rows kernel_projection runs on CTA pairs: a ragged second row group (144 rows),
+    # G = 64 (320 rows), and 260 rows with 48 groups (N = 192: half a column unit past the end)
+    (9, 16, 512, 16), (5, 64, 256, 16), (20, 13, 384, 8)])
 def test_prepare_finish_parity(torch, dtype, B, G, H, gs):
     import dflash2_block_drafter_gb300 as d
     wl = I.conv_case(100 + B * G + H, B, G, H, gs, dtype=dtype)
