@@ -346,14 +346,16 @@ def our_arm(args, wl_name):
         flops = head_flops(M, wl.V, wl.R, wl.H)
         byts = head_bytes(M, wl.V, wl.R, wl.H, wl.K)
         tensor_bound = flops / (pk["bf16_tflops_sustained"] * 1e12) > byts / (pk["hbm_gbs"] * 1e9)
+        kname = ("tc_pair_kernel<bf16, TOPK>" if M > 128 else "tc_gemm_kernel<1, bf16, TOPK>") + \
+            " (head GEMM + fused top-16 + z) + topk_merge"
         if tensor_bound:
-            roofline = {"kernel": "tc_gemm_kernel (head GEMM + fused top-16 + z) + topk_merge", "bound": "tensor",
+            roofline = {"kernel": kname, "bound": "tensor",
                         "achieved": flops / head_avg_s / 1e12, "peak": pk["bf16_tflops_sustained"],
                         "unit": "TFLOP/s", "frac": flops / head_avg_s / 1e12 / pk["bf16_tflops_sustained"],
                         "traffic": None, "peak_kind": f"bf16 sustained, {pk['source']}",
                         "algorithmic_per_launch": flops, "avg_launch_ms": head_avg_s * 1e3}
         else:
-            roofline = {"kernel": "tc_gemm_kernel (head GEMM + fused top-16 + z) + topk_merge", "bound": "hbm",
+            roofline = {"kernel": kname, "bound": "hbm",
                         "achieved": byts / head_avg_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
                         "frac": byts / head_avg_s / 1e9 / pk["hbm_gbs"], "traffic": None,
                         "peak_kind": f"HBM copy, {pk['source']}", "algorithmic_per_launch": byts,
@@ -396,10 +398,10 @@ def our_arm(args, wl_name):
 # per-launch DRAM traffic (bytes) of the head kernel from an ncu capture, by workload; None until
 # measured for the current kernel
 TRAFFIC_PER_LAUNCH = {
-    # dram__bytes_read.sum + dram__bytes_write.sum of tc_gemm_kernel<2, bf16, TOPK> (960 rows),
+    # dram__bytes_read.sum + dram__bytes_write.sum of tc_pair_kernel<bf16, TOPK> (960 rows),
     # profiles/head_topk_selector-B64.md; the full tail runs the same head launch
-    "full-tail-B64": 2.559410e9 + 3.499264e6,
-    "selector-B64": 2.559410e9 + 3.499264e6,
+    "full-tail-B64": 2.623501e9 + 3.369728e6,
+    "selector-B64": 2.623501e9 + 3.369728e6,
     # tc_gemm_kernel<1, bf16, TOPK> (15 rows), profiles/head_topk_selector-B1.md
     "selector-B1": 2.543751e9 + 2.905344e6,
 }
