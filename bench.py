@@ -318,15 +318,19 @@ def our_arm(args, wl_name):
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record(stream)
-        if h_x0 is not None:
-            x0.copy_(h_x0, non_blocking=True)
-        for yd, yh in zip(ys, h_ys):
-            yd.copy_(yh, non_blocking=True)
-        if h_h is not None:
-            h_in.copy_(h_h, non_blocking=True)
-        if h_anchors is not None:
-            anchors.copy_(h_anchors, non_blocking=True)
-        step()
+        if full_tail:
+            # inputs copied on a copy stream; each site waits only for its own sublayer output
+            run.full_from_host(h_x0, h_ys, h_anchors, x0, ys, anchors)
+        else:
+            if h_x0 is not None:
+                x0.copy_(h_x0, non_blocking=True)
+            for yd, yh in zip(ys, h_ys):
+                yd.copy_(yh, non_blocking=True)
+            if h_h is not None:
+                h_in.copy_(h_h, non_blocking=True)
+            if h_anchors is not None:
+                anchors.copy_(h_anchors, non_blocking=True)
+            step()
         h_out.copy_(out_dev, non_blocking=True)
         e.record(stream)
         e.synchronize()

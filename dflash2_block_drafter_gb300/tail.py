@@ -83,8 +83,10 @@ class TailRunner:
             self.head_ws = torch.empty(max(hw, 256), dtype=torch.uint8, device=device)
 
     # ------------------------------------------------------------------ passes
-    def conv_chain(self, x0: torch.Tensor, ys: List[torch.Tensor], emit_h: bool):
-        """Every site in order, starting from x0 (left unchanged); returns the final residual stream (self.x)."""
+    def conv_chain(self, x0: torch.Tensor, ys: List[torch.Tensor], emit_h: bool, before_finish=None):
+        """Every site in order, starting from x0 (left unchanged); returns the final residual stream (self.x).
+        ``before_finish(i)``, if given, runs before site i's finish call is issued (full_from_host
+        makes the compute stream wait there for y_i's copy)."""
         wl = self.wl
         nsites = len(self.sites)
         for i, s in enumerate(self.sites):
@@ -95,6 +97,8 @@ class TailRunner:
                 dflash2_conv_prepare(self.n, None, wl.eps, s.w_kp, s.base, wl.gs, out=self.a, coef1=self.coef1,
                                      workspace=self.conv_ws)
             residual = x0 if i == 0 else self.x
+            if before_finish is not None:
+                before_finish(i)
             if i + 1 < nsites:
                 dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=residual, out=self.x,
                                     next_norm_w=self.sites[i + 1].norm_w, eps=wl.eps, next_n=self.n, next_row0=0)
@@ -132,6 +136,37 @@ class TailRunner:
         """The whole block tail; returns path [B, steps] int32 (device)."""
         self.conv_chain(x0, ys, emit_h=True)
         return self.selector(self.h, anchors, want_S=want_S)
+
+    def full_from_host(self, h_x0: torch.Tensor, h_ys: List[torch.Tensor], h_anchors: torch.Tensor,
+                       x0: torch.Tensor, ys: List[torch.Tensor], anchors: torch.Tensor, want_S: bool = True):
+        """The whole block tail with its inputs in pinned host memory. Every input is copied into
+        the given device buffers on a copy stream, one event per input; the compute stream waits
+        for x0 before the first site, for y_i only before site i's finish and for the anchors
+        before the selector, so the copies of later sites' inputs overlap the earlier sites and
+        the first ones overlap nothing but each other. Returns path [B, steps] int32 (device)."""
+        comp = torch.cuda.current_stream()
+        if getattr(self, "_copy_stream", None) is None:
+            self._copy_stream = torch.cuda.Stream(device=comp.device)
+            self._ev_x0 = torch.cuda.Event()
+            self._ev_y = [torch.cuda.Event() for _ in self.sites]
+            self._ev_anchors = torch.cuda.Event()
+        cs = self._copy_stream
+        cs.wait_stream(comp)  # whatever still reads the device input buffers was queued before this
+        with torch.cuda.stream(cs):
+            x0.copy_(h_x0, non_blocking=True)
+            self._ev_x0.record(cs)
+            for i, (dst, src) in enumerate(zip(ys, h_ys)):
+                dst.copy_(src, non_blocking=True)
+                self._ev_y[i].record(cs)
+            anchors.copy_(h_anchors, non_blocking=True)
+            self._ev_anchors.record(cs)
+        comp.wait_event(self._ev_x0)
+        self.conv_chain(x0, ys, emit_h=True, before_finish=lambda i: comp.wait_event(self._ev_y[i]))
+        comp.wait_event(self._ev_anchors)
+        path = self.selector(self.h, anchors, want_S=want_S)
+        for t in [x0, anchors] + list(ys):  # the copy stream wrote them: keep the allocator honest
+            t.record_stream(cs)
+        return path
 
     def capture(self, fn, *args, **kwargs) -> "torch.cuda.CUDAGraph":
         """Record one pass of ``fn`` (e.g. ``self.full``) into a CUDA graph over the runner's fixed

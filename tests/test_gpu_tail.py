@@ -88,3 +88,28 @@ def test_graph_replay_matches_eager(torch):
     assert torch.equal(run.path, eager[0])
     assert torch.equal(run.S, eager[1])
     assert torch.equal(run.h, eager[2])
+
+
+def test_full_from_host_matches_device_inputs(torch):
+    """The pass that copies its inputs from pinned host memory on a copy stream (each site waiting
+    only for its own sublayer output) gives exactly the results of the pass on device inputs,
+    twice in a row (the second call's copies must not overtake the first call's readers)."""
+    from dflash2_block_drafter_gb300.tail import TailRunner, to_device, to_pinned
+    import dflash2_block_drafter_gb300 as d
+    wl = I.make_config(0, B=4)
+    run = TailRunner(wl)
+    run.full(to_device(wl.x0), [to_device(s.y) for s in wl.sites], to_device(wl.anchors))
+    want = (run.path.clone(), run.S.clone(), run.h.clone())
+    x0 = torch.empty_like(run.x)
+    ys = [torch.empty_like(run.x) for _ in wl.sites]
+    anchors = torch.empty(wl.B, dtype=torch.int32, device="cuda")
+    h_x0, h_ys, h_anchors = to_pinned(wl.x0), [to_pinned(s.y) for s in wl.sites], to_pinned(wl.anchors)
+    for _ in range(2):
+        run.path.zero_()
+        run.S.zero_()
+        run.full_from_host(h_x0, h_ys, h_anchors, x0, ys, anchors)
+        torch.cuda.synchronize()
+        assert d.dflash2_poll_error() == 0
+        assert torch.equal(run.path, want[0])
+        assert torch.equal(run.S, want[1])
+        assert torch.equal(run.h, want[2])
