@@ -5,17 +5,18 @@
 // fp32 split-K partials; the coefficient broadcast (base + per-group delta) is fused into the
 // apply passes and never materialised at channel width.
 //
-// Apply passes: one thread per (row, 8 consecutive channels): it reads its row's and the previous
-// row's 16-byte vectors (the previous row is the neighbouring thread's, an L1 hit), the row's
-// group deltas and the base kernel, and writes one vector. A CTA holds every row of a block for
-// its channels, so the t-1 read never leaves the block, and the grid has B*G*H/8 threads: enough
-// independent loads in flight to run at memory speed. RMSNorm is a row-per-CTA pass.
+// Apply passes: a thread owns one 8-channel strip of a few consecutive rows of one block: it loads
+// the base kernel once, the row before its first row, and then per row the 16-byte input vector
+// and the row's group deltas (all independent loads, issued before any arithmetic), and writes one
+// vector per row, carrying the row as the next row's t-1 input. A CTA holds every row of a block
+// for its channels, so no read crosses a block boundary. RMSNorm is a pass of a few rows per CTA.
 #include <cuda_bf16.h>
 
 #include <algorithm>
 #include <cmath>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dfl {
 namespace {
@@ -56,139 +57,207 @@ __device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat
 __device__ __forceinline__ float load1(const float* p) { return *p; }
 
 
-// Vectors (of 8 channels) per apply CTA for blocks of G rows.
-__host__ __device__ inline int vectors_per_cta(int G) { return G >= kApplyMaxThreads ? 1 : kApplyMaxThreads / G; }
+// Rows per thread of the apply passes: a thread walks RPT consecutive rows of one 8-channel strip,
+// loading the base kernel once and taking each row's t-1 input from the previous iteration.
+#ifndef DFL_APPLY_RPT
+#define DFL_APPLY_RPT 2
+#endif
+constexpr int kRpt = DFL_APPLY_RPT;
 
-// RMSNorm of selected rows, one CTA per output row (dflash2.ts #rms):
+// Vectors (of 8 channels) per apply CTA for blocks of G rows, kRpt rows per thread.
+__host__ __device__ inline int row_groups(int G) { return (G + kRpt - 1) / kRpt; }
+__host__ __device__ inline int vectors_per_cta(int G) {
+  return row_groups(G) >= kApplyMaxThreads ? 1 : kApplyMaxThreads / row_groups(G);
+}
+
+// RMSNorm of selected rows, kNormRows output rows per CTA (dflash2.ts #rms):
 //   n[b, t - row0, :] = x[b, t, :] * rsqrt(mean(x[b, t, :]^2) + eps) * w   for t in [row0, G).
-// The row's H/8 vectors are held in registers between the reduction and the scaling.
+// Thread i owns channels 8i..8i+7 of each of the CTA's rows; the rows' vectors and the weight
+// vector are loaded before the reduction (all independent), and held in registers until scaled.
+#ifndef DFL_NORM_ROWS
+#define DFL_NORM_ROWS 1
+#endif
+constexpr int kNormRows = DFL_NORM_ROWS;
+
 template <typename T>
 __global__ void __launch_bounds__(kNormThreads)
     rms_rows_kernel(const T* __restrict__ x, const T* __restrict__ w, float eps, T* __restrict__ n, int G, int row0,
-                    int H) {
-  __shared__ float warp_ss[32];
-  __shared__ float row_r;
+                    int H, int total_rows) {
+  __shared__ float warp_ss[kNormRows][32];
+  __shared__ float row_r[kNormRows];
+  pdl_trigger();
+  pdl_wait();
   const int rows_out = G - row0;
-  const int b = blockIdx.x / rows_out;
-  const int t = row0 + blockIdx.x % rows_out;
   const int c = threadIdx.x * 8;
   const bool active = c < H;
-  const T* xr = x + (static_cast<size_t>(b) * G + t) * H;
-  float f[8];
-  float ss = 0.f;
-  if (active) {
-    load8(xr + c, f);
+  float f[kNormRows][8];
+  float g[8];
+  float ss[kNormRows];
+  if (active) load8(w + c, g);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+  for (int k = 0; k < kNormRows; ++k) {
+    const int o = blockIdx.x * kNormRows + k;  // output row
+    ss[k] = 0.f;
+    if (active && o < total_rows) {
+      const int b = o / rows_out;
+      const int t = row0 + o % rows_out;
+      load8(x + (static_cast<size_t>(b) * G + t) * H + c, f[k]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[k][i] = 0.f;
+    }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((threadIdx.x & 31) == 0) warp_ss[threadIdx.x >> 5] = ss;
+  for (int k = 0; k < kNormRows; ++k) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss[k] = fmaf(f[k][i], f[k][i], ss[k]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss[k] += __shfl_xor_sync(0xffffffffu, ss[k], o);
+    if ((threadIdx.x & 31) == 0) warp_ss[k][threadIdx.x >> 5] = ss[k];
+  }
   __syncthreads();
   if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? warp_ss[threadIdx.x] : 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (threadIdx.x == 0) row_r = rsqrtf(v / static_cast<float>(H) + eps);
+    for (int k = 0; k < kNormRows; ++k) {
+      float v = threadIdx.x < (blockDim.x >> 5) ? warp_ss[k][threadIdx.x] : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (threadIdx.x == 0) row_r[k] = rsqrtf(v / static_cast<float>(H) + eps);
+    }
   }
   __syncthreads();
   if (!active) return;
-  const float r = row_r;
-  float g[8];
-  load8(w + c, g);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) f[i] = f[i] * r * g[i];
-  store8(n + (static_cast<size_t>(b) * rows_out + (t - row0)) * H + c, f);
+  for (int k = 0; k < kNormRows; ++k) {
+    const int o = blockIdx.x * kNormRows + k;
+    if (o >= total_rows) break;
+    const float r = row_r[k];
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = f[k][i] * r * g[i];
+    store8(n + static_cast<size_t>(o) * H + c, v);
+  }
 }
 
 // prepare's apply pass: out = side-0 conv of n; coef1 = side 1's deltas (no base); d_full = D.
 // part: [k_splits][B*G][4*groups] fp32 split-K partial sums of D, column (side*2+tap)*groups + g.
-// Thread (t, v): row t of block blockIdx.y, channels 8*(blockIdx.x*vpc + v) .. +8. The thread
-// that starts a group also writes that group's side-1 deltas (and D when asked).
-template <typename T>
+// Thread (tg, v): rows tg*RPT .. tg*RPT+RPT-1 of block blockIdx.y, channels
+// 8*(blockIdx.x*vpc + v) .. +8. The thread that starts a group also writes that group's side-1
+// deltas (and D when asked).
+template <typename T, int RPT>
 __global__ void __launch_bounds__(kApplyMaxThreads)
     conv_side0_kernel(const T* __restrict__ n, const float* __restrict__ part, int k_splits,
                       const float* __restrict__ base, T* __restrict__ out, T* __restrict__ coef1,
                       float* __restrict__ d_full, int B, int G, int H, int gs, int groups, int vpc) {
-  const int t = threadIdx.x / vpc;
+  pdl_trigger();
+  pdl_wait();
+  const int t0 = (threadIdx.x / vpc) * RPT;
   const int c = (blockIdx.x * vpc + threadIdx.x % vpc) * 8;
-  if (t >= G || c >= H) return;
-  const size_t row = static_cast<size_t>(blockIdx.y) * G + t;
+  if (t0 >= G || c >= H) return;
+  const size_t row0 = static_cast<size_t>(blockIdx.y) * G + t0;
   const int g = c / gs;
   const int N = 4 * groups;
   const size_t MN = static_cast<size_t>(B) * G * N;
   const bool leader = (c % gs) == 0;
-  const float* pr = part + row * N + g;
-  float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-#pragma unroll 4
-  for (int s = 0; s < k_splits; ++s) {
-    d0 += __ldg(pr + s * MN);
-    d1 += __ldg(pr + s * MN + groups);
-  }
-  if (leader) {
-#pragma unroll 4
-    for (int s = 0; s < k_splits; ++s) {
-      d2 += __ldg(pr + s * MN + 2 * groups);
-      d3 += __ldg(pr + s * MN + 3 * groups);
-    }
-  }
-  float b0[8], b1[8], cur[8], prev[8], o[8];
+  float b0[8], b1[8], prev[8];
   load8(base + c, b0);      // base[0][0][c..]
   load8(base + H + c, b1);  // base[0][1][c..]
-  load8(n + row * H + c, cur);
-  if (t > 0) {
-    load8(n + (row - 1) * H + c, prev);
+  if (t0 > 0) {
+    load8(n + (row0 - 1) * H + c, prev);
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) prev[i] = 0.f;
   }
+  float cur[RPT][8];
+  float d0[RPT], d1[RPT], d2[RPT], d3[RPT];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = (b0[i] + d0) * cur[i] + (b1[i] + d1) * prev[i];
-  store8(out + row * H + c, o);
-  if (leader) {
-    store1(coef1 + (row * 2 + 0) * groups + g, d2);
-    store1(coef1 + (row * 2 + 1) * groups + g, d3);
-    if (d_full != nullptr) {
-      float* df = d_full + row * N + g;
-      df[0] = d0;
-      df[groups] = d1;
-      df[2 * groups] = d2;
-      df[3 * groups] = d3;
+  for (int k = 0; k < RPT; ++k) {
+    d0[k] = d1[k] = d2[k] = d3[k] = 0.f;
+    if (t0 + k >= G) continue;
+    load8(n + (row0 + k) * H + c, cur[k]);
+    const float* pr = part + (row0 + k) * N + g;
+    for (int s = 0; s < k_splits; ++s) {
+      d0[k] += __ldg(pr + s * MN);
+      d1[k] += __ldg(pr + s * MN + groups);
+    }
+    if (leader) {
+      for (int s = 0; s < k_splits; ++s) {
+        d2[k] += __ldg(pr + s * MN + 2 * groups);
+        d3[k] += __ldg(pr + s * MN + 3 * groups);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < RPT; ++k) {
+    if (t0 + k >= G) break;
+    const size_t row = row0 + k;
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = (b0[i] + d0[k]) * cur[k][i] + (b1[i] + d1[k]) * prev[i];
+    store8(out + row * H + c, o);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) prev[i] = cur[k][i];
+    if (leader) {
+      store1(coef1 + (row * 2 + 0) * groups + g, d2[k]);
+      store1(coef1 + (row * 2 + 1) * groups + g, d3[k]);
+      if (d_full != nullptr) {
+        float* df = d_full + row * N + g;
+        df[0] = d0[k];
+        df[groups] = d1[k];
+        df[2 * groups] = d2[k];
+        df[3 * groups] = d3[k];
+      }
     }
   }
 }
 
-// finish's apply pass: out = residual + side-1 conv of y (fp32 add, one rounding).
-template <typename T>
+// finish's apply pass: out = residual + side-1 conv of y (fp32 add, one rounding). `out` may be
+// `residual` (in place): every thread reads and then writes only its own rows and channels.
+template <typename T, int RPT>
 __global__ void __launch_bounds__(kApplyMaxThreads)
     conv_side1_kernel(const T* __restrict__ y, const T* __restrict__ coef1, const float* __restrict__ base,
                       const T* residual, T* out, int G, int H, int gs, int groups, int vpc) {
-  const int t = threadIdx.x / vpc;
+  pdl_trigger();
+  pdl_wait();
+  const int t0 = (threadIdx.x / vpc) * RPT;
   const int c = (blockIdx.x * vpc + threadIdx.x % vpc) * 8;
-  if (t >= G || c >= H) return;
-  const size_t row = static_cast<size_t>(blockIdx.y) * G + t;
+  if (t0 >= G || c >= H) return;
+  const size_t row0 = static_cast<size_t>(blockIdx.y) * G + t0;
   const int g = c / gs;
-  const float d0 = load1(coef1 + (row * 2 + 0) * groups + g);
-  const float d1 = load1(coef1 + (row * 2 + 1) * groups + g);
-  float b0[8], b1[8], cur[8], prev[8], res[8], o[8];
+  float b0[8], b1[8], prev[8];
   load8(base + 2 * H + c, b0);  // base[1][0][c..]
   load8(base + 3 * H + c, b1);  // base[1][1][c..]
-  load8(y + row * H + c, cur);
-  if (t > 0) {
-    load8(y + (row - 1) * H + c, prev);
+  if (t0 > 0) {
+    load8(y + (row0 - 1) * H + c, prev);
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) prev[i] = 0.f;
   }
-  if (residual != nullptr) {
-    load8(residual + row * H + c, res);
-  } else {
+  float cur[RPT][8], res[RPT][8], d0[RPT], d1[RPT];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) res[i] = 0.f;
+  for (int k = 0; k < RPT; ++k) {
+    if (t0 + k >= G) continue;
+    const size_t row = row0 + k;
+    load8(y + row * H + c, cur[k]);
+    if (residual != nullptr) {
+      load8(residual + row * H + c, res[k]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) res[k][i] = 0.f;
+    }
+    d0[k] = load1(coef1 + (row * 2 + 0) * groups + g);
+    d1[k] = load1(coef1 + (row * 2 + 1) * groups + g);
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = (b0[i] + d0) * cur[i] + (b1[i] + d1) * prev[i] + res[i];
-  store8(out + row * H + c, o);
+  for (int k = 0; k < RPT; ++k) {
+    if (t0 + k >= G) break;
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = (b0[i] + d0[k]) * cur[k][i] + (b1[i] + d1[k]) * prev[i] + res[k][i];
+    store8(out + (row0 + k) * H + c, o);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) prev[i] = cur[k][i];
+  }
 }
 
 }  // namespace
@@ -284,9 +353,10 @@ template <typename T>
 static int rms_rows_typed(const void* x, const void* w, float eps, void* n, int B, int G, int row0, int H,
                           cudaStream_t st) {
   const int threads = std::min(kNormThreads, ((H / 8 + 31) / 32) * 32);
-  rms_rows_kernel<T><<<B * (G - row0), threads, 0, st>>>(static_cast<const T*>(x), static_cast<const T*>(w), eps,
-                                                         static_cast<T*>(n), G, row0, H);
-  const cudaError_t e = cudaGetLastError();
+  const int total = B * (G - row0);
+  const cudaError_t e = launch_pdl(rms_rows_kernel<T>, dim3((total + kNormRows - 1) / kNormRows), dim3(threads), 0,
+                                   st, nullptr, 0, static_cast<const T*>(x), static_cast<const T*>(w), eps,
+                                   static_cast<T*>(n), G, row0, H, total);
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "rmsnorm launch failed: %s", cudaGetErrorString(e));
 }
 
@@ -304,16 +374,16 @@ int launch_conv_side0(const ConvShape& s, const void* n, const float* part, int 
                       void* out, void* coef1, float* d_full, cudaStream_t st) {
   const int vpc = vectors_per_cta(s.G);
   const dim3 grid((s.H / 8 + vpc - 1) / vpc, s.B);
-  const int threads = s.G * vpc;
+  const dim3 threads(row_groups(s.G) * vpc);
+  cudaError_t e;
   if (s.dtype == DFLASH2_F32)
-    conv_side0_kernel<float><<<grid, threads, 0, st>>>(static_cast<const float*>(n), part, k_splits, base,
-                                                       static_cast<float*>(out), static_cast<float*>(coef1), d_full,
-                                                       s.B, s.G, s.H, s.gs, s.groups, vpc);
+    e = launch_pdl(conv_side0_kernel<float, kRpt>, grid, threads, 0, st, nullptr, 0, static_cast<const float*>(n), part,
+                   k_splits, base, static_cast<float*>(out), static_cast<float*>(coef1), d_full, s.B, s.G, s.H, s.gs,
+                   s.groups, vpc);
   else
-    conv_side0_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(n), part, k_splits, base, static_cast<__nv_bfloat16*>(out),
-        static_cast<__nv_bfloat16*>(coef1), d_full, s.B, s.G, s.H, s.gs, s.groups, vpc);
-  const cudaError_t e = cudaGetLastError();
+    e = launch_pdl(conv_side0_kernel<__nv_bfloat16, kRpt>, grid, threads, 0, st, nullptr, 0,
+                   static_cast<const __nv_bfloat16*>(n), part, k_splits, base, static_cast<__nv_bfloat16*>(out),
+                   static_cast<__nv_bfloat16*>(coef1), d_full, s.B, s.G, s.H, s.gs, s.groups, vpc);
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "conv side0 launch failed: %s", cudaGetErrorString(e));
 }
 
@@ -321,16 +391,17 @@ int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, cons
                       void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st) {
   const int vpc = vectors_per_cta(s.G);
   const dim3 grid((s.H / 8 + vpc - 1) / vpc, s.B);
-  const int threads = s.G * vpc;
+  const dim3 threads(row_groups(s.G) * vpc);
+  cudaError_t e;
   if (s.dtype == DFLASH2_F32)
-    conv_side1_kernel<float><<<grid, threads, 0, st>>>(static_cast<const float*>(y), static_cast<const float*>(coef1),
-                                                       base, static_cast<const float*>(residual),
-                                                       static_cast<float*>(out), s.G, s.H, s.gs, s.groups, vpc);
+    e = launch_pdl(conv_side1_kernel<float, kRpt>, grid, threads, 0, st, nullptr, 0, static_cast<const float*>(y),
+                   static_cast<const float*>(coef1), base, static_cast<const float*>(residual),
+                   static_cast<float*>(out), s.G, s.H, s.gs, s.groups, vpc);
   else
-    conv_side1_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(y), static_cast<const __nv_bfloat16*>(coef1), base,
-        static_cast<const __nv_bfloat16*>(residual), static_cast<__nv_bfloat16*>(out), s.G, s.H, s.gs, s.groups, vpc);
-  const cudaError_t e = cudaGetLastError();
+    e = launch_pdl(conv_side1_kernel<__nv_bfloat16, kRpt>, grid, threads, 0, st, nullptr, 0,
+                   static_cast<const __nv_bfloat16*>(y), static_cast<const __nv_bfloat16*>(coef1), base,
+                   static_cast<const __nv_bfloat16*>(residual), static_cast<__nv_bfloat16*>(out), s.G, s.H, s.gs,
+                   s.groups, vpc);
   if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "conv side1 launch failed: %s", cudaGetErrorString(e));
   if (next_n == nullptr) return DFLASH2_OK;
   // The next RMSNorm as its own row-per-CTA pass: measured faster than fusing it into the

@@ -274,6 +274,8 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // no global memory is touched above this line
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -618,6 +620,8 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
   cluster_sync_all();  // both CTAs' barriers are initialised before anything arrives on them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // no global memory is touched above this line
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
@@ -859,6 +863,8 @@ __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
 __global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict__ lv, const int* __restrict__ li,
                                                          int n_splits, int M, int K, const int32_t* __restrict__ ids_map,
                                                          int32_t* __restrict__ cand, float* __restrict__ unary) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
@@ -995,8 +1001,8 @@ int launch_tc(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& m
   auto kern = tc_gemm_kernel<MT, TF32, MODE>;
   if (!ensure_smem_attr(kern, Cfg<MT>::kSmem, &done))
     return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(cudaGetLastError()));
-  kern<<<grid, Cfg<MT>::kThreads, Cfg<MT>::kSmem, st>>>(mA, mB, mE, args);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(Cfg<MT>::kThreads), Cfg<MT>::kSmem, st, nullptr, 0, mA, mB,
+                                   mE, args);
   if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "tc_gemm launch failed: %s", cudaGetErrorString(e));
   return DFLASH2_OK;
 }
@@ -1024,9 +1030,13 @@ int launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap&
   auto kern = tc_pair_kernel<TF32, MODE>;
   if (!ensure_smem_attr(kern, PairCfg<MODE>::kSmem, &done))
     return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed: %s", cudaGetErrorString(cudaGetLastError()));
-  cudaLaunchAttribute attr[1];
-  const cudaLaunchConfig_t cfg = pair_config<TF32, MODE>(pairs, st, attr);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mE, mD, args);
+  cudaLaunchAttribute cluster[1];
+  cluster[0].id = cudaLaunchAttributeClusterDimension;
+  cluster[0].val.clusterDim.x = 2;
+  cluster[0].val.clusterDim.y = 1;
+  cluster[0].val.clusterDim.z = 1;
+  const cudaError_t e = launch_pdl(kern, dim3(2 * pairs), dim3(PairCfg<MODE>::kThreads), PairCfg<MODE>::kSmem, st,
+                                   cluster, 1, mA, mB, mE, mD, args);
   if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "pair GEMM launch failed: %s", cudaGetErrorString(e));
   return DFLASH2_OK;
 }
@@ -1178,9 +1188,9 @@ int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bi
     rc = dispatch_tc<1>(plan.mt, p.dtype == DFLASH2_F32, mA, mB, mE, a, grid, st);
   if (rc != DFLASH2_OK) return rc;
   const int rows_per_block = 8;
-  topk_merge_kernel<<<(p.M + rows_per_block - 1) / rows_per_block, 32 * rows_per_block, 0, st>>>(
-      a.list_val, a.list_idx, plan.n_splits, p.M, K, ids_map, cand, unary);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(topk_merge_kernel, dim3((p.M + rows_per_block - 1) / rows_per_block),
+                                   dim3(32 * rows_per_block), 0, st, nullptr, 0, static_cast<const float*>(a.list_val),
+                                   static_cast<const int*>(a.list_idx), plan.n_splits, p.M, K, ids_map, cand, unary);
   if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "topk_merge launch failed: %s", cudaGetErrorString(e));
   return DFLASH2_OK;
 }

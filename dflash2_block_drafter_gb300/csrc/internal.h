@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -35,6 +36,35 @@ bool ensure_smem_attr(F* kern, int bytes, unsigned* done_mask) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
   *done_mask |= bit;
   return true;
+}
+
+// Programmatic dependent launch: every library kernel is launched with programmatic stream
+// serialization, lets its successor's CTAs be scheduled as soon as its own are all running
+// (griddepcontrol.launch_dependents at entry) and waits for its predecessor to complete, with
+// memory visible (griddepcontrol.wait), before its first global-memory access. The successor's
+// launch and prologue then overlap this kernel's last wave instead of following it.
+#ifndef DFL_PDL
+#define DFL_PDL 1
+#endif
+
+// cudaLaunchKernelEx with the programmatic-serialization attribute (and optional extra attributes).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       const cudaLaunchAttribute* extra, int n_extra, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[4];
+  int n = 0;
+  for (int i = 0; i < n_extra && n < 3; ++i) attr[n++] = extra[i];
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = DFL_PDL ? 1 : 0;
+  ++n;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------- conv (conv.cu)

@@ -13,6 +13,7 @@
 #include <cmath>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dfl {
 namespace {
@@ -75,6 +76,8 @@ __global__ void __launch_bounds__(kThreads)
                        int steps, int K, int R, int V, int lchunk, float* __restrict__ S, int32_t* __restrict__ path,
                        const int32_t* __restrict__ depths, int* err) {
   extern __shared__ float sm[];
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   const int RP = R + 1;  // padded row: the K successor rows of a slot fall in distinct banks
   int* sid = reinterpret_cast<int*>(sm);               // [steps*K] candidate ids
@@ -152,6 +155,8 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(128) select_path_kernel(const float* __restrict__ S, const int32_t* __restrict__ cand,
                                                           int B, int steps, int K, int32_t* __restrict__ path,
                                                           const int32_t* __restrict__ depths, int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
@@ -187,24 +192,23 @@ int launch_score_edges(const int32_t* cand, const float* unary, const float* z, 
   if (dtype == DFLASH2_F32) {
     if (!ensure_smem_attr(score_edges_kernel<float>, kSmemBudget, &done_f32)) e = cudaErrorInvalidValue;
     if (e == cudaSuccess)
-      score_edges_kernel<float><<<B, kThreads, smem, st>>>(cand, unary, z, anchors, static_cast<const float*>(pred),
-                                                           static_cast<const float*>(succ), steps, K, R, V, lchunk, S,
-                                                           path, depths, device_error_word());
+      e = launch_pdl(score_edges_kernel<float>, dim3(B), dim3(kThreads), smem, st, nullptr, 0, cand, unary, z, anchors,
+                     static_cast<const float*>(pred), static_cast<const float*>(succ), steps, K, R, V, lchunk, S, path,
+                     depths, device_error_word());
   } else {
     if (!ensure_smem_attr(score_edges_kernel<__nv_bfloat16>, kSmemBudget, &done_bf16)) e = cudaErrorInvalidValue;
     if (e == cudaSuccess)
-      score_edges_kernel<__nv_bfloat16><<<B, kThreads, smem, st>>>(
-          cand, unary, z, anchors, static_cast<const __nv_bfloat16*>(pred), static_cast<const __nv_bfloat16*>(succ),
-          steps, K, R, V, lchunk, S, path, depths, device_error_word());
+      e = launch_pdl(score_edges_kernel<__nv_bfloat16>, dim3(B), dim3(kThreads), smem, st, nullptr, 0, cand, unary, z,
+                     anchors, static_cast<const __nv_bfloat16*>(pred), static_cast<const __nv_bfloat16*>(succ), steps,
+                     K, R, V, lchunk, S, path, depths, device_error_word());
   }
-  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "score_edges launch failed: %s", cudaGetErrorString(e));
 }
 
 int launch_select_path(const float* S, const int32_t* cand, int B, int steps, int K, int32_t* path,
                        cudaStream_t st, const int32_t* depths) {
-  select_path_kernel<<<(B + 3) / 4, 128, 0, st>>>(S, cand, B, steps, K, path, depths, device_error_word());
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(select_path_kernel, dim3((B + 3) / 4), dim3(128), 0, st, nullptr, 0, S, cand, B,
+                                   steps, K, path, depths, device_error_word());
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "select_path launch failed: %s", cudaGetErrorString(e));
 }
 
