@@ -260,6 +260,157 @@ __global__ void __launch_bounds__(kApplyMaxThreads)
   }
 }
 
+// ------------------------------------------------------------------ streamed apply passes
+// Persistent CTAs over items (block b, 256-channel strip j). Warp kStreamConsumers (one lane)
+// streams each item's tiles into a shared-memory ring with TMA; the consumer warps compute from
+// shared memory and store 16-byte vectors. A CTA's items are all in flight as soon as it starts
+// (ring depth >= items per CTA at the drafter's shape), and the bytes in flight cost no registers.
+constexpr int kStreamSW = 256;        // channels per strip
+constexpr int kStreamConsumers = 8;   // consumer warps
+constexpr int kStreamThreads = 32 * (kStreamConsumers + 1);
+constexpr int kStreamMaxStages = 4;
+
+#ifndef DFL_STREAM
+#define DFL_STREAM 1
+#endif
+
+__device__ __forceinline__ void stream_abort(volatile int* abort_flag, int* err) {
+  *abort_flag = 1;
+  if (err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_TIMEOUT));
+}
+
+// Producer side of the ring: waits for the last fills still in flight after an abort.
+__device__ __forceinline__ void stream_drain(uint64_t* full, int stage, uint32_t phase, int issued, int n_stages) {
+  const int n = min(issued, n_stages);
+  for (int i = 0; i < n; ++i) {
+    if (stage == 0) {
+      stage = n_stages - 1;
+      phase ^= 1u;
+    } else {
+      --stage;
+    }
+    mbar_wait_bounded(smem_u32(&full[stage]), phase, nullptr, 100000000ull);
+  }
+}
+
+// finish's apply pass, streamed: out = residual + side-1 conv of y. Per item the ring stage holds
+// y[b, :, strip] (G x 256), residual[b, :, strip] and coef1[b, :, :, strip groups] (2G x 256/gs).
+template <typename T>
+__global__ void __launch_bounds__(kStreamThreads)
+    conv_side1_stream_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmR,
+                             const __grid_constant__ CUtensorMap tmC, const float* __restrict__ base, T* out, int G,
+                             int H, int gs, int n_items, int strips, int has_res, int n_stages, int stage_bytes,
+                             int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tileY = G * kStreamSW * static_cast<int>(sizeof(T));
+  const int cgrp = kStreamSW / gs;  // groups per strip
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + n_stages * stage_bytes);
+  uint64_t* empty = full + n_stages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + n_stages);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < n_stages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), kStreamConsumers);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmY);
+    if (has_res) prefetch_tmap(&tmR);
+    prefetch_tmap(&tmC);
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // no global memory is touched above this line
+  const uint32_t tx = static_cast<uint32_t>((has_res ? 2 : 1) * tileY + 2 * G * cgrp * static_cast<int>(sizeof(T)));
+
+  if (warp == kStreamConsumers) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_normal();
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int b = it / strips;
+        const int j = it - b * strips;
+        if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[stage]);
+        mbar_arrive_expect_tx(fb, tx);
+        uint8_t* st = smem + stage * stage_bytes;
+        tma_load_2d(smem_u32(st), &tmY, fb, j * kStreamSW, b * G, pol);
+        if (has_res) tma_load_2d(smem_u32(st + tileY), &tmR, fb, j * kStreamSW, b * G, pol);
+        tma_load_2d(smem_u32(st + 2 * tileY), &tmC, fb, j * cgrp, b * G * 2, pol);
+        ++issued;
+        if (++stage == n_stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        stream_abort(abort_flag, err);
+        stream_drain(full, stage, phase, issued, n_stages);
+      }
+    }
+    return;
+  }
+  // The grid is a multiple of `strips`, so a CTA's items share one strip and each consumer thread
+  // one 8-channel vector of it (lane = vector): its base-kernel values are loaded once, here.
+  const int j = blockIdx.x % strips;
+  const int v = lane;
+  const int c = j * kStreamSW + v * 8;
+  const int gl = (v * 8) / gs;
+  float b0[8], b1[8];
+  load8(base + 2 * H + c, b0);  // base[1][0][c..]
+  load8(base + 3 * H + c, b1);  // base[1][1][c..]
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const int b = it / strips;
+    if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+      if (lane == 0) stream_abort(abort_flag, err);
+      break;
+    }
+    const uint8_t* st = smem + stage * stage_bytes;
+    const T* sy = reinterpret_cast<const T*>(st);
+    const T* sr = reinterpret_cast<const T*>(st + tileY);
+    const T* sc = reinterpret_cast<const T*>(st + 2 * tileY);
+    for (int t = warp; t < G; t += kStreamConsumers) {
+      float cur[8], prev[8], res[8];
+      load8(sy + t * kStreamSW + v * 8, cur);
+      if (t > 0) {
+        load8(sy + (t - 1) * kStreamSW + v * 8, prev);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) prev[i] = 0.f;
+      }
+      if (has_res) {
+        load8(sr + t * kStreamSW + v * 8, res);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) res[i] = 0.f;
+      }
+      const float d0 = load1(sc + (t * 2 + 0) * cgrp + gl);
+      const float d1 = load1(sc + (t * 2 + 1) * cgrp + gl);
+      float o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = (b0[i] + d0) * cur[i] + (b1[i] + d1) * prev[i] + res[i];
+      store8(out + (static_cast<size_t>(b) * G + t) * H + c, o);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+    if (++stage == n_stages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
 }  // namespace
 
 // Split-K plan of kernel_projection, picked by a small cost model over the M tiles per CTA (1 or
@@ -387,8 +538,61 @@ int launch_conv_side0(const ConvShape& s, const void* n, const float* part, int 
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "conv side0 launch failed: %s", cudaGetErrorString(e));
 }
 
+// The streamed side-1 pass needs tiles TMA can express: whole 256-channel strips, 16-byte rows of
+// the coefficient tile and of coef1 itself, and at most 128 rows per block.
+static bool side1_streamable(const ConvShape& s) {
+  const int es = s.dtype == DFLASH2_F32 ? 4 : 2;
+  if (!(DFL_STREAM && s.H % kStreamSW == 0 && kStreamSW % s.gs == 0 && ((kStreamSW / s.gs) * es) % 16 == 0 &&
+        (s.groups * es) % 16 == 0 && 2 * s.G <= 256))
+    return false;
+  const int stage_bytes = ((2 * s.G * kStreamSW * es + 2 * s.G * (kStreamSW / s.gs) * es) + 1023) & ~1023;
+  return 1024 + 2 * stage_bytes + 128 <= 232448;  // a two-stage ring fits
+}
+
+template <typename T>
+static int launch_side1_stream(const ConvShape& s, const void* y, const void* coef1, const float* base,
+                               const void* residual, void* out, cudaStream_t st) {
+  const int dt = s.dtype;
+  const int es = static_cast<int>(sizeof(T));
+  const uint64_t rows = static_cast<uint64_t>(s.B) * s.G;
+  CUtensorMap mY, mR, mC;
+  const uint64_t dy[2] = {static_cast<uint64_t>(s.H), rows};
+  const uint64_t sy[1] = {static_cast<uint64_t>(s.H) * es};
+  const uint32_t by[2] = {static_cast<uint32_t>(kStreamSW), static_cast<uint32_t>(s.G)};
+  const uint64_t dc[2] = {static_cast<uint64_t>(s.groups), rows * 2};
+  const uint64_t sc[1] = {static_cast<uint64_t>(s.groups) * es};
+  const uint32_t bc[2] = {static_cast<uint32_t>(kStreamSW / s.gs), static_cast<uint32_t>(2 * s.G)};
+  if (!make_tmap_plain(&mY, y, dt, 2, dy, sy, by) || !make_tmap_plain(&mC, coef1, dt, 2, dc, sc, bc) ||
+      (residual != nullptr && !make_tmap_plain(&mR, residual, dt, 2, dy, sy, by)))
+    return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (side-1 stream)");
+  if (residual == nullptr) mR = mY;
+  const int tileY = s.G * kStreamSW * es;
+  const int stage_bytes = ((2 * tileY + 2 * s.G * (kStreamSW / s.gs) * es) + 1023) & ~1023;
+  const int n_stages = std::max(2, std::min(kStreamMaxStages, (200 * 1024) / stage_bytes));
+  const int smem = 1024 + n_stages * stage_bytes + 128;
+  const int per_sm = std::max(1, std::min(3, 232448 / smem));
+  const int strips = s.H / kStreamSW;
+  const int n_items = s.B * strips;
+  // a multiple of `strips` (each CTA keeps one strip), at most one wave
+  const int grid = std::min(n_items, std::max(1, sm_count() * per_sm / strips) * strips);
+  static unsigned done = 0;
+  if (!ensure_smem_attr(conv_side1_stream_kernel<T>, 232448, &done))  // once, for every shape's ring
+    return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed (side-1 stream)");
+  const cudaError_t e = launch_pdl(conv_side1_stream_kernel<T>, dim3(grid), dim3(kStreamThreads), smem, st, nullptr, 0,
+                                   mY, mR, mC, base, static_cast<T*>(out), s.G, s.H, s.gs, n_items, strips,
+                                   residual != nullptr ? 1 : 0, n_stages, stage_bytes, device_error_word());
+  return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "side-1 stream launch failed: %s", cudaGetErrorString(e));
+}
+
 int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, const float* base, const void* residual,
                       void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st) {
+  if (side1_streamable(s)) {
+    const int rc = s.dtype == DFLASH2_F32 ? launch_side1_stream<float>(s, y, coef1, base, residual, out, st)
+                                          : launch_side1_stream<__nv_bfloat16>(s, y, coef1, base, residual, out, st);
+    if (rc != DFLASH2_OK) return rc;
+    if (next_n == nullptr) return DFLASH2_OK;
+    return launch_rmsnorm_rows(out, next_w, eps, next_n, s.B, s.G, next_row0, s.H, s.dtype, st);
+  }
   const int vpc = vectors_per_cta(s.G);
   const dim3 grid((s.H / 8 + vpc - 1) / vpc, s.B);
   const dim3 threads(row_groups(s.G) * vpc);

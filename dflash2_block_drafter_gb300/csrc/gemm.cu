@@ -1150,6 +1150,25 @@ size_t head_workspace(int M, int V, int K, int R, int sms) {
 
 int gemm_pair_capacity() { return pair_capacity(); }
 
+bool make_tmap_plain(CUtensorMap* m, const void* ptr, int dtype, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr || rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+  const CUresult r = enc(m, dtype == DFLASH2_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), d, st, b, e,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int launch_gemm_store(const GemmProblem& p, const GemmPlan& plan, float* part, cudaStream_t st) {
   CUtensorMap mA, mB, mE;
   GemmArgs a;

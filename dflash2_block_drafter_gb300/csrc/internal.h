@@ -6,6 +6,7 @@
 #include <mutex>
 #include <utility>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "dflash2.h"
@@ -66,6 +67,11 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
+
+// Encodes a tiled, non-swizzled tensor map: dims / box innermost first, strides in bytes for
+// dims 1.. (rank - 1 of them). dtype is DFLASH2_BF16 or DFLASH2_F32. False on failure.
+bool make_tmap_plain(CUtensorMap* m, const void* ptr, int dtype, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box);
 
 // ---------------------------------------------------------------- conv (conv.cu)
 struct ConvShape {
