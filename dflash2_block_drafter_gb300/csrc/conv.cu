@@ -411,6 +411,174 @@ __global__ void __launch_bounds__(kStreamThreads)
   }
 }
 
+__host__ __device__ constexpr int round128(int b) { return (b + 127) & ~127; }
+
+// The value a float becomes when stored as T.
+template <typename T>
+__device__ __forceinline__ float round_as(float v);
+template <>
+__device__ __forceinline__ float round_as<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ float round_as<__nv_bfloat16>(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// finish fused with the next RMSNorm. A cluster of C CTAs owns block b; CTA r of the cluster owns
+// the channels [r*SPC*256, (r+1)*SPC*256) of all G rows, one resident shared-memory stage per
+// 256-channel strip (y, residual, coefficient, base-kernel and norm-weight tiles, all loaded by TMA
+// at the start). Pass 1 writes x = residual + side-1 conv of y (rounded to T, to memory and over
+// the residual tile) and each row's partial sum of squares; each row belongs to one warp, so a
+// warp reduction gives the CTA's partial. The C partials of every row are exchanged through
+// distributed shared memory across a cluster barrier; pass 2 writes n = x * rsqrt(mean + eps) * w
+// for rows next_row0..G-1 (compact when next_row0 = 1: the head's h).
+template <typename T>
+__global__ void __launch_bounds__(kStreamThreads)
+    conv_finish_norm_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmR,
+                            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmW, T* out, T* next_n, float eps, int G, int H,
+                            int gs, int spc, int csize, int has_res, int next_row0, int stage_bytes, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int es = static_cast<int>(sizeof(T));
+  const int tileY = G * kStreamSW * es;
+  const int cgrp = kStreamSW / gs;
+  const int offR = round128(tileY);
+  const int offC = offR + round128(tileY);
+  const int offB = offC + round128(2 * G * cgrp * es);
+  const int offW = offB + 2 * kStreamSW * 4;
+  float* ss_all = reinterpret_cast<float*>(smem + spc * stage_bytes);  // [csize][G]
+  uint64_t* full = reinterpret_cast<uint64_t*>(ss_all + 8 * 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + spc);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int b = static_cast<int>(blockIdx.x) / csize;
+  const int strip0 = static_cast<int>(rank) * spc;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < spc; ++s) mbar_init(smem_u32(&full[s]), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmY);
+    if (has_res) prefetch_tmap(&tmR);
+    prefetch_tmap(&tmC);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmW);
+  }
+  __syncthreads();
+  cluster_arrive_relaxed();  // every CTA of the cluster has started once the matching wait returns
+  pdl_trigger();
+  pdl_wait();  // no global memory is touched above this line
+
+  if (warp == kStreamConsumers) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_normal();
+      const uint32_t tx = static_cast<uint32_t>((has_res ? 2 : 1) * tileY + 2 * G * cgrp * es + 2 * kStreamSW * 4 +
+                                                kStreamSW * es);
+      for (int s = 0; s < spc; ++s) {
+        const uint32_t fb = smem_u32(&full[s]);
+        const int x0 = (strip0 + s) * kStreamSW;
+        uint8_t* st = smem + s * stage_bytes;
+        mbar_arrive_expect_tx(fb, tx);
+        tma_load_2d(smem_u32(st), &tmY, fb, x0, b * G, pol);
+        if (has_res) tma_load_2d(smem_u32(st + offR), &tmR, fb, x0, b * G, pol);
+        tma_load_2d(smem_u32(st + offC), &tmC, fb, (strip0 + s) * cgrp, b * G * 2, pol);
+        tma_load_2d(smem_u32(st + offB), &tmB, fb, x0, 2, pol);  // base[1][0..1][strip]
+        tma_load_2d(smem_u32(st + offW), &tmW, fb, x0, 0, pol);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- pass 1: x and the rows' partial sums of squares (lane = 8-channel vector of a strip)
+    const int v = lane;
+    const int gl = (v * 8) / gs;
+    float ss[4] = {0.f, 0.f, 0.f, 0.f};  // rows warp + 8k (G <= 32)
+    bool ok = true;
+    for (int s = 0; s < spc && ok; ++s) {
+      if (!mbar_wait_bounded(smem_u32(&full[s]), 0, abort_flag, kWaitLimitNs)) {
+        if (lane == 0) stream_abort(abort_flag, err);
+        ok = false;
+        break;
+      }
+      uint8_t* st = smem + s * stage_bytes;
+      const T* sy = reinterpret_cast<const T*>(st);
+      T* sr = reinterpret_cast<T*>(st + offR);
+      const T* sc = reinterpret_cast<const T*>(st + offC);
+      const float* sb = reinterpret_cast<const float*>(st + offB);
+      const int c = (strip0 + s) * kStreamSW + v * 8;
+      float b0[8], b1[8];
+      load8(sb + v * 8, b0);              // base[1][0][c..]
+      load8(sb + kStreamSW + v * 8, b1);  // base[1][1][c..]
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int t = warp + k * kStreamConsumers;
+        if (t >= G) break;
+        float cur[8], prev[8], res[8];
+        load8(sy + t * kStreamSW + v * 8, cur);
+        if (t > 0) {
+          load8(sy + (t - 1) * kStreamSW + v * 8, prev);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) prev[i] = 0.f;
+        }
+        if (has_res) {
+          load8(sr + t * kStreamSW + v * 8, res);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) res[i] = 0.f;
+        }
+        const float d0 = load1(sc + (t * 2 + 0) * cgrp + gl);
+        const float d1 = load1(sc + (t * 2 + 1) * cgrp + gl);
+        float o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = round_as<T>((b0[i] + d0) * cur[i] + (b1[i] + d1) * prev[i] + res[i]);
+        store8(out + (static_cast<size_t>(b) * G + t) * H + c, o);
+        store8(sr + t * kStreamSW + v * 8, o);  // x as stored, for pass 2
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss[k] = fmaf(o[i], o[i], ss[k]);
+      }
+    }
+    // the CTA's partial of each of this warp's rows, to every CTA of the cluster
+    cluster_wait();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int t = warp + k * kStreamConsumers;
+      if (t >= G) break;
+      float q = ss[k];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+      if (lane < csize) st_shared_cluster_f32(mapa_shared(smem_u32(&ss_all[rank * G + t]), lane), q);
+    }
+  }
+  if (warp == kStreamConsumers) cluster_wait();
+  cluster_sync_all();  // every partial has arrived in every CTA
+
+  if (warp < kStreamConsumers && *abort_flag == 0) {
+    // ---- pass 2: n = x * r * w for rows next_row0 .. G-1
+    const int v = lane;
+    const int rows_out = G - next_row0;
+    for (int t = warp; t < G; t += kStreamConsumers) {
+      if (t < next_row0) continue;
+      float tot = 0.f;
+      for (int q = 0; q < csize; ++q) tot += ss_all[q * G + t];
+      const float r = rsqrtf(tot / static_cast<float>(H) + eps);
+      for (int s = 0; s < spc; ++s) {
+        const uint8_t* st = smem + s * stage_bytes;
+        const T* sr = reinterpret_cast<const T*>(st + offR);
+        const T* sw = reinterpret_cast<const T*>(st + offW);
+        float x8[8], w8[8], o[8];
+        load8(sr + t * kStreamSW + v * 8, x8);
+        load8(sw + v * 8, w8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = x8[i] * r * w8[i];
+        store8(next_n + (static_cast<size_t>(b) * rows_out + (t - next_row0)) * H + (strip0 + s) * kStreamSW + v * 8, o);
+      }
+    }
+  }
+}
+
 }  // namespace
 
 // Split-K plan of kernel_projection, picked by a small cost model over the M tiles per CTA (1 or
@@ -584,8 +752,88 @@ static int launch_side1_stream(const ConvShape& s, const void* y, const void* co
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "side-1 stream launch failed: %s", cudaGetErrorString(e));
 }
 
+// finish + next RMSNorm in one kernel: a cluster of csize CTAs per block, spc resident strips per
+// CTA. Returns the cluster size (0: not eligible). Prefers the largest cluster that keeps the grid
+// in one wave with two CTAs per SM.
+static int finish_norm_stage_bytes(const ConvShape& s) {  // matches the kernel's tile offsets
+  const int es = s.dtype == DFLASH2_F32 ? 4 : 2;
+  const int b = 2 * round128(s.G * kStreamSW * es) + round128(2 * s.G * (kStreamSW / s.gs) * es) + 2 * kStreamSW * 4 +
+                kStreamSW * es;
+  return (b + 1023) & ~1023;
+}
+static size_t finish_norm_smem(const ConvShape& s, int spc) {
+  return 1024 + static_cast<size_t>(spc) * finish_norm_stage_bytes(s) + 8 * 64 * 4 + 8 * spc + 64;
+}
+static int finish_norm_cluster(const ConvShape& s) {
+  if (!side1_streamable(s) || s.G > 32) return 0;
+  const int strips = s.H / kStreamSW;
+  int any = 0;
+  for (int c = 8; c >= 1; --c) {
+    if (strips % c != 0) continue;
+    const size_t sm = finish_norm_smem(s, strips / c);
+    if (sm > 232448) continue;
+    const int per_sm = static_cast<int>(std::min<size_t>(2, 232448 / sm));
+    if (s.B * c <= sm_count() * per_sm) return c;
+    if (any == 0) any = c;
+  }
+  return any;
+}
+
+template <typename T>
+static int launch_finish_norm(const ConvShape& s, int csize, const void* y, const void* coef1, const float* base,
+                              const void* residual, void* out, const void* next_w, float eps, void* next_n,
+                              int next_row0, cudaStream_t st) {
+  const int dt = s.dtype;
+  const int es = static_cast<int>(sizeof(T));
+  const uint64_t rows = static_cast<uint64_t>(s.B) * s.G;
+  CUtensorMap mY, mR, mC, mB, mW;
+  const uint64_t dy[2] = {static_cast<uint64_t>(s.H), rows};
+  const uint64_t sy[1] = {static_cast<uint64_t>(s.H) * es};
+  const uint32_t by[2] = {static_cast<uint32_t>(kStreamSW), static_cast<uint32_t>(s.G)};
+  const uint64_t dc[2] = {static_cast<uint64_t>(s.groups), rows * 2};
+  const uint64_t sc[1] = {static_cast<uint64_t>(s.groups) * es};
+  const uint32_t bc[2] = {static_cast<uint32_t>(kStreamSW / s.gs), static_cast<uint32_t>(2 * s.G)};
+  const uint64_t db[2] = {static_cast<uint64_t>(s.H), 4};
+  const uint64_t sb[1] = {static_cast<uint64_t>(s.H) * 4};
+  const uint32_t bb[2] = {static_cast<uint32_t>(kStreamSW), 2};
+  const uint64_t dw[2] = {static_cast<uint64_t>(s.H), 1};
+  const uint64_t sw[1] = {static_cast<uint64_t>(s.H) * es};
+  const uint32_t bw[2] = {static_cast<uint32_t>(kStreamSW), 1};
+  if (!make_tmap_plain(&mY, y, dt, 2, dy, sy, by) || !make_tmap_plain(&mC, coef1, dt, 2, dc, sc, bc) ||
+      !make_tmap_plain(&mB, base, DFLASH2_F32, 2, db, sb, bb) || !make_tmap_plain(&mW, next_w, dt, 2, dw, sw, bw) ||
+      (residual != nullptr && !make_tmap_plain(&mR, residual, dt, 2, dy, sy, by)))
+    return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (finish + norm)");
+  if (residual == nullptr) mR = mY;
+  const int spc = (s.H / kStreamSW) / csize;
+  const int smem = static_cast<int>(finish_norm_smem(s, spc));
+  static unsigned done = 0;
+  if (!ensure_smem_attr(conv_finish_norm_kernel<T>, 232448, &done))
+    return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed (finish + norm)");
+  cudaLaunchAttribute cl[1];
+  cl[0].id = cudaLaunchAttributeClusterDimension;
+  cl[0].val.clusterDim.x = static_cast<unsigned>(csize);
+  cl[0].val.clusterDim.y = 1;
+  cl[0].val.clusterDim.z = 1;
+  const cudaError_t e = launch_pdl(conv_finish_norm_kernel<T>, dim3(s.B * csize), dim3(kStreamThreads), smem, st, cl, 1,
+                                   mY, mR, mC, mB, mW, static_cast<T*>(out), static_cast<T*>(next_n), eps, s.G, s.H,
+                                   s.gs, spc, csize, residual != nullptr ? 1 : 0, next_row0,
+                                   finish_norm_stage_bytes(s), device_error_word());
+  return e == cudaSuccess ? DFLASH2_OK
+                          : fail(DFLASH2_ERR_CUDA, "finish + norm launch failed: %s", cudaGetErrorString(e));
+}
+
+#ifndef DFL_FINISH_NORM
+#define DFL_FINISH_NORM 1
+#endif
+
 int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, const float* base, const void* residual,
                       void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st) {
+  const int csize = (DFL_FINISH_NORM && next_n != nullptr) ? finish_norm_cluster(s) : 0;
+  if (csize > 0)
+    return s.dtype == DFLASH2_F32
+               ? launch_finish_norm<float>(s, csize, y, coef1, base, residual, out, next_w, eps, next_n, next_row0, st)
+               : launch_finish_norm<__nv_bfloat16>(s, csize, y, coef1, base, residual, out, next_w, eps, next_n,
+                                                   next_row0, st);
   if (side1_streamable(s)) {
     const int rc = s.dtype == DFLASH2_F32 ? launch_side1_stream<float>(s, y, coef1, base, residual, out, st)
                                           : launch_side1_stream<__nv_bfloat16>(s, y, coef1, base, residual, out, st);
