@@ -579,6 +579,139 @@ __global__ void __launch_bounds__(kStreamThreads)
   }
 }
 
+// prepare's apply pass, streamed: out = side-0 conv of n, coef1 = side 1's deltas, d_full = D.
+// Per item (block b, strip j) the ring stage holds n[b, :, strip] (G x 256) and, for every K split
+// s and (side, tap) st, the G x (256/gs) tile of the fp32 partial sums of D for the strip's groups.
+// The grid is a multiple of `strips`, so each CTA keeps one strip and its base kernel in registers.
+template <typename T>
+__global__ void __launch_bounds__(kStreamThreads)
+    conv_side0_stream_kernel(const __grid_constant__ CUtensorMap tmN, const __grid_constant__ CUtensorMap tmP,
+                             const float* __restrict__ base, T* out, T* coef1, float* d_full, int G, int H, int gs,
+                             int groups, int k_splits, int M, int n_items, int strips, int n_stages, int stage_bytes,
+                             int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int es = static_cast<int>(sizeof(T));
+  const int cgrp = kStreamSW / gs;
+  const int tileN = round128(G * kStreamSW * es);
+  const int tileP = round128(G * cgrp * 4);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + n_stages * stage_bytes);
+  uint64_t* empty = full + n_stages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + n_stages);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < n_stages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), kStreamConsumers);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmN);
+    prefetch_tmap(&tmP);
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // no global memory is touched above this line
+  const uint32_t tx = static_cast<uint32_t>(G * kStreamSW * es + 4 * k_splits * G * cgrp * 4);
+
+  if (warp == kStreamConsumers) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_normal();
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int b = it / strips;
+        const int j = it - b * strips;
+        if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[stage]);
+        mbar_arrive_expect_tx(fb, tx);
+        uint8_t* st = smem + stage * stage_bytes;
+        tma_load_2d(smem_u32(st), &tmN, fb, j * kStreamSW, b * G, pol);
+        for (int s = 0; s < k_splits; ++s)
+          for (int q = 0; q < 4; ++q)
+            tma_load_2d(smem_u32(st + tileN + (s * 4 + q) * tileP), &tmP, fb, q * groups + j * cgrp, s * M + b * G,
+                        pol);
+        ++issued;
+        if (++stage == n_stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        stream_abort(abort_flag, err);
+        stream_drain(full, stage, phase, issued, n_stages);
+      }
+    }
+    return;
+  }
+  const int j = blockIdx.x % strips;
+  const int v = lane;
+  const int c = j * kStreamSW + v * 8;
+  const int gl = (v * 8) / gs;
+  const int g = j * cgrp + gl;
+  const bool leader = ((v * 8) % gs) == 0;
+  const int N = 4 * groups;
+  float b0[8], b1[8];
+  load8(base + c, b0);      // base[0][0][c..]
+  load8(base + H + c, b1);  // base[0][1][c..]
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const int b = it / strips;
+    if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+      if (lane == 0) stream_abort(abort_flag, err);
+      break;
+    }
+    const uint8_t* st = smem + stage * stage_bytes;
+    const T* sn = reinterpret_cast<const T*>(st);
+    const float* sp = reinterpret_cast<const float*>(st + tileN);
+    const int pstride = tileP / 4;  // floats between consecutive (split, side-tap) tiles
+    for (int t = warp; t < G; t += kStreamConsumers) {
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < k_splits; ++s) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d[q] += sp[(s * 4 + q) * pstride + t * cgrp + gl];
+      }
+      float cur[8], prev[8];
+      load8(sn + t * kStreamSW + v * 8, cur);
+      if (t > 0) {
+        load8(sn + (t - 1) * kStreamSW + v * 8, prev);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) prev[i] = 0.f;
+      }
+      float o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = (b0[i] + d[0]) * cur[i] + (b1[i] + d[1]) * prev[i];
+      const size_t row = static_cast<size_t>(b) * G + t;
+      store8(out + row * H + c, o);
+      if (leader) {
+        store1(coef1 + (row * 2 + 0) * groups + g, d[2]);
+        store1(coef1 + (row * 2 + 1) * groups + g, d[3]);
+        if (d_full != nullptr) {
+          float* df = d_full + row * N + g;
+          df[0] = d[0];
+          df[groups] = d[1];
+          df[2 * groups] = d[2];
+          df[3 * groups] = d[3];
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+    if (++stage == n_stages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
 }  // namespace
 
 // Split-K plan of kernel_projection, picked by a small cost model over the M tiles per CTA (1 or
@@ -689,8 +822,63 @@ int launch_rmsnorm(const void* x, const void* w, float eps, void* n, int rows, i
   return launch_rmsnorm_rows(x, w, eps, n, rows, 1, 0, H, dtype, st);
 }
 
+#ifndef DFL_STREAM0
+#define DFL_STREAM0 1
+#endif
+
+static int side0_stage_bytes(const ConvShape& s, int k_splits) {
+  const int es = s.dtype == DFLASH2_F32 ? 4 : 2;
+  const int b = round128(s.G * kStreamSW * es) + 4 * k_splits * round128(s.G * (kStreamSW / s.gs) * 4);
+  return (b + 1023) & ~1023;
+}
+
+// The streamed side-0 pass needs whole 256-channel strips, partial-sum tiles TMA can address
+// (16-byte rows: 256/gs groups a multiple of 4, groups a multiple of 4) and a two-stage ring.
+static bool side0_streamable(const ConvShape& s, int k_splits) {
+  if (!(DFL_STREAM && DFL_STREAM0 && s.H % kStreamSW == 0 && kStreamSW % s.gs == 0 && (kStreamSW / s.gs) % 4 == 0 &&
+        s.groups % 4 == 0 && s.G <= 256))
+    return false;
+  return 1024 + 2 * side0_stage_bytes(s, k_splits) + 128 <= 232448;
+}
+
+template <typename T>
+static int launch_side0_stream(const ConvShape& s, const void* n, const float* part, int k_splits, const float* base,
+                               void* out, void* coef1, float* d_full, cudaStream_t st) {
+  const int es = static_cast<int>(sizeof(T));
+  const uint64_t rows = static_cast<uint64_t>(s.B) * s.G;
+  const int N = 4 * s.groups;
+  CUtensorMap mN, mP;
+  const uint64_t dn[2] = {static_cast<uint64_t>(s.H), rows};
+  const uint64_t sn[1] = {static_cast<uint64_t>(s.H) * es};
+  const uint32_t bn[2] = {static_cast<uint32_t>(kStreamSW), static_cast<uint32_t>(s.G)};
+  const uint64_t dp[2] = {static_cast<uint64_t>(N), rows * k_splits};
+  const uint64_t sp[1] = {static_cast<uint64_t>(N) * 4};
+  const uint32_t bp[2] = {static_cast<uint32_t>(kStreamSW / s.gs), static_cast<uint32_t>(s.G)};
+  if (!make_tmap_plain(&mN, n, s.dtype, 2, dn, sn, bn) || !make_tmap_plain(&mP, part, DFLASH2_F32, 2, dp, sp, bp))
+    return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (side-0 stream)");
+  const int stage_bytes = side0_stage_bytes(s, k_splits);
+  const int n_stages = std::max(2, std::min(kStreamMaxStages, (160 * 1024) / stage_bytes));
+  const int smem = 1024 + n_stages * stage_bytes + 128;
+  const int per_sm = std::max(1, std::min(3, 232448 / smem));
+  const int strips = s.H / kStreamSW;
+  const int n_items = s.B * strips;
+  const int grid = std::min(n_items, std::max(1, sm_count() * per_sm / strips) * strips);
+  static unsigned done = 0;
+  if (!ensure_smem_attr(conv_side0_stream_kernel<T>, 232448, &done))
+    return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed (side-0 stream)");
+  const cudaError_t e = launch_pdl(conv_side0_stream_kernel<T>, dim3(grid), dim3(kStreamThreads), smem, st, nullptr, 0,
+                                   mN, mP, base, static_cast<T*>(out), static_cast<T*>(coef1), d_full, s.G, s.H, s.gs,
+                                   s.groups, k_splits, static_cast<int>(rows), n_items, strips, n_stages, stage_bytes,
+                                   device_error_word());
+  return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "side-0 stream launch failed: %s", cudaGetErrorString(e));
+}
+
 int launch_conv_side0(const ConvShape& s, const void* n, const float* part, int k_splits, const float* base,
                       void* out, void* coef1, float* d_full, cudaStream_t st) {
+  if (side0_streamable(s, k_splits))
+    return s.dtype == DFLASH2_F32
+               ? launch_side0_stream<float>(s, n, part, k_splits, base, out, coef1, d_full, st)
+               : launch_side0_stream<__nv_bfloat16>(s, n, part, k_splits, base, out, coef1, d_full, st);
   const int vpc = vectors_per_cta(s.G);
   const dim3 grid((s.H / 8 + vpc - 1) / vpc, s.B);
   const dim3 threads(row_groups(s.G) * vpc);
