@@ -10,6 +10,7 @@
 // dependent chain; S is built there in fp32 and the 'steps'-long walk runs from shared memory.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "internal.h"
@@ -172,6 +173,169 @@ __global__ void __launch_bounds__(128) select_path_kernel(const float* __restric
   }
 }
 
+// Warp-per-slot variant (the drafter's shapes): warp w of block b's CTA handles slots w, w + nw, ...
+// It issues every 16-byte segment load of the slot's 2K codebook rows before using any of them
+// (one latency round per slot instead of one per loop iteration), keeps pred*z and succ rows in its
+// own padded shared-memory rows, and computes the K x K scores with float4 reads (the lanes of a
+// quarter-warp read different succ rows at a 4-bank offset: no conflicts). Then warp 0 walks.
+constexpr int kEdgeWarpsMax = 16;
+
+__device__ __forceinline__ uint4 ldg16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ void unpack16(const uint4& u, const __nv_bfloat16*, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __bfloat1622float2(h[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+__device__ __forceinline__ void unpack16(const uint4& u, const float*, float* f) {
+  f[0] = __uint_as_float(u.x);
+  f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z);
+  f[3] = __uint_as_float(u.w);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kEdgeWarpsMax)
+    score_edges_warp_kernel(const int32_t* __restrict__ cand, const float* __restrict__ unary,
+                            const float* __restrict__ z, const int32_t* __restrict__ anchors,
+                            const T* __restrict__ pred, const T* __restrict__ succ, int steps, int K, int R, int V,
+                            float* __restrict__ S, int32_t* __restrict__ path, const int32_t* __restrict__ depths,
+                            int tiled, int* err) {
+  extern __shared__ float sm[];
+  pdl_trigger();
+  pdl_wait();
+  constexpr int E = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte segment
+  const int b = blockIdx.x;
+  const int nw = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int RP = R + 4;  // padded row in floats (16-byte aligned, 4-bank offset between rows)
+  float* sS = sm;        // [steps][K][K]
+  float* rows = sm + ((steps * K * K + 3) & ~3) + warp * (2 * K * RP);  // [K] pred*z rows, [K] succ rows
+  const int anchor = anchors[b];
+  const int segs = R / E;
+  const int items = 2 * K * segs;
+  for (int l = warp; l < steps; l += nw) {
+    const size_t slot = static_cast<size_t>(b) * steps + l;
+    const float* zl = z + slot * R;
+    // K = 16: this lane's four unary values, loaded before the gathers (no dependence on them)
+    const float4 un4 = tiled ? __ldg(reinterpret_cast<const float4*>(unary + slot * K) + (lane & 3))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    // When 32 is a multiple of segs every item of this lane has the same segment: its z values
+    // are loaded here, alongside the gathers rather than after them.
+    const bool fixed_sg = (32 % segs) == 0;
+    float zf[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) zf[e] = fixed_sg ? __ldg(zl + (lane % segs) * E + e) : 0.f;
+    for (int q0 = 0; q0 < items; q0 += 32 * 8) {
+      uint4 buf[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = q0 + i * 32 + lane;
+        buf[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (q < items) {
+          const int row = q / segs;
+          const int sg = q - row * segs;
+          const bool is_pred = row < K;
+          const int id = is_pred ? (l == 0 ? anchor : cand[(slot - 1) * K + row]) : cand[slot * K + row - K];
+          if (id >= 0 && id < V) {
+            buf[i] = ldg16((is_pred ? pred : succ) + static_cast<size_t>(id) * R + sg * E);
+          } else if (err != nullptr) {
+            atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_BAD_INDEX));
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = q0 + i * 32 + lane;
+        if (q < items) {
+          const int row = q / segs;
+          const int sg = q - row * segs;
+          float f[E];
+          unpack16(buf[i], static_cast<const T*>(nullptr), f);
+          float* dst = rows + row * RP + sg * E;
+          if (row < K) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) dst[e] = f[e] * (fixed_sg ? zf[e] : __ldg(zl + sg * E + e));
+          } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) dst[e] = f[e];
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (tiled) {
+      // K = 16 (unary and S 16-byte aligned): 2 x 4 register tile per lane: rows p0, p0+1 of pred*z against succ rows c0..c0+3, so each
+      // 4-wide step of r reads 6 float4 for 32 multiply-adds (same order of r as the plain loop)
+      const int p0 = 2 * (lane >> 2);
+      const int c0 = 4 * (lane & 3);
+      float acc[2][4] = {};
+      for (int r = 0; r < R; r += 4) {
+        float4 a4[2], c4[4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) a4[i] = *reinterpret_cast<const float4*>(rows + (p0 + i) * RP + r);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c4[j] = *reinterpret_cast<const float4*>(rows + (K + c0 + j) * RP + r);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[i][j] = fmaf(a4[i].x, c4[j].x, acc[i][j]);
+            acc[i][j] = fmaf(a4[i].y, c4[j].y, acc[i][j]);
+            acc[i][j] = fmaf(a4[i].z, c4[j].z, acc[i][j]);
+            acc[i][j] = fmaf(a4[i].w, c4[j].w, acc[i][j]);
+          }
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        float4 o;
+        o.x = un4.x + acc[i][0];
+        o.y = un4.y + acc[i][1];
+        o.z = un4.z + acc[i][2];
+        o.w = un4.w + acc[i][3];
+        *reinterpret_cast<float4*>(sS + (l * K + p0 + i) * K + c0) = o;
+        if (S != nullptr) *reinterpret_cast<float4*>(S + (slot * K + p0 + i) * K + c0) = o;
+      }
+    } else {
+      for (int e = lane; e < K * K; e += 32) {
+        const int p = e / K;
+        const int c = e - p * K;
+        const float* wr = rows + p * RP;
+        const float* cr = rows + (K + c) * RP;
+        float acc = 0.f;
+        for (int r = 0; r < R; r += 4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(wr + r);
+          const float4 c4 = *reinterpret_cast<const float4*>(cr + r);
+          acc = fmaf(a4.x, c4.x, acc);
+          acc = fmaf(a4.y, c4.y, acc);
+          acc = fmaf(a4.z, c4.z, acc);
+          acc = fmaf(a4.w, c4.w, acc);
+        }
+        const float s = __ldg(unary + slot * K + c) + acc;
+        sS[(l * K + p) * K + c] = s;
+        if (S != nullptr) S[(slot * K + p) * K + c] = s;
+      }
+    }
+    __syncwarp();  // the next slot overwrites this warp's rows
+  }
+  __syncthreads();
+  if (path != nullptr && warp == 0) {
+    const int d = block_depth(depths, b, steps, err);
+    int p = 0;
+    for (int l = 0; l < d; ++l) {
+      const float v = lane < K ? sS[(l * K + p) * K + lane] : -INFINITY;
+      const int c = warp_argmax(v, K);
+      if (lane == 0) path[static_cast<size_t>(b) * steps + l] = cand[(static_cast<size_t>(b) * steps + l) * K + c];
+      p = c;
+    }
+    for (int l = d + lane; l < steps; l += 32) path[static_cast<size_t>(b) * steps + l] = -1;
+  }
+}
+
 size_t edges_smem(int steps, int K, int R, int lchunk) {
   return sizeof(float) * (static_cast<size_t>(steps) * K + static_cast<size_t>(steps) * K * K +
                           2 * static_cast<size_t>(lchunk) * K * (R + 1));
@@ -179,9 +343,46 @@ size_t edges_smem(int steps, int K, int R, int lchunk) {
 
 }  // namespace
 
+#ifndef DFL_EDGE_WARP
+#define DFL_EDGE_WARP 1
+#endif
+
 int launch_score_edges(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
                        const void* pred, const void* succ, int B, int steps, int K, int R, int V, int dtype,
                        float* S, int32_t* path, cudaStream_t st, const int32_t* depths) {
+  {
+    // warp-per-slot kernel when its scores and at least a few warps' rows fit in shared memory
+    const size_t s_floats = (static_cast<size_t>(steps) * K * K + 3) & ~static_cast<size_t>(3);
+    const size_t per_warp = 2 * static_cast<size_t>(K) * (R + 4);
+    const size_t budget = kSmemBudget / sizeof(float);
+    const int nw = s_floats + per_warp <= budget
+                       ? static_cast<int>(std::min<size_t>({static_cast<size_t>(kEdgeWarpsMax),
+                                                            static_cast<size_t>(steps), (budget - s_floats) / per_warp}))
+                       : 0;
+    if (DFL_EDGE_WARP && nw >= 4) {
+      const size_t smem = sizeof(float) * (s_floats + nw * per_warp);
+      const int tiled = K == 16 && reinterpret_cast<uintptr_t>(unary) % 16 == 0 &&
+                        reinterpret_cast<uintptr_t>(S) % 16 == 0;  // float4 unary loads and S stores
+      static unsigned dw_f32 = 0, dw_bf16 = 0;
+      cudaError_t e = cudaSuccess;
+      if (dtype == DFLASH2_F32) {
+        if (!ensure_smem_attr(score_edges_warp_kernel<float>, kSmemBudget, &dw_f32)) e = cudaErrorInvalidValue;
+        if (e == cudaSuccess)
+          e = launch_pdl(score_edges_warp_kernel<float>, dim3(B), dim3(32 * nw), smem, st, nullptr, 0, cand, unary, z,
+                         anchors, static_cast<const float*>(pred), static_cast<const float*>(succ), steps, K, R, V, S,
+                         path, depths, tiled, device_error_word());
+      } else {
+        if (!ensure_smem_attr(score_edges_warp_kernel<__nv_bfloat16>, kSmemBudget, &dw_bf16)) e = cudaErrorInvalidValue;
+        if (e == cudaSuccess)
+          e = launch_pdl(score_edges_warp_kernel<__nv_bfloat16>, dim3(B), dim3(32 * nw), smem, st, nullptr, 0, cand,
+                         unary, z, anchors, static_cast<const __nv_bfloat16*>(pred),
+                         static_cast<const __nv_bfloat16*>(succ), steps, K, R, V, S, path, depths, tiled,
+                         device_error_word());
+      }
+      return e == cudaSuccess ? DFLASH2_OK
+                              : fail(DFLASH2_ERR_CUDA, "score_edges launch failed: %s", cudaGetErrorString(e));
+    }
+  }
   int lchunk = steps;
   while (lchunk > 1 && edges_smem(steps, K, R, lchunk) > static_cast<size_t>(kSmemBudget)) --lchunk;
   const size_t smem = edges_smem(steps, K, R, lchunk);
