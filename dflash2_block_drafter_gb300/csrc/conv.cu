@@ -266,8 +266,12 @@ __global__ void __launch_bounds__(kApplyMaxThreads)
 // shared memory and store 16-byte vectors. A CTA's items are all in flight as soon as it starts
 // (ring depth >= items per CTA at the drafter's shape), and the bytes in flight cost no registers.
 constexpr int kStreamSW = 256;        // channels per strip
-constexpr int kStreamConsumers = 8;   // consumer warps
+#ifndef DFL_STREAM_WARPS
+#define DFL_STREAM_WARPS 8
+#endif
+constexpr int kStreamConsumers = DFL_STREAM_WARPS;  // consumer warps (8 measured faster than 16)
 constexpr int kStreamThreads = 32 * (kStreamConsumers + 1);
+constexpr int kSsRows = (32 + kStreamConsumers - 1) / kStreamConsumers;  // rows per warp, G <= 32
 constexpr int kStreamMaxStages = 4;
 
 #ifndef DFL_STREAM
@@ -296,7 +300,7 @@ __device__ __forceinline__ void stream_drain(uint64_t* full, int stage, uint32_t
 // finish's apply pass, streamed: out = residual + side-1 conv of y. Per item the ring stage holds
 // y[b, :, strip] (G x 256), residual[b, :, strip] and coef1[b, :, :, strip groups] (2G x 256/gs).
 template <typename T>
-__global__ void __launch_bounds__(kStreamThreads)
+__global__ void __launch_bounds__(kStreamThreads, 2)
     conv_side1_stream_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmR,
                              const __grid_constant__ CUtensorMap tmC, const float* __restrict__ base, T* out, int G,
                              int H, int gs, int n_items, int strips, int has_res, int n_stages, int stage_bytes,
@@ -434,7 +438,7 @@ __device__ __forceinline__ float round_as<__nv_bfloat16>(float v) {
 // distributed shared memory across a cluster barrier; pass 2 writes n = x * rsqrt(mean + eps) * w
 // for rows next_row0..G-1 (compact when next_row0 = 1: the head's h).
 template <typename T>
-__global__ void __launch_bounds__(kStreamThreads)
+__global__ void __launch_bounds__(kStreamThreads, 2)
     conv_finish_norm_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmR,
                             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmW, T* out, T* next_n, float eps, int G, int H,
@@ -494,7 +498,7 @@ __global__ void __launch_bounds__(kStreamThreads)
     // ---- pass 1: x and the rows' partial sums of squares (lane = 8-channel vector of a strip)
     const int v = lane;
     const int gl = (v * 8) / gs;
-    float ss[4] = {0.f, 0.f, 0.f, 0.f};  // rows warp + 8k (G <= 32)
+    float ss[kSsRows] = {};  // rows warp + k * kStreamConsumers (G <= 32)
     bool ok = true;
     for (int s = 0; s < spc && ok; ++s) {
       if (!mbar_wait_bounded(smem_u32(&full[s]), 0, abort_flag, kWaitLimitNs)) {
@@ -512,7 +516,7 @@ __global__ void __launch_bounds__(kStreamThreads)
       load8(sb + v * 8, b0);              // base[1][0][c..]
       load8(sb + kStreamSW + v * 8, b1);  // base[1][1][c..]
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kSsRows; ++k) {
         const int t = warp + k * kStreamConsumers;
         if (t >= G) break;
         float cur[8], prev[8], res[8];
@@ -543,7 +547,7 @@ __global__ void __launch_bounds__(kStreamThreads)
     // the CTA's partial of each of this warp's rows, to every CTA of the cluster
     cluster_wait();
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kSsRows; ++k) {
       const int t = warp + k * kStreamConsumers;
       if (t >= G) break;
       float q = ss[k];
@@ -584,7 +588,7 @@ __global__ void __launch_bounds__(kStreamThreads)
 // s and (side, tap) st, the G x (256/gs) tile of the fp32 partial sums of D for the strip's groups.
 // The grid is a multiple of `strips`, so each CTA keeps one strip and its base kernel in registers.
 template <typename T>
-__global__ void __launch_bounds__(kStreamThreads)
+__global__ void __launch_bounds__(kStreamThreads, 2)
     conv_side0_stream_kernel(const __grid_constant__ CUtensorMap tmN, const __grid_constant__ CUtensorMap tmP,
                              const float* __restrict__ base, T* out, T* coef1, float* d_full, int G, int H, int gs,
                              int groups, int k_splits, int M, int n_items, int strips, int n_stages, int stage_bytes,
