@@ -114,6 +114,92 @@ def head_bytes(M, V, R, H, K):
     return 2.0 * (V + R) * H + 2.0 * M * H + 4.0 * V + M * (8.0 * K + 4.0 * R)
 
 
+def prepare_call_bytes(rows, H, groups):
+    """A prepare call after the first site: n in, W_kp in, a out, coef1 out (bf16)."""
+    return 2.0 * (rows * H + 4 * groups * H + rows * H + rows * 2 * groups)
+
+
+def finish_call_bytes(rows, H, groups, out_rows):
+    """A finish call with the next RMSNorm: y, residual and coef1 in, x out, out_rows normed rows out."""
+    return 2.0 * (3 * rows * H + rows * 2 * groups + out_rows * H) + 4.0 * 2 * H + 2.0 * H
+
+
+def edges_call_bytes(B, steps, K, R):
+    """score_edges + walk: cand, unary and z in, 2K codebook rows per slot gathered, S and path out."""
+    slots = B * steps
+    return slots * (4.0 * K + 4.0 * K + 4.0 * R + 2 * K * R * 2.0 + 4.0 * K * K + 4.0)
+
+
+def per_call_timing(d, run, wl, x0, ys, anchors, h_in, stream, flush, passes=10):
+    """Each library call of one pass timed with CUDA events on its stream, eagerly (an event between
+    two calls also cuts the dependent-launch overlap, so these times are an upper bound on the
+    in-graph ones). Returns {call: {ms, bytes, GB/s, frac of measured HBM peak[, TFLOP/s]}}."""
+    import torch
+    pk = peaks()
+    times = {}
+
+    def timed(name, fn):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        times.setdefault(name, []).append((s, e))
+
+    B, G, H, gs = wl.B, wl.G, wl.H, wl.gs
+    groups = H // gs if gs else 0
+    rows = B * G
+    for _ in range(passes):
+        flush.zero_()
+        nsites = len(wl.sites)
+        for i, s in enumerate(run.sites):
+            if i == 0:
+                d.dflash2_conv_prepare(x0, s.norm_w, wl.eps, s.w_kp, s.base, gs, out=run.a, coef1=run.coef1,
+                                       workspace=run.conv_ws)
+            else:
+                timed("conv_prepare", lambda s=s: d.dflash2_conv_prepare(
+                    run.n, None, wl.eps, s.w_kp, s.base, gs, out=run.a, coef1=run.coef1, workspace=run.conv_ws))
+            residual = x0 if i == 0 else run.x
+            if i + 1 < nsites:
+                timed("conv_finish", lambda s=s, i=i, residual=residual: d.dflash2_conv_finish(
+                    ys[i], run.coef1, s.base, gs, residual=residual, out=run.x, next_norm_w=run.sites[i + 1].norm_w,
+                    eps=wl.eps, next_n=run.n, next_row0=0))
+            elif run.with_selector:
+                d.dflash2_conv_finish(ys[i], run.coef1, s.base, gs, residual=residual, out=run.x,
+                                      next_norm_w=run.final_norm_w, eps=wl.eps, next_n=run.h, next_row0=1)
+            else:
+                d.dflash2_conv_finish(ys[i], run.coef1, s.base, gs, residual=residual, out=run.x)
+        if run.with_selector:
+            h_src = run.h if wl.sites else h_in
+            M = B * wl.steps
+            timed("head_topk", lambda: d.dflash2_head_topk(
+                h_src.view(M, H), run.w_head, wl.K, bias=run.bias, w_proj=run.w_proj, cand=run.cand,
+                unary=run.unary, z=run.z, workspace=run.head_ws))
+            timed("score_edges", lambda: d.dflash2_score_edges(
+                run.cand.view(B, wl.steps, wl.K), run.unary.view(B, wl.steps, wl.K), run.z.view(B, wl.steps, wl.R),
+                anchors, run.pred, run.succ, S=run.S, path=run.path))
+    torch.cuda.synchronize()
+    out = {}
+    for name, evs in times.items():
+        ms = statistics.mean(s.elapsed_time(e) for s, e in evs)
+        if name == "conv_prepare":
+            byts = prepare_call_bytes(rows, H, groups)
+            extra = {"tflops": 2.0 * rows * 4 * groups * H / (ms / 1e3) / 1e12}
+        elif name == "conv_finish":
+            byts = finish_call_bytes(rows, H, groups, rows)
+            extra = {}
+        elif name == "head_topk":
+            M = B * wl.steps
+            byts = head_bytes(M, wl.V, wl.R, H, wl.K)
+            extra = {"tflops": head_flops(M, wl.V, wl.R, H) / (ms / 1e3) / 1e12}
+        else:
+            byts = edges_call_bytes(B, wl.steps, wl.K, wl.R)
+            extra = {}
+        gbs = byts / (ms / 1e3) / 1e9
+        out[name] = dict({"ms": ms, "bytes": byts, "gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"]}, **extra)
+    return out
+
+
 def conv_site_bytes(B, G, H, groups):
     """Per conv site: kp weights + prepare (n in, a out, coef1 out) + finish (y, x in, x out, next n out, coef1 in)."""
     rows = B * G
@@ -368,6 +454,7 @@ def our_arm(args, wl_name):
         if traffic is not None:
             roofline["traffic"] = traffic
 
+    calls = per_call_timing(d, run, wl, x0, ys, anchors, h_in, stream, flush) if rank == 0 else None
     launches = run.launches_per_pass(conv=bool(wl.sites), selector=run.with_selector,
                                      emit_h=run.with_selector)
     line = {
@@ -385,6 +472,7 @@ def our_arm(args, wl_name):
         "gpu_launches": launches * args.steps,
         "cuda_graph": bool(args.graph),
         "clocks": clocks,
+        "per_call": calls,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = args.cpu_blocks

@@ -858,52 +858,38 @@ __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
   return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
-// One warp per row: merge the per-split sorted lists into the row's top-K (value desc, id asc).
-// `ids_map` (nullable): token id of each column when the head ran over a draft vocabulary.
-__global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict__ lv, const int* __restrict__ li,
-                                                         int n_splits, int M, int K, const int32_t* __restrict__ ids_map,
-                                                         int32_t* __restrict__ cand, float* __restrict__ unary) {
-  pdl_trigger();
-  pdl_wait();
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= M) return;
-  float tv[kTopL];
-  int ti[kTopL];
+// The list of split `s` for `row` (sorted, value desc / id asc) into a lane's registers; empty slots
+// (id -1) become (-inf, INT_MAX) so that they lose every tie.
+__device__ __forceinline__ void load_list(const float* lv, const int* li, int s, int M, int row, float (&tv)[kTopL],
+                                          int (&ti)[kTopL]) {
+  const size_t o = (static_cast<size_t>(s) * M + row) * kTopL;
+#pragma unroll
+  for (int q = 0; q < kTopL / 4; ++q) {  // the whole sorted list in 8 vector loads
+    const float4 f = __ldg(reinterpret_cast<const float4*>(lv + o) + q);
+    const int4 n = __ldg(reinterpret_cast<const int4*>(li + o) + q);
+    const float fv[4] = {f.x, f.y, f.z, f.w};
+    const int nv[4] = {n.x, n.y, n.z, n.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      tv[4 * q + e] = nv[e] >= 0 ? fv[e] : -INFINITY;
+      ti[4 * q + e] = nv[e] >= 0 ? nv[e] : INT_MAX;
+    }
+  }
+}
+
+__device__ __forceinline__ void empty_list(float (&tv)[kTopL], int (&ti)[kTopL]) {
 #pragma unroll
   for (int i = 0; i < kTopL; ++i) {
     tv[i] = -INFINITY;
     ti[i] = INT_MAX;
   }
-  for (int s = lane; s < n_splits; s += 32) {
-    const size_t o = (static_cast<size_t>(s) * M + row) * kTopL;
-    float lvv[kTopL];
-    int liv[kTopL];
-#pragma unroll
-    for (int q = 0; q < kTopL / 4; ++q) {  // the whole sorted list in 8 vector loads
-      const float4 f = __ldg(reinterpret_cast<const float4*>(lv + o) + q);
-      const int4 n = __ldg(reinterpret_cast<const int4*>(li + o) + q);
-      lvv[4 * q] = f.x; lvv[4 * q + 1] = f.y; lvv[4 * q + 2] = f.z; lvv[4 * q + 3] = f.w;
-      liv[4 * q] = n.x; liv[4 * q + 1] = n.y; liv[4 * q + 2] = n.z; liv[4 * q + 3] = n.w;
-    }
-#pragma unroll
-    for (int i = 0; i < kTopL; ++i) {
-      float cv = lvv[i];
-      int ci = liv[i];
-      if (ci < 0 || !better(cv, ci, tv[kTopL - 1], ti[kTopL - 1])) break;  // lists are sorted
-#pragma unroll
-      for (int j = 0; j < kTopL; ++j) {
-        if (better(cv, ci, tv[j], ti[j])) {
-          const float fv = tv[j];
-          const int fi = ti[j];
-          tv[j] = cv;
-          ti[j] = ci;
-          cv = fv;
-          ci = fi;
-        }
-      }
-    }
-  }
+}
+
+// K-way merge of the lanes' sorted lists (one per lane; ids unique across lanes): round k takes the
+// best head over the warp (value desc, id asc) and its owner pops it. Every lane gets the K results
+// in (ov[k], oi[k]) order through `emit(k, value, id)`.
+template <typename Emit>
+__device__ __forceinline__ void warp_merge_lists(float (&tv)[kTopL], int (&ti)[kTopL], int K, Emit emit) {
   for (int k = 0; k < K; ++k) {
     float bv = tv[0];
     int bi = ti[0];
@@ -916,11 +902,8 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict
         bi = oi;
       }
     }
-    if (lane == 0) {
-      cand[static_cast<size_t>(row) * K + k] = ids_map != nullptr ? __ldg(ids_map + bi) : bi;
-      unary[static_cast<size_t>(row) * K + k] = bv;
-    }
-    if (ti[0] == bi) {  // ids are unique across lanes: the owner pops its head
+    emit(k, bv, bi);
+    if (ti[0] == bi) {
 #pragma unroll
       for (int j = 0; j < kTopL - 1; ++j) {
         tv[j] = tv[j + 1];
@@ -930,6 +913,72 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict
       ti[kTopL - 1] = INT_MAX;
     }
   }
+}
+
+// Up to 32 splits: one warp per row, lane s holding split s's list.
+// `ids_map` (nullable): token id of each column when the head ran over a draft vocabulary.
+__global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict__ lv, const int* __restrict__ li,
+                                                         int n_splits, int M, int K, const int32_t* __restrict__ ids_map,
+                                                         int32_t* __restrict__ cand, float* __restrict__ unary) {
+  pdl_trigger();
+  pdl_wait();
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  float tv[kTopL];
+  int ti[kTopL];
+  if (lane < n_splits)
+    load_list(lv, li, lane, M, row, tv, ti);
+  else
+    empty_list(tv, ti);
+  warp_merge_lists(tv, ti, K, [&](int k, float v, int id) {
+    if (lane == 0) {
+      cand[static_cast<size_t>(row) * K + k] = ids_map != nullptr ? __ldg(ids_map + id) : id;
+      unary[static_cast<size_t>(row) * K + k] = v;
+    }
+  });
+}
+
+// 33 to 512 splits: one CTA of W <= 16 warps per row. Warp w merges splits w, w + W, ... (at most 32)
+// into its top-16 in shared memory; warp 0 then merges the W lists into the row's top-K.
+__global__ void __launch_bounds__(512) topk_merge_wide_kernel(const float* __restrict__ lv,
+                                                               const int* __restrict__ li, int n_splits, int M, int K,
+                                                               const int32_t* __restrict__ ids_map,
+                                                               int32_t* __restrict__ cand, float* __restrict__ unary) {
+  __shared__ float sv[32][kTopL];
+  __shared__ int si[32][kTopL];
+  pdl_trigger();
+  pdl_wait();
+  const int row = blockIdx.x;
+  const int W = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  float tv[kTopL];
+  int ti[kTopL];
+  const int s = warp + W * lane;
+  if (s < n_splits)
+    load_list(lv, li, s, M, row, tv, ti);
+  else
+    empty_list(tv, ti);
+  warp_merge_lists(tv, ti, kTopL, [&](int k, float v, int id) {
+    if (lane == 0) {
+      sv[warp][k] = v;
+      si[warp][k] = id;
+    }
+  });
+  __syncthreads();
+  if (warp != 0) return;
+#pragma unroll
+  for (int i = 0; i < kTopL; ++i) {
+    tv[i] = lane < W ? sv[lane][i] : -INFINITY;
+    ti[i] = lane < W ? si[lane][i] : INT_MAX;
+  }
+  warp_merge_lists(tv, ti, K, [&](int k, float v, int id) {
+    if (lane == 0) {
+      cand[static_cast<size_t>(row) * K + k] = ids_map != nullptr ? __ldg(ids_map + id) : id;
+      unary[static_cast<size_t>(row) * K + k] = v;
+    }
+  });
 }
 
 // One thread waits on an mbarrier that nothing completes; the bounded wait gives up.
@@ -1206,10 +1255,19 @@ int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bi
   else
     rc = dispatch_tc<1>(plan.mt, p.dtype == DFLASH2_F32, mA, mB, mE, a, grid, st);
   if (rc != DFLASH2_OK) return rc;
-  const int rows_per_block = 8;
-  const cudaError_t e = launch_pdl(topk_merge_kernel, dim3((p.M + rows_per_block - 1) / rows_per_block),
-                                   dim3(32 * rows_per_block), 0, st, nullptr, 0, static_cast<const float*>(a.list_val),
-                                   static_cast<const int*>(a.list_idx), plan.n_splits, p.M, K, ids_map, cand, unary);
+  cudaError_t e;
+  if (plan.n_splits <= 32) {
+    const int rows_per_block = 8;
+    e = launch_pdl(topk_merge_kernel, dim3((p.M + rows_per_block - 1) / rows_per_block), dim3(32 * rows_per_block), 0,
+                   st, nullptr, 0, static_cast<const float*>(a.list_val), static_cast<const int*>(a.list_idx),
+                   plan.n_splits, p.M, K, ids_map, cand, unary);
+  } else {
+    const int W = (plan.n_splits + 31) / 32;  // warps per row, each merging at most 32 lists
+    if (W > 16) return fail(DFLASH2_ERR_INVALID_ARG, "top-K merge: %d column ranges exceed 512", plan.n_splits);
+    e = launch_pdl(topk_merge_wide_kernel, dim3(p.M), dim3(32 * W), 0, st, nullptr, 0,
+                   static_cast<const float*>(a.list_val), static_cast<const int*>(a.list_idx), plan.n_splits, p.M, K,
+                   ids_map, cand, unary);
+  }
   if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "topk_merge launch failed: %s", cudaGetErrorString(e));
   return DFLASH2_OK;
 }
