@@ -18,7 +18,8 @@ import torch
 
 __all__ = [
     "Dflash2Error", "library", "library_path", "dflash2_version", "dflash2_poll_error",
-    "dflash2_conv_prepare_workspace_bytes", "dflash2_conv_prepare", "dflash2_conv_finish",
+    "dflash2_conv_prepare_workspace_bytes", "dflash2_conv_prepare_launches", "dflash2_conv_finish_launches",
+    "dflash2_conv_prepare", "dflash2_conv_finish",
     "dflash2_head_topk_workspace_bytes", "dflash2_head_topk", "dflash2_score_edges",
     "dflash2_select_path", "dflash2_selftest_bounded_wait", "dflash2_head_topk_noalloc", "dflash2_head_topk_vocab", "dflash2_score_edges_depths", "dflash2_select_path_depths",
     "DTYPE_CODES",
@@ -41,6 +42,8 @@ _SIGNATURES = {
     "dflash2_last_error_message": (ctypes.c_char_p, []),
     "dflash2_poll_error": (_i, [_vp]),
     "dflash2_conv_prepare_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "dflash2_conv_prepare_launches": (_i, [_i, _i, _i, _i, _i, _i]),
+    "dflash2_conv_finish_launches": (_i, [_i, _i, _i, _i, _i, _i]),
     "dflash2_conv_prepare": (_i, [_vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dflash2_conv_finish": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _f, _vp, _i, _vp]),
     "dflash2_head_topk_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
@@ -130,6 +133,16 @@ def dflash2_poll_error(stream=None) -> int:
 
 def dflash2_conv_prepare_workspace_bytes(B, G, H, group_size, dtype) -> int:
     return library().dflash2_conv_prepare_workspace_bytes(B, G, H, group_size, DTYPE_CODES[dtype])
+
+
+def dflash2_conv_prepare_launches(B, G, H, group_size, dtype, with_norm) -> int:
+    """Kernels one dflash2_conv_prepare call launches for this shape (-1: rejected shape)."""
+    return library().dflash2_conv_prepare_launches(B, G, H, group_size, DTYPE_CODES[dtype], int(bool(with_norm)))
+
+
+def dflash2_conv_finish_launches(B, G, H, group_size, dtype, with_next_norm) -> int:
+    """Kernels one dflash2_conv_finish call launches for this shape (-1: rejected shape)."""
+    return library().dflash2_conv_finish_launches(B, G, H, group_size, DTYPE_CODES[dtype], int(bool(with_next_norm)))
 
 
 def dflash2_conv_prepare(x, norm_w, eps, w_kp, base, group_size, out=None, coef1=None, d_full=None, workspace=None,

@@ -117,6 +117,16 @@ size_t dflash2_conv_prepare_workspace_bytes(int B, int G, int H, int group_size,
   return conv_prepare_workspace(s, sm_count());
 }
 
+int dflash2_conv_prepare_launches(int B, int G, int H, int group_size, int dtype, int with_norm) {
+  if (check_conv_shape(B, G, H, group_size, 2, dtype) != DFLASH2_OK) return -1;
+  return conv_prepare_kernels(ConvShape{B, G, H, group_size, H / group_size, dtype}, with_norm != 0);
+}
+
+int dflash2_conv_finish_launches(int B, int G, int H, int group_size, int dtype, int with_next_norm) {
+  if (check_conv_shape(B, G, H, group_size, 2, dtype) != DFLASH2_OK) return -1;
+  return conv_finish_kernels(ConvShape{B, G, H, group_size, H / group_size, dtype}, with_next_norm != 0);
+}
+
 int dflash2_conv_prepare(const void* x, const void* norm_w, float eps, const void* w_kp, const float* base, int B,
                          int G, int H, int group_size, int taps, int dtype, void* out, void* coef1, float* d_full,
                          void* workspace, size_t workspace_bytes, void* stream) {

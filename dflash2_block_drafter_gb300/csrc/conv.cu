@@ -1053,4 +1053,14 @@ int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, cons
   return launch_rmsnorm_rows(out, next_w, eps, next_n, s.B, s.G, next_row0, s.H, s.dtype, st);
 }
 
+int conv_prepare_kernels(const ConvShape& s, bool with_norm) {
+  (void)s;
+  return (with_norm ? 1 : 0) + 2;  // [RMSNorm] + kernel_projection + side-0 pass
+}
+
+int conv_finish_kernels(const ConvShape& s, bool with_next_norm) {
+  if (!with_next_norm) return 1;
+  return (DFL_FINISH_NORM && finish_norm_cluster(s) > 0) ? 1 : 2;
+}
+
 }  // namespace dfl

@@ -83,6 +83,10 @@ size_t conv_prepare_workspace(const ConvShape& s, int sms);
 int launch_rmsnorm(const void* x, const void* w, float eps, void* n, int rows, int H, int dtype, cudaStream_t st);
 int launch_conv_side0(const ConvShape& s, const void* n, const float* part, int k_splits, const float* base,
                       void* out, void* coef1, float* d_full, cudaStream_t st);
+// Kernels one prepare call launches (the optional first RMSNorm, kernel_projection, the side-0
+// pass) and one finish call (the fused finish + next norm, or the side-1 pass and the norm).
+int conv_prepare_kernels(const ConvShape& s, bool with_norm);
+int conv_finish_kernels(const ConvShape& s, bool with_next_norm);
 int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, const float* base, const void* residual,
                       void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st);
 

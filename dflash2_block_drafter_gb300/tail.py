@@ -19,7 +19,8 @@ from typing import List, Optional
 import numpy as np
 import torch
 
-from . import (dflash2_conv_finish, dflash2_conv_prepare, dflash2_conv_prepare_workspace_bytes, dflash2_head_topk,
+from . import (dflash2_conv_finish, dflash2_conv_finish_launches, dflash2_conv_prepare,
+               dflash2_conv_prepare_launches, dflash2_conv_prepare_workspace_bytes, dflash2_head_topk,
                dflash2_head_topk_workspace_bytes, dflash2_score_edges)
 
 
@@ -110,13 +111,17 @@ class TailRunner:
         return self.x
 
     def launches_per_pass(self, conv: bool = True, selector: bool = True, emit_h: bool = True) -> int:
-        """Library kernels one pass launches: the first site's RMSNorm; per site a kernel_projection
-        GEMM, a side-0 pass, a side-1 pass and the next RMSNorm (not after the last site of a chain
-        that emits no h); then the head GEMM + top-K merge and the fused edge-score/walk kernel."""
+        """Library kernels one pass launches, as the library reports them per call: per site a
+        prepare (the first with its RMSNorm) and a finish (with the next site's norm, or the final
+        norm when h is emitted); then the head GEMM + top-K merge and the edge-score/walk kernel."""
+        wl = self.wl
         n = 0
         ns = len(self.sites)
         if conv and ns:
-            n += 1 + 3 * ns + (ns if emit_h else ns - 1)
+            shape = (wl.B, wl.G, wl.H, wl.gs, self.dtype)
+            n += dflash2_conv_prepare_launches(*shape, True) + (ns - 1) * dflash2_conv_prepare_launches(*shape, False)
+            for i in range(ns):
+                n += dflash2_conv_finish_launches(*shape, i + 1 < ns or emit_h)
         if selector and self.with_selector:
             n += 3
         return n

@@ -111,6 +111,12 @@ DFLASH2_API int dflash2_poll_error(void* stream);
  *                             of device memory, 256-byte aligned; contents are scratch.
  * ---------------------------------------------------------------------------------- */
 DFLASH2_API size_t dflash2_conv_prepare_workspace_bytes(int B, int G, int H, int group_size, int dtype);
+/* Number of kernels one dflash2_conv_prepare call launches for this shape (with_norm: norm_w
+ * given) and one dflash2_conv_finish call (with_next_norm: next_norm_w given): with the next
+ * norm, finish is a single fused kernel where its tiles fit, else a side-1 pass and a norm pass.
+ * -1 for a shape the calls reject. Host-only; launches nothing. */
+DFLASH2_API int dflash2_conv_prepare_launches(int B, int G, int H, int group_size, int dtype, int with_norm);
+DFLASH2_API int dflash2_conv_finish_launches(int B, int G, int H, int group_size, int dtype, int with_next_norm);
 DFLASH2_API int dflash2_conv_prepare(const void* x, const void* norm_w, float eps, const void* w_kp, const float* base,
                          int B, int G, int H, int group_size, int taps, int dtype, void* out, void* coef1,
                          float* d_full, void* workspace, size_t workspace_bytes, void* stream);

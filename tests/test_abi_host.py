@@ -151,3 +151,19 @@ def test_mixed_depth_walk_rejects_bad_arguments(lib):
     g = lib.dflash2_select_path_depths
     assert g(FAKE, FAKE, None, 1, 15, 16, FAKE, None) == -1
     assert g(FAKE, FAKE, FAKE, 1, 15, 33, FAKE, None) == -1
+
+
+def test_launch_count_queries(lib):
+    bf16, f32 = 0, 1
+    # drafter shape: prepare = kernel_projection + side-0 pass (+ the first site's norm)
+    assert lib.dflash2_conv_prepare_launches(64, 16, 5120, 16, bf16, 0) == 2
+    assert lib.dflash2_conv_prepare_launches(64, 16, 5120, 16, bf16, 1) == 3
+    # finish with the next norm is one fused kernel where its tiles fit
+    assert lib.dflash2_conv_finish_launches(64, 16, 5120, 16, bf16, 1) == 1
+    assert lib.dflash2_conv_finish_launches(64, 16, 5120, 16, bf16, 0) == 1
+    # H not a multiple of 256 channels: a side-1 pass and a separate norm
+    assert lib.dflash2_conv_finish_launches(5, 7, 320, 16, bf16, 1) == 2
+    # G above 32 rows per block: not fused either
+    assert lib.dflash2_conv_finish_launches(5, 64, 256, 16, f32, 1) == 2
+    assert lib.dflash2_conv_prepare_launches(1, 16, 5000, 16, bf16, 0) == -1  # H % 64: rejected
+    assert lib.dflash2_conv_finish_launches(1, 65, 5120, 16, bf16, 1) == -1   # G > 64: rejected
