@@ -492,10 +492,10 @@ def our_arm(args, wl_name):
 TRAFFIC_PER_LAUNCH = {
     # dram__bytes_read.sum + dram__bytes_write.sum of tc_pair_kernel<bf16, TOPK> (960 rows),
     # profiles/head_topk_selector-B64.md; the full tail runs the same head launch
-    "full-tail-B64": 2.623501e9 + 3.369728e6,
-    "selector-B64": 2.623501e9 + 3.369728e6,
+    "full-tail-B64": 3.396895e9 + 3.463168e6,
+    "selector-B64": 3.396895e9 + 3.463168e6,
     # tc_gemm_kernel<1, bf16, TOPK> (15 rows), profiles/head_topk_selector-B1.md
-    "selector-B1": 2.543751e9 + 2.905344e6,
+    "selector-B1": 2.543758e9 + 3.118080e6,
 }
 
 

@@ -324,15 +324,23 @@ __global__ void __launch_bounds__(32 * kEdgeWarpsMax)
   }
   __syncthreads();
   if (path != nullptr && warp == 0) {
+    // The walk touches only shared memory: lane l keeps the position chosen at slot l (lane l - 32
+    // for slots 32..63), and the candidate ids are looked up afterwards in one parallel round.
     const int d = block_depth(depths, b, steps, err);
-    int p = 0;
+    int p = 0, pos_lo = 0, pos_hi = 0;
     for (int l = 0; l < d; ++l) {
       const float v = lane < K ? sS[(l * K + p) * K + lane] : -INFINITY;
       const int c = warp_argmax(v, K);
-      if (lane == 0) path[static_cast<size_t>(b) * steps + l] = cand[(static_cast<size_t>(b) * steps + l) * K + c];
+      if (lane == l) pos_lo = c;
+      if (lane + 32 == l) pos_hi = c;
       p = c;
     }
-    for (int l = d + lane; l < steps; l += 32) path[static_cast<size_t>(b) * steps + l] = -1;
+    const size_t base_slot = static_cast<size_t>(b) * steps;
+    for (int h = 0; h < 2; ++h) {
+      const int l = lane + 32 * h;
+      if (l >= steps) break;
+      path[base_slot + l] = l < d ? cand[(base_slot + l) * K + (h == 0 ? pos_lo : pos_hi)] : -1;
+    }
   }
 }
 
