@@ -399,12 +399,18 @@ def our_arm(args, wl_name):
               ([h_h] if h_h is not None else []) + ([h_anchors] if h_anchors is not None else []))
     d2h = h_out.numel() * h_out.element_size()
     e2e_ms = []
+    # the full tail with host inputs as one CUDA graph: the copies are graph nodes on a branch of
+    # their own, each site's finish waiting only for its own sublayer output
+    e2e_graph = run.capture(run.full_from_host, h_x0, h_ys, h_anchors, x0, ys, anchors) \
+        if (full_tail and args.graph) else None
     for i in range(args.warmup + args.steps):
         flush.zero_()
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record(stream)
-        if full_tail:
+        if e2e_graph is not None:
+            e2e_graph.replay()
+        elif full_tail:
             # inputs copied on a copy stream; each site waits only for its own sublayer output
             run.full_from_host(h_x0, h_ys, h_anchors, x0, ys, anchors)
         else:

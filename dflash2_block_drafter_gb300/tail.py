@@ -147,8 +147,11 @@ class TailRunner:
         """The whole block tail with its inputs in pinned host memory. Every input is copied into
         the given device buffers on a copy stream, one event per input; the compute stream waits
         for x0 before the first site, for y_i only before site i's finish and for the anchors
-        before the selector, so the copies of later sites' inputs overlap the earlier sites and
-        the first ones overlap nothing but each other. Returns path [B, steps] int32 (device)."""
+        before the selector, so the copies of later sites' inputs overlap the earlier sites. (Two
+        or four copy streams were measured slower: concurrent host-to-device copies contend.) The
+        pass can be captured with ``capture``: the copies become graph nodes on a forked branch
+        whose events join it where each input is needed, and the host buffers are read at replay
+        time (refresh them in place). Returns path [B, steps] int32 (device)."""
         comp = torch.cuda.current_stream()
         if getattr(self, "_copy_stream", None) is None:
             self._copy_stream = torch.cuda.Stream(device=comp.device)
@@ -169,8 +172,9 @@ class TailRunner:
         self.conv_chain(x0, ys, emit_h=True, before_finish=lambda i: comp.wait_event(self._ev_y[i]))
         comp.wait_event(self._ev_anchors)
         path = self.selector(self.h, anchors, want_S=want_S)
-        for t in [x0, anchors] + list(ys):  # the copy stream wrote them: keep the allocator honest
-            t.record_stream(cs)
+        if not torch.cuda.is_current_stream_capturing():
+            for t in [x0, anchors] + list(ys):  # the copy stream wrote them: keep the allocator honest
+                t.record_stream(cs)
         return path
 
     def capture(self, fn, *args, **kwargs) -> "torch.cuda.CUDAGraph":

@@ -113,3 +113,30 @@ def test_full_from_host_matches_device_inputs(torch):
         assert torch.equal(run.path, want[0])
         assert torch.equal(run.S, want[1])
         assert torch.equal(run.h, want[2])
+
+
+def test_full_from_host_graph_replay(torch):
+    """The host-input pass captured into one CUDA graph (copies as graph nodes on their own
+    branch) gives the eager pass's results exactly, and reads the host buffers at replay time."""
+    from dflash2_block_drafter_gb300.tail import TailRunner, to_device, to_pinned
+    import dflash2_block_drafter_gb300 as d
+    wl = I.make_config(0, B=4)
+    run = TailRunner(wl)
+    run.full(to_device(wl.x0), [to_device(s.y) for s in wl.sites], to_device(wl.anchors))
+    want = (run.path.clone(), run.S.clone(), run.h.clone())
+    x0 = torch.empty_like(run.x)
+    ys = [torch.empty_like(run.x) for _ in wl.sites]
+    anchors = torch.empty(wl.B, dtype=torch.int32, device="cuda")
+    h_x0, h_ys, h_anchors = to_pinned(wl.x0), [to_pinned(s.y) for s in wl.sites], to_pinned(wl.anchors)
+    real_y0 = h_ys[0].clone()
+    h_ys[0].zero_()  # the capture pass sees other inputs than the replay
+    graph = run.capture(run.full_from_host, h_x0, h_ys, h_anchors, x0, ys, anchors)
+    h_ys[0].copy_(real_y0)
+    run.path.zero_()
+    run.S.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert d.dflash2_poll_error() == 0
+    assert torch.equal(run.path, want[0])
+    assert torch.equal(run.S, want[1])
+    assert torch.equal(run.h, want[2])
