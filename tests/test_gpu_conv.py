@@ -29,7 +29,11 @@ def _site_dev(torch, s):
     (1, 8, 256, 16), (3, 16, 512, 16), (5, 7, 320, 16), (2, 16, 1024, 32),
     # above 128 rows kernel_projection runs on CTA pairs: a ragged second row group (144 rows),
     # G = 64 (320 rows), and 260 rows with 48 groups (N = 192: half a column unit past the end)
-    (9, 16, 512, 16), (5, 64, 256, 16), (20, 13, 384, 8)])
+    (9, 16, 512, 16), (5, 64, 256, 16), (20, 13, 384, 8),
+    # the streamed / fused passes at their limits: G = 2 (smallest), G = 32 (largest fused
+    # finish), G = 33 (falls back to the side-1 pass and a separate norm), group 64 (the
+    # coefficient tiles are too narrow for TMA: per-thread passes)
+    (4, 2, 512, 16), (3, 32, 512, 16), (2, 33, 512, 16), (2, 16, 512, 64)])
 def test_prepare_finish_parity(torch, dtype, B, G, H, gs):
     import dflash2_block_drafter_gb300 as d
     wl = I.conv_case(100 + B * G + H, B, G, H, gs, dtype=dtype)

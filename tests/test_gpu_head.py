@@ -50,6 +50,8 @@ def test_head_topk_parity(torch, dtype, B, G, H, V, R, bias):
     (257, 1000, 192),   # one row past a 256-row group; fewer column units than CTA pairs; 1.5 units of z
     (513, 9000, 16),    # ragged third group; z narrower than a chunk
     (1024, 2500, 64),   # four full groups; units not a multiple of the column ranges
+    (128, 4096, 64),    # the largest single-CTA head
+    (256, 4096, 64),    # exactly one CTA-pair row group
 ])
 def test_head_topk_row_and_column_edges(torch, dtype, M, V, R):
     """Row counts just past the 128- and 256-row boundaries of the head's tiles (some CTAs hold a

@@ -29,7 +29,9 @@ def _case(seed, B, steps, K, R, V, dtype="bf16", book_std=0.5):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("B,steps,K,R,V", [(1, 15, 16, 64, 5000), (33, 15, 16, 64, 248320), (7, 7, 16, 16, 4096),
-                                           (5, 4, 3, 8, 50), (3, 31, 32, 128, 1000)])
+                                           (5, 4, 3, 8, 50), (3, 31, 32, 128, 1000),
+                                           (4, 15, 16, 128, 3000),   # K = 16 tiles with R = 128
+                                           (200, 15, 16, 64, 9000)])  # more blocks than SMs
 def test_score_edges_and_walk(torch, dtype, B, steps, K, R, V):
     import dflash2_block_drafter_gb300 as d
     from dflash2_block_drafter_gb300.tail import to_device
@@ -85,3 +87,22 @@ def test_bad_index_sets_error_word(torch):
                           to_device(succ))
     assert d.dflash2_poll_error() == -6
     assert d.dflash2_poll_error() == 0   # cleared
+
+
+def test_misaligned_unary_and_S_take_the_scalar_path(torch):
+    """unary and S 4 bytes off a 16-byte boundary: the edge-score kernel must not use its float4
+    tiles there, and gives the same scores and walk as with aligned buffers."""
+    import dflash2_block_drafter_gb300 as d
+    from dflash2_block_drafter_gb300.tail import to_device
+    cand, unary, z, anchors, pred, succ = _case(31, 6, 15, 16, 64, 4000)
+    args = [to_device(cand), None, to_device(z), to_device(anchors), to_device(pred), to_device(succ)]
+    S0, p0 = d.dflash2_score_edges(args[0], to_device(unary), *args[2:])
+    flat_u = torch.empty(unary.size + 1, dtype=torch.float32, device="cuda")
+    u_off = flat_u[1:].view(unary.shape)
+    u_off.copy_(to_device(unary))
+    flat_s = torch.empty(S0.numel() + 1, dtype=torch.float32, device="cuda")
+    s_off = flat_s[1:].view(S0.shape)
+    S1, p1 = d.dflash2_score_edges(args[0], u_off, *args[2:], S=s_off)
+    assert d.dflash2_poll_error() == 0
+    assert torch.equal(S1, S0)
+    assert torch.equal(p1, p0)
