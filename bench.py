@@ -200,6 +200,91 @@ def per_call_timing(d, run, wl, x0, ys, anchors, h_in, stream, flush, passes=10)
     return out
 
 
+def bandwidth_sweep(kind, iters=10):
+    """Achieved bandwidth of one library call as the batch grows: the edge scores + walk at
+    B = 64 .. 4096 blocks (uniform random candidates over the full vocabulary, so the gathered
+    codebook rows come from HBM after the L2 flush), or a prepare / finish pair of the conv at
+    B = 64 .. 512. Seeded synthetic device inputs; every timed call follows a 256 MB L2 flush;
+    CUDA events on the stream around the call, median over `iters`."""
+    import torch
+    import dflash2_block_drafter_gb300 as d
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20261202)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    pk = peaks()
+
+    def time_call(fn):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        ts = []
+        for _ in range(iters):
+            flush.zero_()
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            e.synchronize()
+            ts.append(s.elapsed_time(e))
+        assert d.dflash2_poll_error() == 0
+        return statistics.median(ts)
+
+    points = []
+    if kind == "edges":
+        V, steps, K, R = 248320, 15, 16, 64
+        pred = (0.3 * torch.randn(V, R, generator=gen, device=dev)).to(torch.bfloat16)
+        succ = (0.3 * torch.randn(V, R, generator=gen, device=dev)).to(torch.bfloat16)
+        for B in (64, 256, 1024, 4096):
+            cand = torch.randint(0, V, (B, steps, K), generator=gen, device=dev, dtype=torch.int32)
+            unary = torch.sort(torch.randn(B, steps, K, generator=gen, device=dev), dim=-1, descending=True).values
+            z = torch.randn(B, steps, R, generator=gen, device=dev)
+            anchors = torch.randint(0, V, (B,), generator=gen, device=dev, dtype=torch.int32)
+            S = torch.empty(B, steps, K, K, device=dev)
+            path = torch.empty(B, steps, dtype=torch.int32, device=dev)
+            ms = time_call(lambda: d.dflash2_score_edges(cand, unary, z, anchors, pred, succ, S=S, path=path))
+            byts = edges_call_bytes(B, steps, K, R)
+            gbs = byts / (ms / 1e3) / 1e9
+            points.append({"B": B, "ms": ms, "bytes": byts, "gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"]})
+    else:
+        G, H, gs = 16, 5120, 16
+        groups = H // gs
+        w_kp = (torch.randn(4 * groups, H, generator=gen, device=dev) / H ** 0.5).to(torch.bfloat16)
+        base = torch.zeros(2, 2, H, device=dev)
+        base[:, 0] = 1.0
+        base += 0.1 * torch.randn(2, 2, H, generator=gen, device=dev)
+        norm_w = torch.ones(H, dtype=torch.bfloat16, device=dev)
+        for B in (64, 128, 256, 512):
+            rows = B * G
+            n = torch.randn(B, G, H, generator=gen, device=dev).to(torch.bfloat16)
+            x = torch.randn(B, G, H, generator=gen, device=dev).to(torch.bfloat16)
+            y = torch.randn(B, G, H, generator=gen, device=dev).to(torch.bfloat16)
+            a = torch.empty_like(n)
+            nxt = torch.empty_like(n)
+            coef1 = torch.empty(B, G, 2, groups, dtype=torch.bfloat16, device=dev)
+            ws = torch.empty(d.dflash2_conv_prepare_workspace_bytes(B, G, H, gs, torch.bfloat16), dtype=torch.uint8,
+                             device=dev)
+            d.dflash2_conv_prepare(n, None, 1e-6, w_kp, base, gs, out=a, coef1=coef1, workspace=ws)
+            ms_p = time_call(lambda: d.dflash2_conv_prepare(n, None, 1e-6, w_kp, base, gs, out=a, coef1=coef1,
+                                                            workspace=ws))
+            ms_f = time_call(lambda: d.dflash2_conv_finish(y, coef1, base, gs, residual=x, out=x, next_norm_w=norm_w,
+                                                           eps=1e-6, next_n=nxt, next_row0=0))
+            bp = prepare_call_bytes(rows, H, groups)
+            bf = finish_call_bytes(rows, H, groups, rows)
+            points.append({"B": B, "prepare_ms": ms_p, "prepare_gbs": bp / (ms_p / 1e3) / 1e9,
+                           "prepare_frac_hbm": bp / (ms_p / 1e3) / 1e9 / pk["hbm_gbs"],
+                           "prepare_tflops": 2.0 * rows * 4 * groups * H / (ms_p / 1e3) / 1e12,
+                           "finish_ms": ms_f, "finish_gbs": bf / (ms_f / 1e3) / 1e9,
+                           "finish_frac_hbm": bf / (ms_f / 1e3) / 1e9 / pk["hbm_gbs"]})
+    print(json.dumps({"sweep": kind, "peak_hbm_gbs": pk["hbm_gbs"], "peak_source": pk["source"],
+                      "timing": "median of CUDA-event times of single calls, 256 MB L2 flush before each",
+                      "points": points}), flush=True)
+    return 0
+
+
 def conv_site_bytes(B, G, H, groups):
     """Per conv site: kp weights + prepare (n in, a out, coef1 out) + finish (y, x in, x out, next n out, coef1 in)."""
     rows = B * G
@@ -518,7 +603,13 @@ def main():
     ap.add_argument("--graph", dest="graph", action="store_true", default=True,
                     help="replay each part of a timed step as a CUDA graph (default)")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
+    ap.add_argument("--sweep", choices=["edges", "conv"], default=None,
+                    help="instead of the step benchmark: one call's bandwidth as the batch grows")
     args = ap.parse_args()
+    if args.sweep is not None:
+        import __graft_entry__
+        __graft_entry__.build()
+        return bandwidth_sweep(args.sweep)
     if args.impl == "reference":
         return reference_arm(args, args.workload)
     return our_arm(args, args.workload)

@@ -231,23 +231,31 @@ __global__ void __launch_bounds__(32 * kEdgeWarpsMax)
 #pragma unroll
     for (int e = 0; e < E; ++e) zf[e] = fixed_sg ? __ldg(zl + (lane % segs) * E + e) : 0.f;
     for (int q0 = 0; q0 < items; q0 += 32 * 8) {
-      uint4 buf[8];
+      // Branch-free in two rounds: every candidate id of this lane's 8 items first, then every row
+      // segment (an invalid id or an item past the end reads row 0 and is zeroed afterwards), so
+      // the compiler can keep all 8 loads of each round in flight at once.
+      int ids[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int q = q0 + i * 32 + lane;
-        buf[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (q < items) {
-          const int row = q / segs;
-          const int sg = q - row * segs;
-          const bool is_pred = row < K;
-          const int id = is_pred ? (l == 0 ? anchor : cand[(slot - 1) * K + row]) : cand[slot * K + row - K];
-          if (id >= 0 && id < V) {
-            buf[i] = ldg16((is_pred ? pred : succ) + static_cast<size_t>(id) * R + sg * E);
-          } else if (err != nullptr) {
-            atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_BAD_INDEX));
-          }
-        }
+        const int q = min(q0 + i * 32 + lane, items - 1);
+        const int row = q / segs;
+        const bool from_anchor = row < K && l == 0;  // slot 0's predecessor is the anchor
+        const size_t src = from_anchor ? 0 : (row < K ? (slot - 1) * K + row : slot * K + row - K);
+        ids[i] = from_anchor ? anchor : __ldg(cand + src);
       }
+      uint4 buf[8];
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = min(q0 + i * 32 + lane, items - 1);
+        const int row = q / segs;
+        const int sg = q - row * segs;
+        const bool ok = ids[i] >= 0 && ids[i] < V;
+        bad |= !ok && (q0 + i * 32 + lane < items);
+        buf[i] = ldg16((row < K ? pred : succ) + static_cast<size_t>(ok ? ids[i] : 0) * R + sg * E);
+        if (!ok) buf[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (bad && err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_BAD_INDEX));
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int q = q0 + i * 32 + lane;
