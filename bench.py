@@ -35,6 +35,7 @@ WORKLOADS = {
     "selector-B32": (3, 32),
     "selector-B64": (3, 64),
     "conv-chain-B64": (1, 64),
+    "conv-chain-B8": (1, 8),
     "conv-chain-B1": (1, 1),
 }
 METRIC = "draft blocks/sec (G=16, hidden 5120) at 1 GB300; % of HBM roofline per kernel"
