@@ -854,8 +854,14 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------ top-K merge
-__device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
-  return v1 > v2 || (v1 == v2 && i1 < i2);
+// Order-preserving unsigned key of a float, -0.0 counted as +0.0 so that equal values tie (and
+// fall to the lower id); key_float inverts it.
+__device__ __forceinline__ uint32_t float_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 // The list of split `s` for `row` (sorted, value desc / id asc) into a lane's registers; empty slots
@@ -886,24 +892,18 @@ __device__ __forceinline__ void empty_list(float (&tv)[kTopL], int (&ti)[kTopL])
 }
 
 // K-way merge of the lanes' sorted lists (one per lane; ids unique across lanes): round k takes the
-// best head over the warp (value desc, id asc) and its owner pops it. Every lane gets the K results
-// in (ov[k], oi[k]) order through `emit(k, value, id)`.
+// best head over the warp (value desc, id asc) with two warp reductions and its owner pops it.
+// Every lane sees the K results in order through `emit(k, value, id)`.
 template <typename Emit>
 __device__ __forceinline__ void warp_merge_lists(float (&tv)[kTopL], int (&ti)[kTopL], int K, Emit emit) {
   for (int k = 0; k < K; ++k) {
-    float bv = tv[0];
-    int bi = ti[0];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    emit(k, bv, bi);
-    if (ti[0] == bi) {
+    // best head: the warp's largest value key, then the smallest id among the lanes holding it
+    const uint32_t key = float_key(tv[0]);
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    const int bi = static_cast<int>(
+        __reduce_min_sync(0xffffffffu, key == kmax ? static_cast<uint32_t>(ti[0]) : 0xffffffffu));
+    emit(k, key_float(kmax), bi);
+    if (key == kmax && ti[0] == bi) {
 #pragma unroll
       for (int j = 0; j < kTopL - 1; ++j) {
         tv[j] = tv[j + 1];
