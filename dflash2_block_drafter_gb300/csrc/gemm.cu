@@ -23,6 +23,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "warp_keys.cuh"
 
 namespace dfl {
 namespace {
@@ -854,15 +855,7 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------ top-K merge
-// Order-preserving unsigned key of a float, -0.0 counted as +0.0 so that equal values tie (and
-// fall to the lower id); key_float inverts it.
-__device__ __forceinline__ uint32_t float_key(float v) {
-  const uint32_t u = __float_as_uint(v + 0.0f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_float(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
+
 
 // The list of split `s` for `row` (sorted, value desc / id asc) into a lane's registers; empty slots
 // (id -1) become (-inf, INT_MAX) so that they lose every tie.
@@ -899,9 +892,9 @@ __device__ __forceinline__ void warp_merge_lists(float (&tv)[kTopL], int (&ti)[k
   for (int k = 0; k < K; ++k) {
     // best head: the warp's largest value key, then the smallest id among the lanes holding it
     const uint32_t key = float_key(tv[0]);
-    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-    const int bi = static_cast<int>(
-        __reduce_min_sync(0xffffffffu, key == kmax ? static_cast<uint32_t>(ti[0]) : 0xffffffffu));
+    uint32_t kmax, imin;
+    warp_max_min_index(key, true, static_cast<uint32_t>(ti[0]), kmax, imin);
+    const int bi = static_cast<int>(imin);
     emit(k, key_float(kmax), bi);
     if (key == kmax && ti[0] == bi) {
 #pragma unroll

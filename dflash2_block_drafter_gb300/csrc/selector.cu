@@ -15,6 +15,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "warp_keys.cuh"
 
 namespace dfl {
 namespace {
@@ -39,21 +40,13 @@ __device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
-// Warp argmax over lanes [0, K) (value desc, position asc); every lane gets the winner.
+// Warp argmax over lanes [0, K) (value desc, position asc); every lane gets the winner. Two warp
+// reductions: the largest value key, then the lowest lane holding it.
 __device__ __forceinline__ int warp_argmax(float v, int K) {
   const int lane = threadIdx.x & 31;
-  float bv = lane < K ? v : -INFINITY;
-  int bi = lane < K ? lane : 0x7fffffff;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-    if (ov > bv || (ov == bv && oi < bi)) {
-      bv = ov;
-      bi = oi;
-    }
-  }
-  return bi;
+  uint32_t kmax, imin;
+  warp_max_min_index(float_key(v), lane < K, static_cast<uint32_t>(lane), kmax, imin);
+  return static_cast<int>(imin);
 }
 
 // Draft length of block b: depths[b] slots (the rest of the block's rows are padding of a
