@@ -531,15 +531,19 @@ struct PairCfg {
   static constexpr int kTmemCols = 512;
   static constexpr int kBarBytes = 256;
   static constexpr int kBiasBytes = (MODE == 1 && DFL_PAIR_SMEM_BIAS) ? kEpiWarps * 256 * 4 : 0;
-  // STORE: two 32x32 fp32 staging tiles (128-byte swizzled rows) per epilogue warp
+  // STORE: 32x32 fp32 staging tiles (128-byte swizzled rows), eight per epilogue warp (one per
+  // 32-column chunk of a two-unit tile), carved out of the stage ring once the accumulator is ready
   static constexpr int kOutTile = 32 * 32 * 4;
-  static constexpr int kOutBytes = MODE == 0 ? kEpiWarps * 2 * kOutTile : 0;
-  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes - kBiasBytes - kOutBytes) / kStageBytes;
+  static constexpr int kOutPerWarp = 8;
+  static constexpr int kFit = (kSmemLimit - 1024 - kBarBytes - kBiasBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kBiasBytes + kOutBytes;
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes + kBiasBytes;
 };
 static_assert(PairCfg<1>::kStages >= 2 && PairCfg<1>::kSmem <= kSmemLimit, "shared memory budget (pair, head)");
 static_assert(PairCfg<0>::kStageBytes % 1024 == 0 && PairCfg<0>::kOutTile % 1024 == 0, "staging tile alignment");
+static_assert(PairCfg<0>::kEpiWarps * PairCfg<0>::kOutPerWarp * PairCfg<0>::kOutTile <=
+                  PairCfg<0>::kStages * PairCfg<0>::kStageBytes,
+              "STORE staging tiles fit in the stage ring");
 static_assert(PairCfg<0>::kStages >= 2 && PairCfg<0>::kSmem <= kSmemLimit, "shared memory budget (pair, store)");
 static_assert((2 * PairCfg<1>::kStages + 2 * PairCfg<1>::kAccBufs + 1) * 8 + 8 <= PairCfg<1>::kBarBytes, "barriers");
 static_assert((2 * PairCfg<0>::kStages + 2 * PairCfg<0>::kAccBufs + 1) * 8 + 8 <= PairCfg<0>::kBarBytes, "barriers");
@@ -569,9 +573,10 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  // layout: stages | STORE staging tiles (1024-aligned, as the 128-byte swizzle needs) | barriers | bias
-  uint8_t* sout_all = smem + C::kStages * C::kStageBytes;
-  uint8_t* bar_area = sout_all + C::kOutBytes;
+  // layout: stages | barriers | bias. STORE stages its output tiles in the stage ring: a STORE pair
+  // computes exactly one tile (the launcher checks), so once that accumulator is complete every
+  // stage has been consumed by the MMAs and no further load is issued.
+  uint8_t* bar_area = smem + C::kStages * C::kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(bar_area);
   uint64_t* empty = full + C::kStages;
   uint64_t* acc_full = empty + C::kStages;
@@ -767,8 +772,7 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
       ti[i] = -1;
     }
     float* sbias = sbias_all + e * 256;
-    uint8_t* sout = sout_all + e * 2 * C::kOutTile;  // STORE: this warp's two staging tiles
-    int n_out = 0;                                  // STORE: tiles handed to TMA so far
+    uint8_t* sout = smem + e * C::kOutPerWarp * C::kOutTile;  // STORE: this warp's staging tiles
     int tile_i = 0;
     int u = u_begin, u0 = 0, nu = 0;
     while (next_unit_tile(u, u_end, a.main_units, u0, nu)) {
@@ -795,17 +799,12 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
           // This warp's 32 rows x 32 columns of the partial sum: into a staging tile laid out as
           // the tensor map's 128-byte swizzle expects (16-byte unit j of row i at unit j ^ (i % 8),
           // so the eight lanes of a store phase hit eight different units), then one TMA store.
-          // Boxes that start past the last row or column are not stored (warp-uniform test), and
-          // every stored box is one bulk group, so "at most one group still reading" below means
-          // the store that last used this staging tile is done with it.
+          // Boxes that start past the last row or column are not stored (warp-uniform test). Each
+          // chunk has a staging tile of its own, so no store waits for an earlier one.
           const int col0 = u0 * 128 + cc * 32;
           const int row0 = rowA + q * 32;
           if (row0 < a.M && col0 < a.n_main) {
-            uint8_t* tile = sout + (n_out & 1) * C::kOutTile;
-            if (n_out >= 2) {
-              if (lane == 0) bulk_wait_group_read<1>();
-              __syncwarp();
-            }
+            uint8_t* tile = sout + cc * C::kOutTile;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               *reinterpret_cast<float4*>(tile + lane * 128 + ((j ^ (lane & 7)) << 4)) =
@@ -817,7 +816,6 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
               tma_store_3d(&tmD, smem_u32(tile), col0, row0, ks);
               bulk_commit_group();
             }
-            ++n_out;
           }
         } else if (extra) {
           store_z32(r, (u0 - a.main_units) * 128 + cc * 32, a, valid, row);
@@ -1220,6 +1218,10 @@ int launch_gemm_store(const GemmProblem& p, const GemmPlan& plan, float* part, c
   const int grid = plan.m_groups * plan.n_splits * plan.k_splits;
   if (plan.pair) {
     if (p.n_main % 4 != 0) return fail(DFLASH2_ERR_INVALID_ARG, "pair GEMM store needs N %% 4 == 0 (N=%d)", p.n_main);
+    // one tile (at most two 128-column units) per pair: its output is staged in the stage ring
+    if ((a.n_units + plan.n_splits - 1) / plan.n_splits > 2)
+      return fail(DFLASH2_ERR_INVALID_ARG, "pair GEMM store: %d column units over %d splits is more than one tile",
+                  a.n_units, plan.n_splits);
     CUtensorMap mD;
     if (!make_part_map(&mD, part, plan.k_splits, p.M, p.n_main))
       return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (partials)");
