@@ -276,13 +276,35 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_trigger();
-  pdl_wait();  // no global memory is touched above this line
+  // The weight tiles of the first stages are requested before the wait on the preceding kernel
+  // (weights are never an output of the kernels this one overlaps); the activations follow.
+  int w_pre = 0;
+  const uint64_t pol_keep = policy_evict_last();    // activations: re-read by every column tile
+  const uint64_t pol_stream = policy_evict_first(); // weights: streamed
+  if (warp == 0 && lane == 0) {
+    int c = c_begin, t0 = 0, nch = 0;
+    if (next_tile(c, c_end, a.main_chunks, t0, nch)) {
+      w_pre = min(C::kStages, kb1 - kb0);
+      for (int i = 0; i < w_pre; ++i) {
+        const uint32_t fb = smem_u32(&full[i]);
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(mt_valid * kATile + nch * kBChunkBytes));
+        uint8_t* sb = smem + i * C::kStageBytes + MT * kATile;
+        const int kx = (kb0 + i) * (kRowBytes / (TF32 ? 4 : 2));
+        for (int j = 0; j < nch; ++j) {
+          const int ch = t0 + j;
+          if (ch < a.main_chunks)
+            tma_load_2d(smem_u32(sb + j * kBChunkBytes), &tmB, fb, kx, ch * kChunk, pol_stream);
+          else
+            tma_load_2d(smem_u32(sb + j * kBChunkBytes), &tmE, fb, kx, (ch - a.main_chunks) * kChunk, pol_keep);
+        }
+      }
+    }
+  }
+  pdl_wait();  // no global memory but the weights is touched above this line
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t pol_keep = policy_evict_last();    // activations: re-read by every column tile
-      const uint64_t pol_stream = policy_evict_first(); // weights: streamed
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -290,18 +312,20 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
       int c = c_begin, t0 = 0, nch = 0;
       while (ok && next_tile(c, c_end, a.main_chunks, t0, nch)) {
         for (int kb = kb0; kb < kb1; ++kb) {
+          // the first tile's first w_pre stages: fresh barriers, byte count and weights already set
+          const bool pre = issued < w_pre;
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
           const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(mt_valid * kATile + nch * kBChunkBytes));
+          if (!pre) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(mt_valid * kATile + nch * kBChunkBytes));
           uint8_t* sa = smem + stage * C::kStageBytes;
           uint8_t* sb = sa + MT * kATile;
           const int kx = kb * (kRowBytes / (TF32 ? 4 : 2));
           for (int mt = 0; mt < mt_valid; ++mt)
             tma_load_2d(smem_u32(sa + mt * kATile), &tmA, fb, kx, row0 + mt * 128, pol_keep);
-          for (int j = 0; j < nch; ++j) {
+          for (int j = 0; !pre && j < nch; ++j) {
             const int ch = t0 + j;
             if (ch < a.main_chunks)
               tma_load_2d(smem_u32(sb + j * kBChunkBytes), &tmB, fb, kx, ch * kChunk, pol_stream);
@@ -627,15 +651,38 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_trigger();
-  pdl_wait();  // no global memory is touched above this line
+  // The weight tiles of the first stages are requested before the wait on the preceding kernel:
+  // weights are never an output of the kernels this one overlaps, and their loads (from HBM) then
+  // run under that kernel's tail. The activation tiles follow after the wait.
+  int w_pre = 0;
+  const uint64_t pol_keep = policy_evict_last();  // activations: re-read by every column tile
+  // weights: streamed, but read by the pairs of every row group
+  const uint64_t pol_stream = DFL_PAIR_WPOL == 0 ? policy_evict_first()
+                              : DFL_PAIR_WPOL == 1 ? policy_evict_normal() : policy_evict_last();
+  if (warp == 0 && lane == 0) {
+    int u = u_begin, u0 = 0, nu = 0;
+    if (next_unit_tile(u, u_end, a.main_units, u0, nu)) {
+      const bool extra = u0 >= a.main_units;
+      const CUtensorMap* mw = extra ? &tmE : &tmB;
+      const int wrow0 = (extra ? u0 - a.main_units : u0) * 128 + static_cast<int>(rank) * nu * kChunk;
+      const uint32_t cta_bytes = static_cast<uint32_t>(kATile + nu * kBChunkBytes);
+      w_pre = min(C::kStages, kb1 - kb0);
+      for (int i = 0; i < w_pre; ++i) {
+        const uint32_t fb_own = smem_u32(&full[i]);
+        const uint32_t fb = mapa_shared(fb_own, 0);  // the leader's full barrier
+        if (rank == 0) mbar_arrive_expect_tx(fb_own, 2 * cta_bytes);
+        uint8_t* sb = smem + i * C::kStageBytes + kATile;
+        const int kx = (kb0 + i) * (kRowBytes / (TF32 ? 4 : 2));
+        for (int j = 0; j < nu; ++j)
+          tma_load_2d_pair(smem_u32(sb + j * kBChunkBytes), mw, fb, kx, wrow0 + j * kChunk, extra ? pol_keep : pol_stream);
+      }
+    }
+  }
+  pdl_wait();  // no global memory but the weights is touched above this line
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
-      const uint64_t pol_keep = policy_evict_last();  // activations: re-read by every column tile
-      // weights: streamed, but read by the pairs of every row group
-      const uint64_t pol_stream = DFL_PAIR_WPOL == 0 ? policy_evict_first()
-                                  : DFL_PAIR_WPOL == 1 ? policy_evict_normal() : policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -648,19 +695,22 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
         const int wrow0 = (extra ? u0 - a.main_units : u0) * 128 + static_cast<int>(rank) * nu * kChunk;
         const uint32_t cta_bytes = static_cast<uint32_t>(kATile + nu * kBChunkBytes);
         for (int kb = kb0; kb < kb1; ++kb) {
+          // the first tile's first w_pre stages: fresh barriers, byte count and weights already set
+          const bool pre = issued < w_pre;
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
           const uint32_t fb_own = smem_u32(&full[stage]);
           const uint32_t fb = mapa_shared(fb_own, 0);  // the leader's full barrier
-          if (rank == 0) mbar_arrive_expect_tx(fb_own, 2 * cta_bytes);
+          if (rank == 0 && !pre) mbar_arrive_expect_tx(fb_own, 2 * cta_bytes);
           uint8_t* sa = smem + stage * C::kStageBytes;
           uint8_t* sb = sa + kATile;
           const int kx = kb * (kRowBytes / (TF32 ? 4 : 2));
           tma_load_2d_pair(smem_u32(sa), &tmA, fb, kx, rowA, pol_keep);
-          for (int j = 0; j < nu; ++j)
-            tma_load_2d_pair(smem_u32(sb + j * kBChunkBytes), mw, fb, kx, wrow0 + j * kChunk, pol_w);
+          if (!pre)
+            for (int j = 0; j < nu; ++j)
+              tma_load_2d_pair(smem_u32(sb + j * kBChunkBytes), mw, fb, kx, wrow0 + j * kChunk, pol_w);
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
