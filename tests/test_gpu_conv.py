@@ -33,7 +33,10 @@ def _site_dev(torch, s):
     # the streamed / fused passes at their limits: G = 2 (smallest), G = 32 (largest fused
     # finish), G = 33 (falls back to the side-1 pass and a separate norm), group 64 (the
     # coefficient tiles are too narrow for TMA: per-thread passes)
-    (4, 2, 512, 16), (3, 32, 512, 16), (2, 33, 512, 16), (2, 16, 512, 64)])
+    (4, 2, 512, 16), (3, 32, 512, 16), (2, 33, 512, 16), (2, 16, 512, 64),
+    # CTA pairs: 320 columns (two and a half units) over 160 rows, and two row groups with
+    # group 32 where the second group's peer CTA has no rows
+    (10, 16, 1280, 16), (10, 30, 1024, 32)])
 def test_prepare_finish_parity(torch, dtype, B, G, H, gs):
     import dflash2_block_drafter_gb300 as d
     wl = I.conv_case(100 + B * G + H, B, G, H, gs, dtype=dtype)
@@ -61,9 +64,10 @@ def test_prepare_finish_parity(torch, dtype, B, G, H, gs):
         assert_close_scaled(dev_f64(out), rx, rel=2e-3, what="finish out (f32)")
 
 
-def test_identity_and_shift_bit_exact(torch):
+@pytest.mark.parametrize("B", [4, 12])  # 64 rows (single-CTA GEMM) and 192 rows (CTA pairs)
+def test_identity_and_shift_bit_exact(torch, B):
     import dflash2_block_drafter_gb300 as d
-    B, G, H, gs = 4, 16, 512, 16
+    G, H, gs = 16, 512, 16
     wl = I.conv_case(3, B, G, H, gs)
     x = _dev(torch, wl.x0)
     w0 = torch.zeros((4 * H // gs, H), dtype=torch.bfloat16, device="cuda")
