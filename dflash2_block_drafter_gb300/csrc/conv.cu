@@ -56,6 +56,44 @@ __device__ __forceinline__ void store1(float* p, float v) { *p = v; }
 __device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float load1(const float* p) { return *p; }
 
+// 16 consecutive elements as 8 float pairs (bf16 widens exactly: its bits are the top half of
+// the float's), for the packed fp32 arithmetic of the streamed passes.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ void load16(const __nv_bfloat16* p, float2 (&f)[8]) {
+  const uint4 a = reinterpret_cast<const uint4*>(p)[0];
+  const uint4 b = reinterpret_cast<const uint4*>(p)[1];
+  f[0] = bf16x2_to_float2(a.x);
+  f[1] = bf16x2_to_float2(a.y);
+  f[2] = bf16x2_to_float2(a.z);
+  f[3] = bf16x2_to_float2(a.w);
+  f[4] = bf16x2_to_float2(b.x);
+  f[5] = bf16x2_to_float2(b.y);
+  f[6] = bf16x2_to_float2(b.z);
+  f[7] = bf16x2_to_float2(b.w);
+}
+__device__ __forceinline__ void load16(const float* p, float2 (&f)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 v = reinterpret_cast<const float4*>(p)[i];
+    f[2 * i] = make_float2(v.x, v.y);
+    f[2 * i + 1] = make_float2(v.z, v.w);
+  }
+}
+__device__ __forceinline__ void store16(__nv_bfloat16* p, const float2 (&f)[8]) {
+  uint4 u[2];
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(u);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = __float22bfloat162_rn(f[i]);
+  reinterpret_cast<uint4*>(p)[0] = u[0];
+  reinterpret_cast<uint4*>(p)[1] = u[1];
+}
+__device__ __forceinline__ void store16(float* p, const float2 (&f)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) reinterpret_cast<float4*>(p)[i] = make_float4(f[2 * i].x, f[2 * i].y, f[2 * i + 1].x, f[2 * i + 1].y);
+}
+
 
 // Rows per thread of the apply passes: a thread walks RPT consecutive rows of one 8-channel strip,
 // loading the base kernel once and taking each row's t-1 input from the previous iteration.
@@ -654,16 +692,29 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     }
     return;
   }
+  // Half-warp h of consumer warp w takes rows 2w + h (+ 16 k); lane l of the half owns the 16
+  // channels [16 l, 16 l + 16) of the strip: one group (or two, at group size 8), whose summed
+  // partials serve all 16 channels. Arithmetic in packed fp32 pairs, in the order
+  // (base[0][0] + D0) * n[t] + ((base[0][1] + D1) * n[t-1]).
   const int j = blockIdx.x % strips;
-  const int v = lane;
-  const int c = j * kStreamSW + v * 8;
-  const int gl = (v * 8) / gs;
-  const int g = j * cgrp + gl;
-  const bool leader = ((v * 8) % gs) == 0;
+  const int h = lane >> 4;
+  const int cl = (lane & 15) * 16;    // first channel within the strip
+  const int c = j * kStreamSW + cl;
+  const int gla = cl / gs;            // strip-local group of channels cl .. cl+7
+  const int glb = (cl + 8) / gs;      // and of cl+8 .. cl+15
+  const bool lead_a = (cl % gs) == 0;
+  const bool lead_b = glb != gla;     // group size 8: the second vector starts its own group
   const int N = 4 * groups;
-  float b0[8], b1[8];
-  load8(base + c, b0);      // base[0][0][c..]
-  load8(base + H + c, b1);  // base[0][1][c..]
+  float2 b0[8], b1[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 x = reinterpret_cast<const float4*>(base + c)[i];      // base[0][0][c..]
+    const float4 y = reinterpret_cast<const float4*>(base + H + c)[i];  // base[0][1][c..]
+    b0[2 * i] = make_float2(x.x, x.y);
+    b0[2 * i + 1] = make_float2(x.z, x.w);
+    b1[2 * i] = make_float2(y.x, y.y);
+    b1[2 * i + 1] = make_float2(y.z, y.w);
+  }
   int stage = 0;
   uint32_t phase = 0;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -676,34 +727,61 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     const T* sn = reinterpret_cast<const T*>(st);
     const float* sp = reinterpret_cast<const float*>(st + tileN);
     const int pstride = tileP / 4;  // floats between consecutive (split, side-tap) tiles
-    for (int t = warp; t < G; t += kStreamConsumers) {
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int s = 0; s < k_splits; ++s) {
+    for (int t = 2 * warp + h; t < G; t += 2 * kStreamConsumers) {
+      float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
+      const float* pa = sp + t * cgrp + gla;
+      for (int s = 0; s < k_splits; ++s, pa += 4 * pstride) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) d[q] += sp[(s * 4 + q) * pstride + t * cgrp + gl];
+        for (int q = 0; q < 4; ++q) {
+          da[q] += pa[q * pstride];
+          if (lead_b) db[q] += pa[q * pstride + 1];
+        }
       }
-      float cur[8], prev[8];
-      load8(sn + t * kStreamSW + v * 8, cur);
+      if (!lead_b) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) db[q] = da[q];
+      }
+      float2 cur[8], prev[8];
+      load16(sn + t * kStreamSW + cl, cur);
       if (t > 0) {
-        load8(sn + (t - 1) * kStreamSW + v * 8, prev);
+        load16(sn + (t - 1) * kStreamSW + cl, prev);
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) prev[i] = 0.f;
+        for (int i = 0; i < 8; ++i) prev[i] = make_float2(0.f, 0.f);
       }
-      float o[8];
+      const float2 d0a = make_float2(da[0], da[0]), d1a = make_float2(da[1], da[1]);
+      const float2 d0b = make_float2(db[0], db[0]), d1b = make_float2(db[1], db[1]);
+      float2 o[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = (b0[i] + d[0]) * cur[i] + (b1[i] + d[1]) * prev[i];
+      for (int i = 0; i < 8; ++i) {
+        const float2 k0 = __fadd2_rn(b0[i], i < 4 ? d0a : d0b);
+        const float2 k1 = __fadd2_rn(b1[i], i < 4 ? d1a : d1b);
+        o[i] = __ffma2_rn(k0, cur[i], __fmul2_rn(k1, prev[i]));
+      }
       const size_t row = static_cast<size_t>(b) * G + t;
-      store8(out + row * H + c, o);
-      if (leader) {
-        store1(coef1 + (row * 2 + 0) * groups + g, d[2]);
-        store1(coef1 + (row * 2 + 1) * groups + g, d[3]);
+      store16(out + row * H + c, o);
+      if (lead_a) {
+        const int g = j * cgrp + gla;
+        store1(coef1 + (row * 2 + 0) * groups + g, da[2]);
+        store1(coef1 + (row * 2 + 1) * groups + g, da[3]);
         if (d_full != nullptr) {
           float* df = d_full + row * N + g;
-          df[0] = d[0];
-          df[groups] = d[1];
-          df[2 * groups] = d[2];
-          df[3 * groups] = d[3];
+          df[0] = da[0];
+          df[groups] = da[1];
+          df[2 * groups] = da[2];
+          df[3 * groups] = da[3];
+        }
+      }
+      if (lead_b) {
+        const int g = j * cgrp + glb;
+        store1(coef1 + (row * 2 + 0) * groups + g, db[2]);
+        store1(coef1 + (row * 2 + 1) * groups + g, db[3]);
+        if (d_full != nullptr) {
+          float* df = d_full + row * N + g;
+          df[0] = db[0];
+          df[groups] = db[1];
+          df[2 * groups] = db[2];
+          df[3 * groups] = db[3];
         }
       }
     }
