@@ -582,12 +582,17 @@ def our_arm(args, wl_name):
 # per-launch DRAM traffic (bytes) of the head kernel from an ncu capture, by workload; None until
 # measured for the current kernel
 TRAFFIC_PER_LAUNCH = {
-    # dram__bytes_read.sum + dram__bytes_write.sum of tc_pair_kernel<bf16, TOPK> (960 rows),
-    # profiles/head_topk_selector-B64.md; the full tail runs the same head launch
-    "full-tail-B64": 3.396895e9 + 3.463168e6,
-    "selector-B64": 3.396895e9 + 3.463168e6,
-    # tc_gemm_kernel<1, bf16, TOPK> (15 rows), profiles/head_topk_selector-B1.md
-    "selector-B1": 2.543758e9 + 3.118080e6,
+    # dram__bytes_read.sum + dram__bytes_write.sum of the head GEMM and its top-K merge, per launch,
+    # caches flushed before each launch:
+    # tc_pair_kernel<bf16, TOPK> (960 rows) + topk_merge_kernel, profiles/launches_full-tail-B64.md
+    "full-tail-B64": 2.568084e9 + 1.66016e5 + 2.347744e6,
+    # the same launch in the selector workload, profiles/head_topk_selector-B64.md (the weight
+    # re-reads between row groups vary from capture to capture: 2.57-3.67 GB)
+    "selector-B64": 3.669052e9 + 3.286016e6 + 2.347776e6,
+    # tc_pair_kernel<bf16, TOPK> (480 rows) + topk_merge_wide_kernel, profiles/head_topk_selector-B32.md
+    "selector-B32": 3.173487e9 + 2.999296e6 + 2.359808e6,
+    # tc_gemm_kernel<1, bf16, TOPK> (15 rows) + topk_merge_wide_kernel, profiles/head_topk_selector-B1.md
+    "selector-B1": 2.543724e9 + 2.79168e6 + 3.16928e5,
 }
 
 
