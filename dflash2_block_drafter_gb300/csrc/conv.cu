@@ -344,8 +344,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                              int H, int gs, int n_items, int strips, int has_res, int n_stages, int stage_bytes,
                              int* err) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem =
-      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align1024(smem_raw);
   const int tileY = G * kStreamSW * static_cast<int>(sizeof(T));
   const int cgrp = kStreamSW / gs;  // groups per strip
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + n_stages * stage_bytes);
@@ -482,8 +481,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                             const __grid_constant__ CUtensorMap tmW, T* out, T* next_n, float eps, int G, int H,
                             int gs, int spc, int csize, int has_res, int next_row0, int stage_bytes, int* err) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem =
-      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align1024(smem_raw);
   const int es = static_cast<int>(sizeof(T));
   const int tileY = G * kStreamSW * es;
   const int cgrp = kStreamSW / gs;
@@ -621,6 +619,27 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   }
 }
 
+// D of one row and group (and of the next group when `two`) summed over KS split-K partial tiles
+// in split order; pa points at split 0's (side, tap) 0 tile, pstride floats apart.
+template <int KS>
+__device__ __forceinline__ void sum_splits(const float* pa, int pstride, bool two, float (&da)[4], float (&db)[4]) {
+  float va[KS][4], vb[KS][4];
+#pragma unroll
+  for (int s = 0; s < KS; ++s)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      va[s][q] = pa[(s * 4 + q) * pstride];
+      vb[s][q] = two ? pa[(s * 4 + q) * pstride + 1] : 0.f;
+    }
+#pragma unroll
+  for (int s = 0; s < KS; ++s)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      da[q] += va[s][q];
+      db[q] += vb[s][q];
+    }
+}
+
 // prepare's apply pass, streamed: out = side-0 conv of n, coef1 = side 1's deltas, d_full = D.
 // Per item (block b, strip j) the ring stage holds n[b, :, strip] (G x 256) and, for every K split
 // s and (side, tap) st, the G x (256/gs) tile of the fp32 partial sums of D for the strip's groups.
@@ -632,8 +651,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
                              int groups, int k_splits, int M, int n_items, int strips, int n_stages, int stage_bytes,
                              int* err) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem =
-      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align1024(smem_raw);
   const int es = static_cast<int>(sizeof(T));
   const int cgrp = kStreamSW / gs;
   const int tileN = round128(G * kStreamSW * es);
@@ -730,12 +748,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     for (int t = 2 * warp + h; t < G; t += 2 * kStreamConsumers) {
       float da[4] = {0.f, 0.f, 0.f, 0.f}, db[4] = {0.f, 0.f, 0.f, 0.f};
       const float* pa = sp + t * cgrp + gla;
-      for (int s = 0; s < k_splits; ++s, pa += 4 * pstride) {
+      switch (k_splits) {  // the common split counts unrolled: every load issued before the sums
+        case 1: sum_splits<1>(pa, pstride, lead_b, da, db); break;
+        case 2: sum_splits<2>(pa, pstride, lead_b, da, db); break;
+        case 3: sum_splits<3>(pa, pstride, lead_b, da, db); break;
+        default:
+          for (int s = 0; s < k_splits; ++s, pa += 4 * pstride) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          da[q] += pa[q * pstride];
-          if (lead_b) db[q] += pa[q * pstride + 1];
-        }
+            for (int q = 0; q < 4; ++q) {
+              da[q] += pa[q * pstride];
+              if (lead_b) db[q] += pa[q * pstride + 1];
+            }
+          }
       }
       if (!lead_b) {
 #pragma unroll

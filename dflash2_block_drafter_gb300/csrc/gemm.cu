@@ -223,8 +223,7 @@ __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
                    const __grid_constant__ CUtensorMap tmE, const GemmArgs a) {
   using C = Cfg<MT>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem =
-      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align1024(smem_raw);
   uint8_t* bar_area = smem + C::kStages * C::kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(bar_area);
   uint64_t* empty = full + C::kStages;
@@ -595,8 +594,7 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
                    const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmD, const GemmArgs a) {
   using C = PairCfg<MODE>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem =
-      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align1024(smem_raw);
   // layout: stages | barriers | bias. STORE stages its output tiles in the stage ring: a STORE pair
   // computes exactly one tile (the launcher checks), so once that accumulator is complete every
   // stage has been consumed by the MMAs and no further load is issued.

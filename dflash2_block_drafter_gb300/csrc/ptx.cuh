@@ -11,6 +11,9 @@ namespace dfl {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// The first 1024-byte-aligned byte of a dynamic shared-memory array (TMA and the 128-byte swizzle
+// want that alignment), computed as an offset so the pointer keeps its shared-memory provenance.
+__device__ __forceinline__ uint8_t* align1024(uint8_t* raw) { return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u); }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
