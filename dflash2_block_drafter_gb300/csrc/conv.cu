@@ -571,13 +571,25 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         }
         const float d0 = load1(sc + (t * 2 + 0) * cgrp + gl);
         const float d1 = load1(sc + (t * 2 + 1) * cgrp + gl);
+        // packed fp32 pairs: x = ((base + D0) * y[t] + (base' + D1) * y[t-1]) + residual
+        const float2 d0p = make_float2(d0, d0), d1p = make_float2(d1, d1);
         float o[8];
+        float2 sq = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = round_as<T>((b0[i] + d0) * cur[i] + (b1[i] + d1) * prev[i] + res[i]);
+        for (int i = 0; i < 4; ++i) {
+          const float2 k0 = __fadd2_rn(make_float2(b0[2 * i], b0[2 * i + 1]), d0p);
+          const float2 k1 = __fadd2_rn(make_float2(b1[2 * i], b1[2 * i + 1]), d1p);
+          const float2 pv = __fmul2_rn(k1, make_float2(prev[2 * i], prev[2 * i + 1]));
+          const float2 x = __fadd2_rn(__ffma2_rn(k0, make_float2(cur[2 * i], cur[2 * i + 1]), pv),
+                                      make_float2(res[2 * i], res[2 * i + 1]));
+          const float2 xr = make_float2(round_as<T>(x.x), round_as<T>(x.y));
+          o[2 * i] = xr.x;
+          o[2 * i + 1] = xr.y;
+          sq = __ffma2_rn(xr, xr, sq);
+        }
         store8(out + (static_cast<size_t>(b) * G + t) * H + c, o);
         store8(sr + t * kStreamSW + v * 8, o);  // x as stored, for pass 2
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ss[k] = fmaf(o[i], o[i], ss[k]);
+        ss[k] += sq.x + sq.y;
       }
     }
     // the CTA's partial of each of this warp's rows, to every CTA of the cluster
@@ -611,8 +623,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
         float x8[8], w8[8], o[8];
         load8(sr + t * kStreamSW + v * 8, x8);
         load8(sw + v * 8, w8);
+        const float2 r2 = make_float2(r, r);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = x8[i] * r * w8[i];
+        for (int i = 0; i < 4; ++i) {  // (x * r) * w in packed pairs
+          const float2 y2 = __fmul2_rn(__fmul2_rn(make_float2(x8[2 * i], x8[2 * i + 1]), r2),
+                                       make_float2(w8[2 * i], w8[2 * i + 1]));
+          o[2 * i] = y2.x;
+          o[2 * i + 1] = y2.y;
+        }
         store8(next_n + (static_cast<size_t>(b) * rows_out + (t - next_row0)) * H + (strip0 + s) * kStreamSW + v * 8, o);
       }
     }
