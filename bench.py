@@ -585,14 +585,14 @@ TRAFFIC_PER_LAUNCH = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the head GEMM and its top-K merge, per launch,
     # caches flushed before each launch:
     # tc_pair_kernel<bf16, TOPK> (960 rows) + topk_merge_kernel, profiles/launches_full-tail-B64.md
-    "full-tail-B64": 2.568084e9 + 1.66016e5 + 2.347744e6,
+    "full-tail-B64": 3.744952e9 + 4.1728e5 + 2.351872e6,
     # the same launch in the selector workload, profiles/head_topk_selector-B64.md (the weight
-    # re-reads between row groups vary from capture to capture: 2.57-3.67 GB)
-    "selector-B64": 3.669052e9 + 3.286016e6 + 2.347776e6,
+    # re-reads between row groups vary from capture to capture: 2.57-3.96 GB)
+    "selector-B64": 3.687497e9 + 3.536896e6 + 2.347264e6,
     # tc_pair_kernel<bf16, TOPK> (480 rows) + topk_merge_wide_kernel, profiles/head_topk_selector-B32.md
-    "selector-B32": 3.173487e9 + 2.999296e6 + 2.359808e6,
+    "selector-B32": 2.824793e9 + 3.0336e6 + 2.36032e6,
     # tc_gemm_kernel<1, bf16, TOPK> (15 rows) + topk_merge_wide_kernel, profiles/head_topk_selector-B1.md
-    "selector-B1": 2.543724e9 + 2.79168e6 + 3.16928e5,
+    "selector-B1": 2.543954e9 + 2.483968e6 + 3.16928e5,
 }
 
 
