@@ -402,6 +402,54 @@ def test_block_tail_composition_shapes_and_zero_codebooks():
     assert np.array_equal(out["path"], np.argmax(h @ W.T + bias, axis=-1))
 
 
+def test_block_tail_predecessor_free_codebooks_reduce_to_per_slot_choice():
+    # End to end with hand-computed intermediates: identity conv sites make x = x0 + sum of the
+    # sublayer outputs; the final norm, head, top-K and z are written out in plain numpy; and with
+    # every predecessor codebook row equal, S no longer depends on the previous choice, so the walk
+    # picks, slot by slot, the candidate maximising logit + sum_r pred_r z_r succ[cand, r].
+    class Site:
+        pass
+    B, G, H, gs, V, K, R, eps = 4, 9, 32, 16, 64, 4, 8, 1e-6
+    ident = np.zeros((2, 2, H))
+    ident[:, 0] = 1.0
+    sites = []
+    for _ in range(2):
+        st = Site()
+        st.w_kp = np.zeros((4 * H // gs, H))
+        st.base = ident
+        st.norm_w = np.ones(H)
+        st.y = _rand(B, G, H)
+        sites.append(st)
+    x0 = _rand(B, G, H)
+    g = 0.5 + RNG.random(H)
+    W, bias, P = _rand(V, H), _rand(V), _rand(R, H)
+    p_row = _rand(R)
+    pred = np.tile(p_row, (V, 1))
+    succ = _rand(V, R, scale=0.05)  # the pairwise term on the scale of the logit gaps
+    anchors = RNG.integers(0, V, size=B)
+    out = O.block_tail(x0, sites, g, eps, gs, W, bias, P, pred, succ, anchors, K)
+
+    x = x0 + sites[0].y + sites[1].y
+    xr = x[:, 1:]
+    h = xr / np.sqrt((xr * xr).mean(axis=-1, keepdims=True) + eps) * g
+    logits = h @ W.T + bias
+    z = h @ P.T
+    assert np.allclose(out["x"], x) and np.allclose(out["h"], h) and np.allclose(out["z"], z)
+    want = np.empty((B, G - 1), dtype=np.int64)
+    unary_only = np.empty_like(want)
+    pair_only = np.empty_like(want)
+    for b in range(B):
+        for l in range(G - 1):
+            cand = np.argsort(-logits[b, l], kind="stable")[:K]
+            pair = (succ[cand] * (p_row * z[b, l])).sum(axis=-1)
+            want[b, l] = cand[int(np.argmax(logits[b, l, cand] + pair))]
+            unary_only[b, l] = cand[0]
+            pair_only[b, l] = cand[int(np.argmax(pair))]
+    # both terms decide some slots, so dropping either one would change the path
+    assert not np.array_equal(want, unary_only) and not np.array_equal(want, pair_only)
+    assert np.array_equal(out["path"], want)
+
+
 def test_listed_vocabulary_equals_masked_full_head():
     # Top-K over a sorted draft vocabulary S (head rows W[S]) mapped through ids equals the full
     # head's top-K with every unlisted logit removed (same tie rule: the listed order is id order).
