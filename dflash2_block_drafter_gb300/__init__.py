@@ -116,6 +116,27 @@ def _code(t):
         raise ValueError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float32") from None
 
 
+def _head_shapes(h, w_head, w_proj, K, cand, unary, z, logits):
+    """Shape checks of the head calls, before anything reaches the library: the kernels trust M, H,
+    V and R, so an undersized output or a weight of the wrong width would be read or written out
+    of bounds. Returns (M, H, V, R)."""
+    if h.dim() != 2:
+        raise ValueError(f"h must be [M, H], got shape {tuple(h.shape)}")
+    M, H = h.shape
+    if w_head.dim() != 2 or w_head.shape[1] != H:
+        raise ValueError(f"w_head must be [V, {H}], got shape {tuple(w_head.shape)}")
+    V = w_head.shape[0]
+    R = 0
+    if w_proj is not None:
+        if w_proj.dim() != 2 or w_proj.shape[1] != H:
+            raise ValueError(f"w_proj must be [R, {H}], got shape {tuple(w_proj.shape)}")
+        R = w_proj.shape[0]
+    for t, n, name in ((cand, M * K, "cand"), (unary, M * K, "unary"), (z, M * R, "z"), (logits, M * V, "logits")):
+        if t is not None and t.numel() < n:
+            raise ValueError(f"{name} holds {t.numel()} elements, fewer than the {n} the call writes")
+    return M, H, V, R
+
+
 def _workspace(nbytes, device, ws):
     if ws is None:
         ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
@@ -184,9 +205,7 @@ def dflash2_head_topk_workspace_bytes(M, H, V, K, R) -> int:
 def dflash2_head_topk(h, w_head, K, bias=None, w_proj=None, cand=None, unary=None, z=None, logits=None,
                       want_logits=False, workspace=None, stream=None):
     """Head GEMM + fused top-K (+ z). h: [M, H]. Returns (cand [M,K] int32, unary [M,K] f32, z [M,R] or None, logits or None)."""
-    M, H = h.shape
-    V = w_head.shape[0]
-    R = w_proj.shape[0] if w_proj is not None else 0
+    M, H, V, R = _head_shapes(h, w_head, w_proj, K, cand, unary, z, logits)
     dt = h.dtype
     dev = h.device
     cand = torch.empty((M, K), dtype=torch.int32, device=dev) if cand is None else cand
@@ -209,9 +228,9 @@ def dflash2_head_topk_vocab(h, w_listed, vocab_ids, K, bias_listed=None, w_proj=
                             logits=None, want_logits=False, workspace=None, stream=None):
     """Head GEMM + fused top-K over a draft vocabulary: rows of w_listed are the listed tokens
     vocab_ids (int32). Returns (cand [M,K] token ids, unary, z or None, logits [M,V_listed] or None)."""
-    M, H = h.shape
-    V = w_listed.shape[0]
-    R = w_proj.shape[0] if w_proj is not None else 0
+    M, H, V, R = _head_shapes(h, w_listed, w_proj, K, cand, unary, z, logits)
+    if vocab_ids.numel() < V:
+        raise ValueError(f"vocab_ids holds {vocab_ids.numel()} ids, fewer than the {V} listed rows")
     dt = h.dtype
     dev = h.device
     cand = torch.empty((M, K), dtype=torch.int32, device=dev) if cand is None else cand
@@ -267,14 +286,12 @@ def dflash2_head_topk_noalloc(h, w_head, K, bias=None, w_proj=None, cand=None, u
                               want_logits=False, stream=None):
     """dflash2_head_topk with its scratch in the library's fixed device array instead of a workspace.
 
-    For callers that cannot allocate device memory while the head runs (inside a graph capture, a
-    serving loop, or a host that only passes input and output buffers). Outputs not passed in are
+    For callers that cannot allocate device memory while the head runs (a serving loop where an
+    allocation would stall the device, or a host that only passes input and output buffers). Outputs not passed in are
     still allocated here by torch for convenience; pass them all to allocate nothing. Calls that
     overlap on the GPU share the array and race; keep them on one stream.
     """
-    M, H = h.shape
-    V = w_head.shape[0]
-    R = w_proj.shape[0] if w_proj is not None else 0
+    M, H, V, R = _head_shapes(h, w_head, w_proj, K, cand, unary, z, logits)
     dt = h.dtype
     dev = h.device
     cand = torch.empty((M, K), dtype=torch.int32, device=dev) if cand is None else cand

@@ -1,10 +1,10 @@
 // dflash2_head_topk_noalloc: the head GEMM + fused top-K + hidden_projection with its scratch
 // in a fixed device array owned by this library, for callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc at all, or not at the moment they need the head: code
-// running inside a CUDA-graph capture or a real-time serving loop where an allocation would
-// stall or break the capture, a host runtime whose allocator is not CUDA-aware, or plug-in hosts
-// that hand over only the input and output buffers. dflash2_head_topk needs a caller workspace
+// Some callers cannot call cudaMalloc at all, or not at the moment they need the head: a
+// real-time serving loop where an allocation would stall every other stream of the device, a host
+// runtime whose allocator is not CUDA-aware, or plug-in hosts that hand over only the input and
+// output buffers. dflash2_head_topk needs a caller workspace
 // for the per-column-range top-K lists; this variant keeps those lists in `g_head_scratch`, a
 // file-scope device array of kNoallocScratchBytes (8 MiB) instead.
 //
@@ -18,7 +18,10 @@
 //  * Nothing in the array must start at zero: every list entry the merge step reads is written
 //    earlier in the same call, so the array is never cleared.
 //  * The first call on a device looks up the array's device address (cudaGetSymbolAddress with
-//    that device current) and caches it; make that first call before any stream capture.
+//    that device current) and caches it; make that first call before any stream capture. The
+//    cache is keyed by device index, so the address belongs to the device's primary context (the
+//    CUDA runtime's) and is valid until cudaDeviceReset; after a reset, or in another driver-API
+//    context, this entry point must not be called.
 //  * Sizes whose lists need more than 8 MiB are rejected with DFLASH2_ERR_INVALID_ARG (e.g. up to
 //    about 65,000 rows on a 152-SM GB300; 960 rows need about 4.7 MB).
 //  * No cudaMalloc, cudaFree or allocating library routine is called.

@@ -49,17 +49,13 @@ __device__ __forceinline__ int warp_argmax(float v, int K) {
   return static_cast<int>(imin);
 }
 
-// Draft length of block b: depths[b] slots (the rest of the block's rows are padding of a
-// mixed-depth batch; dflash2.ts blockColumns), all `steps` without a depths array. A value
-// outside [0, steps] records DFLASH2_ERR_INVALID_ARG in the error word and is clamped.
-__device__ __forceinline__ int block_depth(const int32_t* depths, int b, int steps, int* err) {
+// Draft length of block b: all `steps` slots without a depths array; else the tokens a block
+// asked to draft depths[b] drafts, min(steps, max(1, depths[b])) (dflash2.ts blockColumns: the
+// anchor and max(1, depth) mask rows, at most the block; MAX supports_zero_draft_rows is False).
+// Every value is accepted, as blockColumns accepts it.
+__device__ __forceinline__ int block_depth(const int32_t* depths, int b, int steps) {
   if (depths == nullptr) return steps;
-  const int d = depths[b];
-  if (d < 0 || d > steps) {
-    if (err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_INVALID_ARG));
-    return d < 0 ? 0 : steps;
-  }
-  return d;
+  return min(steps, max(1, static_cast<int>(depths[b])));
 }
 
 // Slots are processed in chunks of `lchunk` (all of them at once at the drafter's shape).
@@ -133,7 +129,7 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
   }
   if (path != nullptr && tid < 32) {
-    const int d = block_depth(depths, b, steps, err);
+    const int d = block_depth(depths, b, steps);
     int p = 0;
     for (int l = 0; l < d; ++l) {
       const float v = tid < K ? sS[(l * K + p) * K + tid] : -INFINITY;
@@ -154,7 +150,7 @@ __global__ void __launch_bounds__(128) select_path_kernel(const float* __restric
   const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
-  const int d = block_depth(depths, b, steps, err);
+  const int d = block_depth(depths, b, steps);
   for (int l = d + lane; l < steps; l += 32) path[static_cast<size_t>(b) * steps + l] = -1;
   int p = 0;
   for (int l = 0; l < d; ++l) {
@@ -327,7 +323,7 @@ __global__ void __launch_bounds__(32 * kEdgeWarpsMax)
   if (path != nullptr && warp == 0) {
     // The walk touches only shared memory: lane l keeps the position chosen at slot l (lane l - 32
     // for slots 32..63), and the candidate ids are looked up afterwards in one parallel round.
-    const int d = block_depth(depths, b, steps, err);
+    const int d = block_depth(depths, b, steps);
     int p = 0, pos_lo = 0, pos_hi = 0;
     for (int l = 0; l < d; ++l) {
       const float v = lane < K ? sS[(l * K + p) * K + lane] : -INFINITY;

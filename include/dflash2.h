@@ -185,10 +185,10 @@ DFLASH2_API int dflash2_head_topk_vocab(const void* h, int M, int H, const void*
 
 /* ------------------------------------------------------------------------------------
  * Allocation-free variant of dflash2_head_topk. The pages describe no counterpart: this entry
- * point exists for callers that cannot allocate device memory when they run the head — code
- * inside a CUDA-graph capture or a latency-bound serving loop where cudaMalloc would stall or break
- * the capture, host runtimes without a CUDA-aware allocator, and plug-in hosts that only hand over
- * the input and output buffers. Arguments and results are those of dflash2_head_topk without the
+ * point exists for callers that cannot allocate device memory when they run the head — a
+ * latency-bound serving loop where a cudaMalloc would stall every other stream of the device, a
+ * host runtime whose allocator is not CUDA-aware, and plug-in hosts that only hand over the input
+ * and output buffers. Arguments and results are those of dflash2_head_topk without the
  * workspace: the top-K scratch lives in a fixed 8 MiB device array inside the library, held on
  * every device that loads the library until the process exits.
  *  - Calls whose scratch would exceed 8 MiB are rejected with DFLASH2_ERR_INVALID_ARG (960 rows
@@ -196,6 +196,9 @@ DFLASH2_API int dflash2_head_topk_vocab(const void* h, int M, int H, const void*
  *  - All calls on a device share the array and it keeps the last call's contents; nothing in it
  *    needs to start at zero. Calls that overlap on the GPU race on it: keep them on one stream.
  *  - The first call on a device looks up the array's address; make it before any stream capture.
+ *    The address is cached per device index: it belongs to the device's primary context (the one
+ *    the CUDA runtime uses) and stays valid until cudaDeviceReset; callers that bind another
+ *    context with the driver API, or reset the device, must not call this entry point afterwards.
  *  - Never calls cudaMalloc, cudaFree or any allocating library routine.
  * ---------------------------------------------------------------------------------- */
 DFLASH2_API int dflash2_head_topk_noalloc(const void* h, int M, int H, const void* w_head, int V, const float* bias,
@@ -227,14 +230,16 @@ DFLASH2_API int dflash2_score_edges(const int32_t* cand, const float* unary, con
  * 1 <= steps, 1 <= K <= 32. */
 DFLASH2_API int dflash2_select_path(const float* S, const int32_t* cand, int B, int steps, int K, int32_t* path, void* stream);
 
-/* Mixed-depth batches (dflash2.ts blockColumns / #block: a block drafting `depth` tokens runs over
- * its anchor and `depth` mask rows). In a dense [B, G, ...] batch block b may draft only
- * depths[b] <= G-1 tokens; its rows past depths[b] + 1 are padding. The conv and the head need no
- * change for that (the conv only looks one row back, and the head works row by row), so only the
- * walk honours the depths: block b walks slots [0, depths[b]) and path[b, l] = -1 for later slots.
- *   depths [B] int32 in [0, steps] (device; a value outside records DFLASH2_ERR_INVALID_ARG in the
- *   device error word and is clamped). Other arguments as for dflash2_score_edges /
- *   dflash2_select_path; path is required. S (if requested) is computed for every slot. */
+/* Mixed-depth batches (dflash2.ts blockColumns / #block: a block asked to draft `depth` tokens runs
+ * over its anchor and min(G - 1, max(1, depth)) mask rows; MAX DFlash2Qwen3_5.supports_zero_draft_rows
+ * is False, so no block drafts nothing). In a dense [B, G, ...] batch block b drafts
+ * d_b = min(steps, max(1, depths[b])) tokens; its rows past d_b + 1 are padding. The conv and the
+ * head need no change for that (the conv only looks one row back, and the head works row by row),
+ * so only the walk honours the depths: block b walks slots [0, d_b) and path[b, l] = -1 for later
+ * slots.
+ *   depths [B] int32 (device). Every value is accepted and clamped to [1, steps] as blockColumns
+ *   clamps it. Other arguments as for dflash2_score_edges / dflash2_select_path; path is required.
+ *   S (if requested) is computed for every slot. */
 DFLASH2_API int dflash2_score_edges_depths(const int32_t* cand, const float* unary, const float* z,
                                            const int32_t* anchors, const void* pred_book, const void* succ_book,
                                            const int32_t* depths, int B, int steps, int K, int R, int V, int dtype,

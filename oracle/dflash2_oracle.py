@@ -250,13 +250,24 @@ def select_path(S, cand, seed_index: int = 0):
     return path, pos
 
 
+def block_columns(depth: int, G: int) -> int:
+    """Rows a block drafting ``depth`` tokens runs over: min(G, max(1, depth) + 1).
+
+    [ts] ``blockColumns`` (the anchor and up to ``depth`` mask positions, never fewer than one);
+    [max] ``DFlash2Qwen3_5.supports_zero_draft_rows`` is False (no block drafts nothing).
+    A block over ``columns`` rows drafts ``columns - 1`` tokens.
+    """
+    return min(int(G), max(1, int(depth)) + 1)
+
+
 def select_path_depths(S, cand, depths):
     """The greedy walk of blocks that draft different numbers of tokens in one batch.
 
-    [ts] ``blockColumns`` / ``#block`` (a block runs over ``columns = min(G, depth + 1)`` rows: the
-    anchor and ``depth`` mask rows, so it drafts ``depth`` tokens). Block b walks only its first
-    ``depths[b]`` slots; the slots after them hold -1 (no token). Rows past a block's depth are
-    padding in a dense [B, G, ...] batch.
+    [ts] ``blockColumns`` / ``#block``: a block asked to draft ``depth`` tokens runs over
+    ``block_columns(depth, steps + 1)`` rows (the anchor and its mask rows) and drafts one token
+    per mask row, so block b walks its first ``min(steps, max(1, depths[b]))`` slots; every
+    value of ``depths`` is accepted, as ``blockColumns`` accepts it. The slots after them hold -1
+    (no token). Rows past a block's depth are padding in a dense [B, G, ...] batch.
     Returns (path ids [B, steps] with -1 padding, chosen positions [B, steps] with -1 padding).
     """
     S = _f64(S)
@@ -265,7 +276,7 @@ def select_path_depths(S, cand, depths):
     pos = np.full((B, steps), -1, dtype=np.int64)
     path = np.full((B, steps), -1, dtype=np.int64)
     for b in range(B):
-        d = int(depths[b])
+        d = block_columns(depths[b], steps + 1) - 1
         p = 0
         for l in range(d):
             c = int(np.argmax(S[b, l, p, :]))

@@ -24,3 +24,17 @@ def load_golden(name):
             key, *vals = line.split()
             out[key] = [float(v) for v in vals]
     return out
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the near-tie counts the GPU parity tests recorded (rows whose top-K membership, and
+    blocks whose walk, the tolerance cannot decide), so that they reach the session's output."""
+    try:
+        from tests.parity import REPORT
+    except Exception:
+        return
+    if not REPORT:
+        return
+    terminalreporter.write_line("parity near-tie counts:")
+    for name, counts in REPORT:
+        terminalreporter.write_line(f"  {name}: " + ", ".join(f"{k}={v}" for k, v in counts.items()))

@@ -167,3 +167,32 @@ def test_launch_count_queries(lib):
     assert lib.dflash2_conv_finish_launches(5, 64, 256, 16, f32, 1) == 2
     assert lib.dflash2_conv_prepare_launches(1, 16, 5000, 16, bf16, 0) == -1  # H % 64: rejected
     assert lib.dflash2_conv_finish_launches(1, 65, 5120, 16, bf16, 1) == -1   # G > 64: rejected
+
+
+@pytest.mark.parametrize("entry", ["dflash2_head_topk", "dflash2_head_topk_noalloc", "dflash2_head_topk_vocab"])
+def test_head_bindings_reject_mismatched_shapes_before_the_library(entry):
+    """The bindings check sizes before any pointer reaches the library: an undersized output or a
+    weight of the wrong width would make the head kernels read or write out of bounds."""
+    import torch
+    import dflash2_block_drafter_gb300 as d
+    fn = getattr(d, entry)
+    M, H, V, R, K = 6, 64, 100, 16, 4
+    h = torch.zeros(M, H)
+    good = dict(w=torch.zeros(V, H), w_proj=torch.zeros(R, H))
+    extra = (torch.arange(V, dtype=torch.int32),) if entry.endswith("vocab") else ()
+
+    def call(w=good["w"], **kw):
+        kw.setdefault("w_proj", good["w_proj"])
+        return fn(h, w, *extra, K, **kw)
+    bad = [dict(w=torch.zeros(V, H + 64)),                       # head width != H
+           dict(w_proj=torch.zeros(R, H - 8)),                   # projection width != H
+           dict(cand=torch.zeros(M * K - 1, dtype=torch.int32)),  # undersized outputs
+           dict(unary=torch.zeros(M, K - 1)),
+           dict(z=torch.zeros(M, R - 1)),
+           dict(logits=torch.zeros(M, V - 1))]
+    for kw in bad:
+        with pytest.raises(ValueError):
+            call(**kw)
+    if extra:
+        with pytest.raises(ValueError):
+            fn(h, good["w"], extra[0][:V - 1], K, w_proj=good["w_proj"])

@@ -1,5 +1,5 @@
 """Host-side checks of bench.py: the algorithmic byte and flop formulas behind every roofline
-fraction, the per-workload traffic table, and the JSON line of the reference (oracle) arm."""
+fraction, the per-workload traffic table (dropped once the kernel changes), and the JSON line of the reference (oracle) arm."""
 import json
 import os
 import subprocess
@@ -48,11 +48,21 @@ def test_edge_score_bytes_per_slot():
     assert bench.edges_call_bytes(64, 15, K, R) == 64 * 15 * per_slot
 
 
-def test_traffic_table_names_only_known_workloads():
-    assert set(bench.TRAFFIC_PER_LAUNCH) <= set(bench.WORKLOADS)
-    for name, t in bench.TRAFFIC_PER_LAUNCH.items():
+def test_traffic_table_names_only_known_workloads_and_is_dropped_when_the_kernel_changes():
+    assert set(bench.HEAD_TRAFFIC) <= set(bench.WORKLOADS)
+    for name, t in bench.HEAD_TRAFFIC.items():
         # every measured launch read at least the head weight once
-        assert t >= 2 * (V + R) * H, name
+        assert t["bytes"] >= 2 * (V + R) * H, name
+        assert t["date"] and len(t["gemm_sha"]) == 16
+    saved = dict(bench.HEAD_TRAFFIC)
+    try:
+        bench.HEAD_TRAFFIC["full-tail-B64"] = {"bytes": 3e9, "date": "then", "gemm_sha": "0" * 16}
+        assert bench.head_traffic("full-tail-B64")["traffic"] is None
+        bench.HEAD_TRAFFIC["full-tail-B64"]["gemm_sha"] = bench.kernel_source_sha("gemm.cu")
+        assert bench.head_traffic("full-tail-B64")["traffic"] == 3e9
+    finally:
+        bench.HEAD_TRAFFIC.clear()
+        bench.HEAD_TRAFFIC.update(saved)
 
 
 def test_reference_arm_prints_one_contract_line():

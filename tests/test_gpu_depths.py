@@ -1,5 +1,6 @@
 """GPU parity of the mixed-depth walk (blocks of one batch drafting different numbers of tokens)
-against the float64 oracle: block b walks its first depths[b] slots, the rest of its path is -1."""
+against the float64 oracle: block b walks its first min(steps, max(1, depths[b])) slots (dflash2.ts
+blockColumns), the rest of its path is -1."""
 import numpy as np
 import pytest
 
@@ -25,10 +26,12 @@ def _case(seed, B, steps, K, R, V, dtype="bf16"):
     anchors = rng.integers(0, V, size=B).astype(np.int32)
     pred = I.normal(seed, "pred", (V, R), 0.5, dtype=dtype)
     succ = I.normal(seed, "succ", (V, R), 0.5, dtype=dtype)
-    depths = rng.integers(0, steps + 1, size=B).astype(np.int32)
+    depths = rng.integers(1, steps + 1, size=B).astype(np.int32)
     depths[0] = steps          # one full-depth block
     if B > 1:
-        depths[1] = 0          # and one that drafts nothing
+        depths[1] = 0          # one asked for nothing: it drafts one token (blockColumns)
+    if B > 2:
+        depths[2] = steps + 5  # one asked for more than the block holds: it drafts `steps`
     return cand, unary, z, anchors, pred, succ, depths
 
 
@@ -53,10 +56,9 @@ def test_mixed_depth_walk(torch, dtype, B, steps, K, R, V):
     gpath, _ = O.select_path_depths(S.astype(np.float64), cand, depths)
     np.testing.assert_array_equal(path, gpath)
     full_path, full_pos = O.select_path(rS, cand)
-    margins = O.walk_margins(rS, full_pos)
     tol = REL_TOL * scale_of(rS)
     mask = rpath >= 0
-    compare_walk(np.where(mask, path, full_path), full_path, margins, tol)
+    compare_walk(np.where(mask, path, full_path), rS, full_pos, cand, tol)
     # the standalone walk agrees with the fused one
     p2 = d.dflash2_select_path_depths(to_device(S), to_device(cand), to_device(depths)).cpu().numpy()
     np.testing.assert_array_equal(p2, path)
@@ -73,14 +75,21 @@ def test_full_depths_equal_the_plain_walk(torch):
     np.testing.assert_array_equal(p1.cpu().numpy(), p0.cpu().numpy())
 
 
-def test_out_of_range_depth_sets_error_word_and_clamps(torch):
+def test_depths_clamp_like_block_columns(torch):
+    """Depths outside [1, steps] draft min(steps, max(1, depth)) tokens and set no error."""
     import dflash2_block_drafter_gb300 as d
     from dflash2_block_drafter_gb300.tail import to_device
-    cand, unary, z, anchors, pred, succ, _ = _case(6, 3, 7, 8, 16, 500)
-    depths = np.array([7, 9, -2], np.int32)
-    S, path = d.dflash2_score_edges_depths(*[to_device(a) for a in (cand, unary, z, anchors, pred, succ, depths)])
-    assert d.dflash2_poll_error() == -1
+    cand, unary, z, anchors, pred, succ, _ = _case(6, 4, 7, 8, 16, 500)
+    depths = np.array([7, 9, -2, 0], np.int32)
+    args = [to_device(a) for a in (cand, unary, z, anchors, pred, succ)]
+    S, path = d.dflash2_score_edges_depths(*args, to_device(depths))
     assert d.dflash2_poll_error() == 0
     path = path.cpu().numpy()
-    assert (path[1] >= 0).all()        # 9 clamped to the 7 slots
-    assert (path[2] == -1).all()       # -2 clamped to nothing
+    _, full = d.dflash2_score_edges(*args)
+    full = full.cpu().numpy()
+    np.testing.assert_array_equal(path[0], full[0])
+    np.testing.assert_array_equal(path[1], full[1])        # 9 -> the 7 slots
+    for b in (2, 3):                                        # -2 and 0 -> one token
+        assert path[b, 0] == full[b, 0] and (path[b, 1:] == -1).all()
+    p2 = d.dflash2_select_path_depths(S, args[0], to_device(depths)).cpu().numpy()
+    np.testing.assert_array_equal(p2, path)

@@ -5,7 +5,7 @@ import pytest
 from oracle import dflash2_oracle as O
 from synth import inputs as I
 from tests.gpu_util import dev_f64, require_gpu
-from tests.parity import REL_TOL, assert_close_scaled, compare_topk, scale_of
+from tests.parity import REL_TOL, assert_close_scaled, compare_topk, record, scale_of
 
 pytestmark = pytest.mark.gpu
 
@@ -77,7 +77,8 @@ def _check_head(wl, dtype):
     bound = _arith_bound(np.abs(h) @ np.abs(W).T, H, dtype)
     assert np.max(np.abs(logits - ref)) <= bound, "logits outside the fp32-accumulation bound"
     tight = compare_topk(cand, unary, ref, wl.K, bound)
-    print(f"near-tie rows: {near} (stated rule), {tight} (arithmetic bound {bound:.3g}) of {h.shape[0]}")
+    record(f"head {dtype} M={h.shape[0]} V={wl.V}", near_tie_rows=near, near_tie_rows_arith_bound=tight,
+           rows=h.shape[0])
     # the unary values equal the logits the same kernel reported (no second rounding)
     np.testing.assert_array_equal(unary, np.take_along_axis(logits, cand.astype(np.int64), axis=1).astype(np.float32))
 
@@ -115,5 +116,5 @@ def test_head_topk_drafter_shape(torch, cfg, rows):
         mx = max(mx, float(np.max(np.abs(h[sel]) @ np.abs(W[v0:v0 + 16384]).T)))
     bound = _arith_bound(np.array([mx]), wl.H, "bf16")
     tight = compare_topk(cand[sel], unary[sel], ref, wl.K, bound)
-    print(f"config {cfg}: near-tie rows {near} (stated), {tight} (arithmetic bound {bound:.3g}) of {len(sel)}")
+    record(f"head drafter shape config {cfg}", near_tie_rows=near, near_tie_rows_arith_bound=tight, rows=len(sel))
     assert_close_scaled(z[sel], O.hidden_projection(h[sel], I.to_f64(wl.w_proj)), what="z")

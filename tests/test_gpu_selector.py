@@ -5,7 +5,7 @@ import pytest
 from oracle import dflash2_oracle as O
 from synth import inputs as I
 from tests.gpu_util import require_gpu
-from tests.parity import REL_TOL, assert_close_scaled, compare_walk, scale_of
+from tests.parity import REL_TOL, assert_close_scaled, compare_walk, record, scale_of
 
 pytestmark = pytest.mark.gpu
 
@@ -46,14 +46,14 @@ def test_score_edges_and_walk(torch, dtype, B, steps, K, R, V):
     assert_close_scaled(S, rS, rel=1e-5, what="S (fp32 bound)")
     rpath, rpos = O.select_path(rS, cand)
     tol = REL_TOL * scale_of(rS)
-    near, checked = compare_walk(path, rpath, O.walk_margins(rS, rpos), tol)
+    near, checked = compare_walk(path, rS, rpos, cand, tol)
     # the walk over the GPU's own S is exact (same fp32 values, same tie rule)
     gpath, _ = O.select_path(S.astype(np.float64), cand)
     np.testing.assert_array_equal(path, gpath)
     # the standalone walk agrees with the fused one
     p2 = d.dflash2_select_path(to_device(S), to_device(cand)).cpu().numpy()
     np.testing.assert_array_equal(p2, path)
-    print(f"walk: {checked} slots strict, {near} near-tie blocks")
+    record(f"score_edges {dtype} B={B} steps={steps} K={K} R={R} V={V}", near_tie_blocks=near, strict_slots=checked)
 
 
 def test_zero_codebooks_walk_is_top1(torch):

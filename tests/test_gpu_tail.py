@@ -5,7 +5,8 @@ import pytest
 from oracle import dflash2_oracle as O
 from synth import inputs as I
 from tests.gpu_util import dev_f64, oracle_sites, require_gpu
-from tests.parity import REL_TOL, assert_close_scaled, compare_topk, compare_walk, scale_of
+from tests.parity import (REL_TOL, assert_close_scaled, compare_path_end_to_end, compare_topk, compare_walk, record,
+                          scale_of)
 
 pytestmark = pytest.mark.gpu
 
@@ -15,7 +16,7 @@ def torch():
     return require_gpu()
 
 
-def _check_tail(run, wl, blocks):
+def _check_tail(run, wl, blocks, name):
     """Compare the GPU tail with the oracle on the listed blocks (blocks never interact)."""
     blocks = list(blocks)
     ref = O.block_tail(I.to_f64(wl.x0)[blocks], oracle_sites(wl, blocks), I.to_f64(wl.final_norm_w), wl.eps, wl.gs,
@@ -38,9 +39,14 @@ def _check_tail(run, wl, blocks):
     assert_close_scaled(S, ref_S, what="S")
     ref_path, ref_pos = O.select_path(ref_S, cand)
     path = run.path.cpu().numpy()[blocks]
-    walk_near, checked = compare_walk(path, ref_path, O.walk_margins(ref_S, ref_pos), REL_TOL * scale_of(ref_S))
-    # end to end against the oracle's own walk, up to the first slot either side leaves the decided region
-    print(f"tail: near-tie rows {near}, walk near-tie blocks {walk_near}, strict slots {checked}")
+    walk_near, checked = compare_walk(path, ref_S, ref_pos, cand, REL_TOL * scale_of(ref_S))
+    # end to end: the GPU's path against the oracle's own walk over the oracle's own candidates,
+    # slot by slot while both the head row and the walk are decided
+    e2e_near, e2e_checked = compare_path_end_to_end(path, ref, tol, REL_TOL * scale_of(ref["S"]))
+    assert e2e_checked > 0, "no slot of the end-to-end path was compared"
+    record(name, blocks=len(blocks), near_tie_rows=near, rows=len(blocks) * steps,
+           walk_near_tie_blocks=walk_near, walk_strict_slots=checked,
+           e2e_near_tie_blocks=e2e_near, e2e_strict_slots=e2e_checked)
     return ref
 
 
@@ -51,7 +57,7 @@ def test_tiny_full_tail_f32(torch):
     run.full(to_device(wl.x0), [to_device(s.y) for s in wl.sites], to_device(wl.anchors))
     import dflash2_block_drafter_gb300 as d
     assert d.dflash2_poll_error() == 0
-    ref = _check_tail(run, wl, range(wl.B))
+    ref = _check_tail(run, wl, range(wl.B), "tail tiny f32 (B=1, G=8, H=256)")
     assert_close_scaled(dev_f64(run.x), ref["x"], rel=2e-3, what="x (f32)")
 
 
@@ -63,7 +69,7 @@ def test_full_tail_b64_sampled(torch):
     run.full(to_device(wl.x0), [to_device(s.y) for s in wl.sites], to_device(wl.anchors))
     import dflash2_block_drafter_gb300 as d
     assert d.dflash2_poll_error() == 0
-    _check_tail(run, wl, [0, 31, 63])
+    _check_tail(run, wl, [0, 31, 63], "tail B=64 drafter shape (blocks 0, 31, 63)")
     path = run.path.cpu().numpy()
     assert path.shape == (64, 15) and np.all((path >= 0) & (path < wl.V))
 

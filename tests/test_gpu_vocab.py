@@ -5,7 +5,7 @@ import pytest
 from oracle import dflash2_oracle as O
 from synth import inputs as I
 from tests.gpu_util import dev_f64, require_gpu
-from tests.parity import REL_TOL, assert_close_scaled, compare_topk, compare_walk, scale_of
+from tests.parity import REL_TOL, assert_close_scaled, compare_topk, compare_walk, record, scale_of
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,8 @@ def test_listed_head_parity(torch, B, V, n_listed, bias):
     decided = O.kth_margin(ref, wl.K) > 4 * bound
     for r in np.where(decided)[0]:
         assert set(cand[r].tolist()) == set(ref_ids[r].tolist())
-    print(f"listed head: near-tie rows {near} (stated), {tight} (bound) of {h.shape[0]}")
+    record(f"listed head M={h.shape[0]} V_listed={len(S)}", near_tie_rows=near, near_tie_rows_arith_bound=tight,
+           rows=h.shape[0])
 
 
 def test_identity_vocabulary_equals_full_head(torch):
@@ -88,5 +89,5 @@ def test_listed_head_drafter_shape_feeds_the_walk(torch):
                        I.f64_view(wl.pred_book), I.f64_view(wl.succ_book))
     assert_close_scaled(S_gpu.cpu().numpy(), rS, what="S over listed candidates")
     rpath, rpos = O.select_path(rS, cand.reshape(B, steps, K))
-    compare_walk(path.cpu().numpy(), rpath, O.walk_margins(rS, rpos), REL_TOL * scale_of(rS))
+    compare_walk(path.cpu().numpy(), rS, rpos, cand.reshape(B, steps, K), REL_TOL * scale_of(rS))
     assert np.all(np.isin(path.cpu().numpy(), S))

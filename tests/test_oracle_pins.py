@@ -480,23 +480,33 @@ def test_listed_vocabulary_identity_map():
 
 def test_mixed_depth_walk_is_prefix_of_full_walk():
     # The walk is causal: a block that drafts d tokens chooses exactly the first d tokens of the
-    # full-depth walk, followed by -1 padding; d = steps reproduces the full walk.
-    B, steps, K, R, V = 6, 7, 5, 8, 60
+    # full-depth walk, followed by -1 padding; d = steps reproduces the full walk. Depths outside
+    # [1, steps] draft min(steps, max(1, d)) tokens (dflash2.ts blockColumns clamps both ends).
+    B, steps, K, R, V = 8, 7, 5, 8, 60
     cand = RNG.integers(0, V, size=(B, steps, K))
     unary = _rand(B, steps, K)
     z = _rand(B, steps, R)
     anchors = RNG.integers(0, V, size=B)
     S = O.score_edges(cand, unary, z, anchors, _rand(V, R), _rand(V, R))
     full, full_pos = O.select_path(S, cand)
-    depths = np.array([1, 7, 3, 0, 5, 2])
+    depths = np.array([1, 7, 3, 0, 5, 2, -4, 11])
+    drafted = [1, 7, 3, 1, 5, 2, 1, 7]
     path, pos = O.select_path_depths(S, cand, depths)
     for b in range(B):
-        d = depths[b]
+        d = drafted[b]
         assert np.array_equal(path[b, :d], full[b, :d])
         assert np.array_equal(pos[b, :d], full_pos[b, :d])
         assert np.all(path[b, d:] == -1) and np.all(pos[b, d:] == -1)
     p2, _ = O.select_path_depths(S, cand, np.full(B, steps))
     assert np.array_equal(p2, full)
+
+
+def test_block_columns_never_drafts_nothing():
+    # dflash2.ts blockColumns: the anchor plus max(1, depth) mask rows, at most the block size;
+    # MAX DFlash2Qwen3_5.supports_zero_draft_rows is False. Values worked by hand for G = 16.
+    G = 16
+    for depth, columns in [(0, 2), (-3, 2), (1, 2), (2, 3), (8, 9), (15, 16), (16, 16), (40, 16)]:
+        assert O.block_columns(depth, G) == columns, (depth, columns)
 
 
 def test_conv_rows_past_depth_do_not_reach_earlier_rows():

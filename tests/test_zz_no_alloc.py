@@ -1,7 +1,7 @@
 """The allocation-free head entry point (dflash2_head_topk_noalloc) against dflash2_head_topk.
 
-Callers that cannot allocate device memory while the head runs (inside a graph capture, in a
-serving loop, or in a host that only passes input and output buffers) use this variant: its top-K
+Callers that cannot allocate device memory while the head runs (a serving loop where an
+allocation would stall the device, or a host that only passes input and output buffers) use this variant: its top-K
 scratch is a fixed array inside the library rather than a caller workspace. Here both entry points
 run through the C ABI on the same inputs, twice in a row with different shapes (the shared array
 keeps the first call's contents), and must agree within the parity tolerance; every output buffer
