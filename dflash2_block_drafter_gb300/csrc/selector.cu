@@ -341,12 +341,407 @@ __global__ void __launch_bounds__(32 * kEdgeWarpsMax)
   }
 }
 
+// K = 16 kernel (the drafter's top-16): a CTA per block, W warps taking slots w, w + W, ...
+// Lane (c = lane & 15, half = lane >> 4) keeps successor row cand[c]'s half of r in registers
+// (fp32), the warp's 16 predecessor rows times z go to a padded shared-memory tile, and every
+// lane accumulates the 16 scores S[p][c] over its half of r with packed fp32 FMAs, reading the
+// tile as float4 broadcasts (the two halves sit 4 banks apart). One shuffle adds the halves.
+// The gathers of the warp's next slot are issued before the current slot is computed, and the
+// candidate ids two slots ahead before that, so each warp keeps a slot's rows in flight while it
+// computes. Every slot's 16 x 16 scores go to shared memory for the walk (warp 0, after the CTA
+// barrier) and, when requested, to S.
+template <typename T, int R>
+struct K16Slot {
+  static constexpr int E = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte segment
+  static constexpr int NS = R / E;                             // segments per codebook row
+  static constexpr int PS = NS / 2;                            // segments per lane (pred and succ)
+  static constexpr int HR = R / 2;                             // r values per half
+  static constexpr int WS = R + 8;                             // floats per pred*z row (2 halves + pad)
+  static_assert(NS >= 2 && NS <= 32 && (32 % NS) == 0, "row segments must tile a warp");
+};
+
+template <typename T, int R>
+__device__ __forceinline__ void k16_ids(const int32_t* __restrict__ cand, int anchor, size_t slot, int l, int lane,
+                                        int& cid, int (&pid)[K16Slot<T, R>::PS]) {
+  using P = K16Slot<T, R>;
+  cid = __ldg(cand + slot * 16 + (lane & 15));
+#pragma unroll
+  for (int i = 0; i < P::PS; ++i) {
+    const int p = lane / P::NS + i * (32 / P::NS);
+    pid[i] = l == 0 ? anchor : __ldg(cand + (slot - 1) * 16 + p);
+  }
+}
+
+template <typename T, int R>
+__device__ __forceinline__ bool k16_rows(const T* __restrict__ pred, const T* __restrict__ succ, int V, int lane,
+                                         int cid, const int (&pid)[K16Slot<T, R>::PS], uint4 (&rs)[K16Slot<T, R>::PS],
+                                         uint4 (&rp)[K16Slot<T, R>::PS]) {
+  using P = K16Slot<T, R>;
+  const int half = lane >> 4;
+  const int sg = lane % P::NS;
+  const bool okc = cid >= 0 && cid < V;
+  bool bad = !okc;
+  const T* srow = succ + static_cast<size_t>(okc ? cid : 0) * R + half * P::HR;
+#pragma unroll
+  for (int j = 0; j < P::PS; ++j) rs[j] = ldg16(srow + j * P::E);
+  if (!okc)
+#pragma unroll
+    for (int j = 0; j < P::PS; ++j) rs[j] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int i = 0; i < P::PS; ++i) {
+    const bool ok = pid[i] >= 0 && pid[i] < V;
+    bad |= !ok;
+    rp[i] = ldg16(pred + static_cast<size_t>(ok ? pid[i] : 0) * R + sg * P::E);
+    if (!ok) rp[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  return bad;
+}
+
+template <typename T, int R>
+__global__ void __launch_bounds__(512)
+    score_edges_k16_kernel(const int32_t* __restrict__ cand, const float* __restrict__ unary,
+                           const float* __restrict__ z, const int32_t* __restrict__ anchors,
+                           const T* __restrict__ pred, const T* __restrict__ succ, int steps, int V,
+                           float* __restrict__ S, int32_t* __restrict__ path, const int32_t* __restrict__ depths,
+                           int* err) {
+  using P = K16Slot<T, R>;
+  constexpr int PS = P::PS, E = P::E, NS = P::NS, HR = P::HR, WS = P::WS;
+  extern __shared__ float sm[];
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x;
+  const int W = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = lane & 15;
+  const int half = lane >> 4;
+  const int sg = lane % NS;  // this lane's segment of each predecessor row it gathers
+  float* sS = sm;            // [steps][16][16]
+  float* wt = sm + steps * 256 + warp * 16 * WS;  // [16][2 halves][HR + 4] pred rows * z
+  const int anchor = __ldg(anchors + b);
+  const size_t slot0 = static_cast<size_t>(b) * steps;
+  bool bad = false;
+
+  int l = warp;
+  int cid = 0, pid[PS] = {};
+  uint4 rs[PS], rp[PS];
+  float zc[E];
+  float un = 0.f;
+  if (l < steps) {
+    k16_ids<T, R>(cand, anchor, slot0 + l, l, lane, cid, pid);
+    bad |= k16_rows<T, R>(pred, succ, V, lane, cid, pid, rs, rp);
+#pragma unroll
+    for (int e = 0; e < E; e += 4) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(z + (slot0 + l) * R + sg * E + e));
+      zc[e] = v.x; zc[e + 1] = v.y; zc[e + 2] = v.z; zc[e + 3] = v.w;
+    }
+    un = __ldg(unary + (slot0 + l) * 16 + c);
+  }
+  int cidn = 0, pidn[PS] = {};
+  if (l + W < steps) k16_ids<T, R>(cand, anchor, slot0 + l + W, l + W, lane, cidn, pidn);
+
+  for (; l < steps; l += W) {
+    const int ln = l + W;
+    // next slot's rows, z and unary; the ids one slot further
+    uint4 rsn[PS], rpn[PS];
+    float zn[E];
+    float unn = 0.f;
+    if (ln < steps) {
+      bad |= k16_rows<T, R>(pred, succ, V, lane, cidn, pidn, rsn, rpn);
+#pragma unroll
+      for (int e = 0; e < E; e += 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(z + (slot0 + ln) * R + sg * E + e));
+        zn[e] = v.x; zn[e + 1] = v.y; zn[e + 2] = v.z; zn[e + 3] = v.w;
+      }
+      unn = __ldg(unary + (slot0 + ln) * 16 + c);
+      if (ln + W < steps) k16_ids<T, R>(cand, anchor, slot0 + ln + W, ln + W, lane, cidn, pidn);
+    }
+    // predecessor rows times z into the warp's tile
+#pragma unroll
+    for (int i = 0; i < PS; ++i) {
+      const int p = lane / NS + i * (32 / NS);
+      float f[E];
+      unpack16(rp[i], static_cast<const T*>(nullptr), f);
+      const int r0 = sg * E;
+      float* dst = wt + p * WS + (r0 >= HR ? HR + 4 : 0) + (r0 % HR);
+#pragma unroll
+      for (int e = 0; e < E; e += 4)
+        *reinterpret_cast<float4*>(dst + e) =
+            make_float4(f[e] * zc[e], f[e + 1] * zc[e + 1], f[e + 2] * zc[e + 2], f[e + 3] * zc[e + 3]);
+    }
+    // this lane's successor half-row in registers
+    float sv[HR];
+#pragma unroll
+    for (int j = 0; j < PS; ++j) unpack16(rs[j], static_cast<const T*>(nullptr), sv + j * E);
+    __syncwarp();
+    float2 acc[16];
+#pragma unroll
+    for (int p = 0; p < 16; ++p) acc[p] = make_float2(0.f, 0.f);
+    const float* wr = wt + half * (HR + 4);
+#pragma unroll
+    for (int j = 0; j < HR; j += 4) {
+#pragma unroll
+      for (int p = 0; p < 16; ++p) {
+        const float4 w4 = *reinterpret_cast<const float4*>(wr + p * WS + j);
+        acc[p] = __ffma2_rn(make_float2(w4.x, w4.y), make_float2(sv[j], sv[j + 1]), acc[p]);
+        acc[p] = __ffma2_rn(make_float2(w4.z, w4.w), make_float2(sv[j + 2], sv[j + 3]), acc[p]);
+      }
+    }
+    __syncwarp();  // the tile is rewritten for the next slot
+    const size_t slot = slot0 + l;
+#pragma unroll
+    for (int pp = 0; pp < 8; ++pp) {
+      float v0 = acc[2 * pp].x + acc[2 * pp].y;
+      float v1 = acc[2 * pp + 1].x + acc[2 * pp + 1].y;
+      v0 += __shfl_xor_sync(0xffffffffu, v0, 16);
+      v1 += __shfl_xor_sync(0xffffffffu, v1, 16);
+      const int p = 2 * pp + half;
+      const float v = un + (half ? v1 : v0);
+      sS[(l * 16 + p) * 16 + c] = v;
+      if (S != nullptr) S[(slot * 16 + p) * 16 + c] = v;
+    }
+    // rotate the pipeline
+#pragma unroll
+    for (int j = 0; j < PS; ++j) {
+      rs[j] = rsn[j];
+      rp[j] = rpn[j];
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) zc[e] = zn[e];
+    un = unn;
+  }
+  if (bad && err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_BAD_INDEX));
+  __syncthreads();
+  if (path != nullptr && warp == 0) {
+    const int d = block_depth(depths, b, steps);
+    int p = 0, pos_lo = 0, pos_hi = 0;
+    for (int t = 0; t < d; ++t) {
+      const float v = lane < 16 ? sS[(t * 16 + p) * 16 + lane] : -INFINITY;
+      const int cc = warp_argmax(v, 16);
+      if (lane == t) pos_lo = cc;
+      if (lane + 32 == t) pos_hi = cc;
+      p = cc;
+    }
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int t = lane + 32 * h2;
+      if (t >= steps) break;
+      path[slot0 + t] = t < d ? __ldg(cand + (slot0 + t) * 16 + (h2 == 0 ? pos_lo : pos_hi)) : -1;
+    }
+  }
+}
+
 size_t edges_smem(int steps, int K, int R, int lchunk) {
   return sizeof(float) * (static_cast<size_t>(steps) * K + static_cast<size_t>(steps) * K * K +
                           2 * static_cast<size_t>(lchunk) * K * (R + 1));
 }
 
 }  // namespace
+
+// bf16 codebooks, K = 16: each slot's edge term is a 16 x 16 x R product of the predecessor rows
+// times z (fp32) and the successor rows (bf16), done on the tensor cores with warp-level
+// mma.sync m16n8k8 tf32, straight from registers. The operand fragments are gathered directly:
+// the reduction index k of each MMA is mapped to r so that lane t (= lane & 3) owns the
+// contiguous chunk r in [t R/4, (t + 1) R/4) of its rows, which it loads as 16-byte vectors
+// (g = lane >> 2 gives the rows g and g + 8). Successor values are bf16, so exact in tf32; the
+// product w = pred * z is split into w_big = tf32(w) and w_small = w - w_big and both are
+// multiplied, so every product keeps about 21 bits (the error is below 2^-21 |w succ| per term),
+// with fp32 accumulation. One CTA per block: warp w takes slots w, w + W, ... . For every slot the
+// warp also reduces each predecessor row p to its best successor position (largest score, lowest
+// position on a tie) in shared memory, so that the walk after the CTA barrier is a chain of
+// table lookups, c_l = best[l][c_{l-1}], run by one thread.
+__device__ __forceinline__ void mma_16x8x8_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+template <int R>
+__global__ void __launch_bounds__(512, 2)
+    score_edges_mma_kernel(const int32_t* __restrict__ cand, const float* __restrict__ unary,
+                           const float* __restrict__ z, const int32_t* __restrict__ anchors,
+                           const __nv_bfloat16* __restrict__ pred, const __nv_bfloat16* __restrict__ succ, int steps,
+                           int V, float* __restrict__ S, int32_t* __restrict__ path,
+                           const int32_t* __restrict__ depths, int* err) {
+  constexpr int Q = R / 4;   // r values per lane and row
+  constexpr int NV = Q / 8;  // 16-byte vectors per lane and row
+  constexpr int KS = R / 8;  // MMA k-steps
+  static_assert(NV >= 1 && Q % 8 == 0, "R must be a multiple of 32");
+  extern __shared__ float sm[];
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x;
+  const int W = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  int* sId = reinterpret_cast<int*>(sm);                       // [steps][16] candidate ids, then [steps] path
+  uint8_t* sBest = reinterpret_cast<uint8_t*>(sId + steps * 17);  // [steps][16] best successor of each row
+  const int anchor = __ldg(anchors + b);
+  const size_t slot0 = static_cast<size_t>(b) * steps;
+  bool bad = false;
+  for (int l = warp; l < steps; l += W) {
+    const size_t slot = slot0 + l;
+    // this lane's rows: successors g and g + 8 of the slot, predecessors g and g + 8
+    int cs[2], ps[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      cs[h] = __ldg(cand + slot * 16 + g + 8 * h);
+      ps[h] = l == 0 ? anchor : __ldg(cand + (slot - 1) * 16 + g + 8 * h);
+    }
+    // z and unary do not depend on the ids: in flight with them, before the row gathers
+    float zc[Q];
+#pragma unroll
+    for (int e = 0; e < Q; e += 4) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(z + slot * R + Q * t + e));
+      zc[e] = v.x; zc[e + 1] = v.y; zc[e + 2] = v.z; zc[e + 3] = v.w;
+    }
+    float u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) u[i] = __ldg(unary + slot * 16 + 2 * t + (i & 1) + 8 * (i >> 1));
+    uint4 sv[2][NV], pv[2][NV];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const bool okc = cs[h] >= 0 && cs[h] < V;
+      const bool okp = ps[h] >= 0 && ps[h] < V;
+      bad |= !okc || !okp;
+      const __nv_bfloat16* srow = succ + static_cast<size_t>(okc ? cs[h] : 0) * R + Q * t;
+      const __nv_bfloat16* prow = pred + static_cast<size_t>(okp ? ps[h] : 0) * R + Q * t;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        sv[h][v] = okc ? ldg16(srow + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+        pv[h][v] = okp ? ldg16(prow + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    float acc[2][4] = {};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int v = ks / 4, wi = ks % 4;
+      const uint32_t p0 = word_of(pv[0][v], wi), p1 = word_of(pv[1][v], wi);
+      const float w0 = __uint_as_float(p0 << 16) * zc[2 * ks];              // row g,     r = Qt + 2ks
+      const float w1 = __uint_as_float(p1 << 16) * zc[2 * ks];              // row g + 8, r = Qt + 2ks
+      const float w2 = __uint_as_float(p0 & 0xffff0000u) * zc[2 * ks + 1];  // row g,     r = Qt + 2ks + 1
+      const float w3 = __uint_as_float(p1 & 0xffff0000u) * zc[2 * ks + 1];  // row g + 8, r = Qt + 2ks + 1
+      const uint32_t h0 = tf32_rna(w0), h1 = tf32_rna(w1), h2 = tf32_rna(w2), h3 = tf32_rna(w3);
+      const uint32_t l0 = __float_as_uint(w0 - __uint_as_float(h0)), l1 = __float_as_uint(w1 - __uint_as_float(h1));
+      const uint32_t l2 = __float_as_uint(w2 - __uint_as_float(h2)), l3 = __float_as_uint(w3 - __uint_as_float(h3));
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        const uint32_t sw = word_of(sv[n][v], wi);  // successor row g + 8n: r = Qt + 2ks (lo), + 1 (hi)
+        mma_16x8x8_tf32(acc[n], h0, h1, h2, h3, sw << 16, sw & 0xffff0000u);
+        mma_16x8x8_tf32(acc[n], l0, l1, l2, l3, sw << 16, sw & 0xffff0000u);
+      }
+    }
+    // acc[n] = S[g][8n + 2t], S[g][8n + 2t + 1], S[g + 8][8n + 2t], S[g + 8][8n + 2t + 1] (edge terms)
+    uint32_t bk[2] = {0u, 0u};
+    int bc[2] = {0, 0};
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int hr = i >> 1;  // row g + 8 hr
+        const int c = 8 * n + 2 * t + (i & 1);
+        const float val = u[2 * n + (i & 1)] + acc[n][i];
+        if (S != nullptr) S[(slot * 16 + g + 8 * hr) * 16 + c] = val;
+        // best successor of each predecessor row: largest score, lowest position on a tie
+        const uint32_t k = float_key(val);
+        if ((n == 0 && (i & 1) == 0) || k > bk[hr] || (k == bk[hr] && c < bc[hr])) {
+          bk[hr] = k;
+          bc[hr] = c;
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const uint32_t ok = __shfl_xor_sync(0xffffffffu, bk[hr], m);
+        const int oc = __shfl_xor_sync(0xffffffffu, bc[hr], m);
+        if (ok > bk[hr] || (ok == bk[hr] && oc < bc[hr])) {
+          bk[hr] = ok;
+          bc[hr] = oc;
+        }
+      }
+    }
+    if (t == 0) {
+      sBest[l * 16 + g] = static_cast<uint8_t>(bc[0]);
+      sBest[l * 16 + g + 8] = static_cast<uint8_t>(bc[1]);
+      sId[l * 16 + g] = cs[0];
+      sId[l * 16 + g + 8] = cs[1];
+    }
+  }
+  if (bad && err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_BAD_INDEX));
+  __syncthreads();
+  if (path != nullptr && warp == 0) {
+    // the walk follows the best-successor table: c_l = best[l][c_{l-1}], c_{-1} = 0
+    int* sPath = sId + steps * 16;
+    if (lane == 0) {
+      const int d = block_depth(depths, b, steps);
+      int p = 0;
+      for (int tt = 0; tt < steps; ++tt) {
+        if (tt < d) {
+          p = sBest[tt * 16 + p];
+          sPath[tt] = sId[tt * 16 + p];
+        } else {
+          sPath[tt] = -1;
+        }
+      }
+    }
+    __syncwarp();
+    for (int tt = lane; tt < steps; tt += 32) path[slot0 + tt] = sPath[tt];
+  }
+}
+
+template <int R>
+cudaError_t launch_mma_t(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
+                         const void* pred, const void* succ, int B, int steps, int V, float* S, int32_t* path,
+                         cudaStream_t st, const int32_t* depths, int W, size_t smem) {
+  static unsigned done = 0;
+  if (!ensure_smem_attr(score_edges_mma_kernel<R>, kSmemBudget, &done)) return cudaErrorInvalidValue;
+  return launch_pdl(score_edges_mma_kernel<R>, dim3(B), dim3(32 * W), smem, st, nullptr, 0, cand, unary, z, anchors,
+                    static_cast<const __nv_bfloat16*>(pred), static_cast<const __nv_bfloat16*>(succ), steps, V, S,
+                    path, depths, device_error_word());
+}
+
+template <typename T, int R>
+cudaError_t launch_k16_t(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
+                         const void* pred, const void* succ, int B, int steps, int V, float* S, int32_t* path,
+                         cudaStream_t st, const int32_t* depths, int W, size_t smem) {
+  static unsigned done = 0;
+  if (!ensure_smem_attr(score_edges_k16_kernel<T, R>, kSmemBudget, &done)) return cudaErrorInvalidValue;
+  return launch_pdl(score_edges_k16_kernel<T, R>, dim3(B), dim3(32 * W), smem, st, nullptr, 0, cand, unary, z,
+                    anchors, static_cast<const T*>(pred), static_cast<const T*>(succ), steps, V, S, path, depths,
+                    device_error_word());
+}
+
+int launch_k16(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors, const void* pred,
+               const void* succ, int B, int steps, int R, int V, int dtype, float* S, int32_t* path,
+               cudaStream_t st, const int32_t* depths, int W, size_t smem) {
+  if (smem > static_cast<size_t>(kSmemBudget))
+    return fail(DFLASH2_ERR_INVALID_ARG, "score_edges: steps=%d needs %zu bytes of shared memory", steps, smem);
+  cudaError_t e = cudaErrorInvalidValue;
+#define DFL_K16(TT, RR)                                                                                      \
+  e = launch_k16_t<TT, RR>(cand, unary, z, anchors, pred, succ, B, steps, V, S, path, st, depths, W, smem)
+  if (dtype == DFLASH2_F32) {
+    if (R == 16) DFL_K16(float, 16); else DFL_K16(float, 32);
+  } else {
+    if (R == 16) DFL_K16(__nv_bfloat16, 16); else if (R == 32) DFL_K16(__nv_bfloat16, 32);
+    else DFL_K16(__nv_bfloat16, 64);
+  }
+#undef DFL_K16
+  return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "score_edges launch failed: %s", cudaGetErrorString(e));
+}
 
 #ifndef DFL_EDGE_WARP
 #define DFL_EDGE_WARP 1
@@ -355,6 +750,31 @@ size_t edges_smem(int steps, int K, int R, int lchunk) {
 int launch_score_edges(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
                        const void* pred, const void* succ, int B, int steps, int K, int R, int V, int dtype,
                        float* S, int32_t* path, cudaStream_t st, const int32_t* depths) {
+  if (K == 16 && dtype == DFLASH2_BF16 && (R == 32 || R == 64)) {
+    // tensor-core edge terms; W warps per block: every CTA resident at once at 32 warps per SM
+    // where B allows (a slot per warp at small B), down to 4 warps at large B
+    const int sms = sm_count();
+    int W = 16;
+    while (W > 4 && static_cast<long long>(B) * W > 32LL * sms) W >>= 1;
+    W = std::max(1, std::min(W, steps));
+    const size_t smem = static_cast<size_t>(steps) * (17 * sizeof(int) + 16);
+    const cudaError_t e =
+        R == 32 ? launch_mma_t<32>(cand, unary, z, anchors, pred, succ, B, steps, V, S, path, st, depths, W, smem)
+                : launch_mma_t<64>(cand, unary, z, anchors, pred, succ, B, steps, V, S, path, st, depths, W, smem);
+    return e == cudaSuccess ? DFLASH2_OK
+                            : fail(DFLASH2_ERR_CUDA, "score_edges launch failed: %s", cudaGetErrorString(e));
+  }
+  // (the shapes whose registers fit without spills: bf16 rows up to R = 64, f32 up to R = 32)
+  if (K == 16 && (R == 16 || R == 32 || (R == 64 && dtype == DFLASH2_BF16))) {
+    // W warps per block: as many as keep every CTA resident in one wave at 16 warps per SM (a
+    // slot per warp at small B, for latency), down to 2 at large B (pipelined slots per warp)
+    const int sms = sm_count();
+    int W = 16;
+    while (W > 2 && static_cast<long long>(B) * W > 16LL * sms) W >>= 1;
+    W = std::max(1, std::min(W, steps));
+    const size_t smem = sizeof(float) * (static_cast<size_t>(steps) * 256 + static_cast<size_t>(W) * 16 * (R + 8));
+    return launch_k16(cand, unary, z, anchors, pred, succ, B, steps, R, V, dtype, S, path, st, depths, W, smem);
+  }
   {
     // warp-per-slot kernel when its scores and at least a few warps' rows fit in shared memory
     const size_t s_floats = (static_cast<size_t>(steps) * K * K + 3) & ~static_cast<size_t>(3);

@@ -100,44 +100,58 @@ def compare_walk(gpu_path, ref_S, ref_pos, cand, tol):
     return near, checked
 
 
-def compare_path_end_to_end(gpu_path, ref, logits_tol, S_tol):
+def _edge_scores(ids, prev_id, z_row, pred_book, succ_book):
+    """Oracle edge term sum_r pred[prev, r] * z[r] * succ[u, r] for each id u (float64)."""
+    w = np.asarray(pred_book[int(prev_id)], dtype=np.float64) * np.asarray(z_row, dtype=np.float64)
+    rows = np.stack([np.asarray(succ_book[int(u)], dtype=np.float64) for u in ids])
+    return rows @ w
+
+
+def path_parity(gpu_path, ref, anchors, pred_book, succ_book, logits_tol, S_tol, strict=True):
     """The GPU's path against the oracle's own walk (``ref`` = the oracle's block_tail dict), each
-    on its own candidates. Slot by slot the ids must match while the oracle's head row of that
-    slot has a K-th margin above 4 * logits_tol and its walk margin exceeds 4 * S_tol. At the
-    first slot that is a near-tie either way, the GPU's id g must be a valid choice: if g is an
-    oracle candidate, its oracle score is within 4 * S_tol of the best; otherwise the row must be
-    a head near-tie (only then may the candidate sets differ). That slot ends the block's strict
-    comparison. Returns (near_tie_blocks, slots_checked)."""
+    on its own candidates, under the stated margins.
+
+    A slot is decided when the oracle's choice c* is certainly in any top-K the tolerance allows
+    (its logit exceeds the (K+1)-th by more than 4 * logits_tol) and its oracle score
+    unary + edge beats, by more than 4 * S_tol, every other id that may be a candidate (logit at
+    least the K-th minus 4 * logits_tol), scored with the same predecessor. Decided slots must give
+    the oracle's id; the first undecided slot of a block must give a valid choice (an id that may
+    be a candidate, scoring within 4 * S_tol of c*) and ends the block's comparison (predecessors
+    may differ after it). Returns dict(near_tie_blocks, strict_slots, mismatches); with
+    strict=True a mismatch raises instead of being counted."""
     gpu_path = np.asarray(gpu_path)
-    cand, S, pos, logits = ref["cand"], ref["S"], ref["pos"], ref["logits"]
-    B, steps, K = cand.shape
-    near, checked = 0, 0
+    logits, z, path = ref["logits"], ref["z"], ref["path"]
+    B, steps = path.shape
+    K = ref["cand"].shape[-1]
+    out = dict(near_tie_blocks=0, strict_slots=0, mismatches=0)
     for b in range(B):
-        p = 0
+        prev = int(anchors[b])
         for l in range(steps):
-            row_logits = logits[b, l]
-            srt = -np.sort(-row_logits)
-            head_margin = srt[K - 1] - srt[K] if row_logits.size > K else np.inf
-            row = S[b, l, p]
-            best = int(pos[b, l])
-            second = np.max(np.delete(row, best)) if K > 1 else -np.inf
+            L = np.asarray(logits[b, l], dtype=np.float64)
+            srt = -np.sort(-L)
+            vK, vK1 = srt[K - 1], (srt[K] if L.size > K else -np.inf)
+            possible = np.flatnonzero(L >= vK - 4 * logits_tol)
+            score = L[possible] + _edge_scores(possible, prev, z[b, l], pred_book, succ_book)
+            best_id = int(path[b, l])
+            best = float(score[possible == best_id][0])
+            others = score[possible != best_id]
+            runner_up = float(np.max(others)) if others.size else -np.inf
             g = int(gpu_path[b, l])
-            if head_margin <= 4 * logits_tol or row[best] - second <= 4 * S_tol:
-                near += 1
-                hit = np.flatnonzero(cand[b, l] == g)
-                if hit.size:
-                    assert row[hit[0]] >= row[best] - 4 * S_tol, \
-                        f"block {b} slot {l}: near-tie choice {g} scores {row[hit[0]]:.4g}, best {row[best]:.4g}"
-                else:
-                    assert head_margin <= 4 * logits_tol, \
-                        f"block {b} slot {l}: GPU id {g} is not an oracle candidate of a decided row"
-                    assert row_logits[g] >= srt[K - 1] - 4 * logits_tol, \
-                        f"block {b} slot {l}: GPU id {g} lies far below the oracle's K-th logit"
+            decided = L[best_id] > vK1 + 4 * logits_tol and best - runner_up > 4 * S_tol
+            if not decided:
+                out["near_tie_blocks"] += 1
+                ok = g in set(possible.tolist()) and float(score[possible == g][0]) >= best - 4 * S_tol
+                if not ok:
+                    out["mismatches"] += 1
+                    assert not strict, f"block {b} slot {l}: near-tie choice {g} is not a valid candidate/score"
                 break
-            assert g == int(ref["path"][b, l]), f"block {b} slot {l}: {g} != {int(ref['path'][b, l])} (end to end)"
-            checked += 1
-            p = best
-    return near, checked
+            if g != best_id:
+                out["mismatches"] += 1
+                assert not strict, f"block {b} slot {l}: {g} != {best_id} (end to end, decided slot)"
+                break
+            out["strict_slots"] += 1
+            prev = best_id
+    return out
 
 
 REPORT = []

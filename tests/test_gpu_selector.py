@@ -17,7 +17,10 @@ def torch():
 
 def _case(seed, B, steps, K, R, V, dtype="bf16", book_std=0.5):
     rng = np.random.default_rng(seed)
-    cand = np.stack([np.stack([rng.choice(V, size=K, replace=False) for _ in range(steps)]) for _ in range(B)])
+    cand = rng.integers(0, V, size=(B, steps, K))
+    for idx in np.ndindex(B, steps):   # distinct ids within a slot (a top-K list never repeats one)
+        if len(set(cand[idx].tolist())) < K:
+            cand[idx] = rng.choice(V, size=K, replace=False)
     cand = cand.astype(np.int32)
     unary = np.sort(rng.standard_normal((B, steps, K)).astype(np.float32), axis=-1)[..., ::-1].copy()
     z = rng.standard_normal((B, steps, R)).astype(np.float32)
@@ -31,7 +34,9 @@ def _case(seed, B, steps, K, R, V, dtype="bf16", book_std=0.5):
 @pytest.mark.parametrize("B,steps,K,R,V", [(1, 15, 16, 64, 5000), (33, 15, 16, 64, 248320), (7, 7, 16, 16, 4096),
                                            (5, 4, 3, 8, 50), (3, 31, 32, 128, 1000),
                                            (4, 15, 16, 128, 3000),   # K = 16 tiles with R = 128
-                                           (200, 15, 16, 64, 9000)])  # more blocks than SMs
+                                           (200, 15, 16, 64, 9000),   # more blocks than SMs
+                                           (700, 15, 16, 64, 248320),  # two warps per block, pipelined
+                                           (3, 63, 16, 32, 2000)])     # the longest block
 def test_score_edges_and_walk(torch, dtype, B, steps, K, R, V):
     import dflash2_block_drafter_gb300 as d
     from dflash2_block_drafter_gb300.tail import to_device
@@ -87,6 +92,24 @@ def test_bad_index_sets_error_word(torch):
                           to_device(succ))
     assert d.dflash2_poll_error() == -6
     assert d.dflash2_poll_error() == 0   # cleared
+
+
+@pytest.mark.parametrize("dtype,R", [("bf16", 64), ("f32", 16)])
+def test_bad_index_sets_error_word_k16(torch, dtype, R):
+    """The K = 16 kernel: an id outside [0, V) in a successor and in a predecessor position sets
+    DFLASH2_ERR_BAD_INDEX and reads as a zero row (its edge term is 0: S equals unary there)."""
+    import dflash2_block_drafter_gb300 as d
+    from dflash2_block_drafter_gb300.tail import to_device
+    cand, unary, z, anchors, pred, succ = _case(13, 3, 6, 16, R, 500, dtype)
+    cand[1, 2, 5] = 500       # == V
+    cand[2, 0, 7] = -1        # a predecessor of slot 1
+    S, _ = d.dflash2_score_edges(to_device(cand), to_device(unary), to_device(z), to_device(anchors),
+                                 to_device(pred), to_device(succ))
+    assert d.dflash2_poll_error() == -6
+    assert d.dflash2_poll_error() == 0
+    S = S.cpu().numpy()
+    np.testing.assert_array_equal(S[1, 2, :, 5], np.full(16, unary[1, 2, 5], np.float32))
+    np.testing.assert_array_equal(S[2, 1, 7, :], unary[2, 1, :])
 
 
 def test_misaligned_unary_and_S_take_the_scalar_path(torch):
