@@ -30,6 +30,8 @@ import numpy as np  # noqa: E402
 WORKLOADS = {
     # name: (config index, B)
     "full-tail-B64": (4, 64),
+    # the same with seeded per-block depths: only the drafted rows reach the head and the selector
+    "full-tail-B64-ragged": (4, 64),
     "full-tail-B8": (4, 8),
     "selector-B1": (2, 1),
     "selector-B32": (3, 32),
@@ -39,6 +41,12 @@ WORKLOADS = {
     "conv-chain-B1": (1, 1),
 }
 METRIC = "draft blocks/sec (G=16, hidden 5120) at 1 GB300; % of HBM roofline per kernel"
+RAGGED = {"full-tail-B64-ragged"}
+
+
+def ragged_depths(B, steps, seed=20261202):
+    """Requested draft depths of a ragged workload: seeded, uniform over [1, steps]."""
+    return np.random.default_rng(seed).integers(1, steps + 1, size=B).tolist()
 
 
 def peaks():
@@ -318,8 +326,9 @@ def oracle_cores():
     return len(os.sched_getaffinity(0))
 
 
-def oracle_block_tail(wl, blocks):
-    """The oracle's full tail on the listed blocks of the workload (blocks never interact)."""
+def oracle_block_tail(wl, blocks, depths=None):
+    """The oracle's full tail on the listed blocks of the workload (blocks never interact); with
+    `depths` (per block of the workload) the ragged tail, drafted rows only."""
     from oracle import dflash2_oracle as O
     from synth import inputs as I
 
@@ -340,17 +349,21 @@ def oracle_block_tail(wl, blocks):
         z = O.hidden_projection(h, I.to_f64(wl.w_proj))
         S = O.score_edges(cand, unary, z, wl.anchors[blocks], I.f64_view(wl.pred_book), I.f64_view(wl.succ_book))
         return O.select_path(S, cand)
+    if depths is not None:
+        return O.block_tail_ragged(I.to_f64(wl.x0)[blocks], sites, I.to_f64(wl.final_norm_w), wl.eps, wl.gs,
+                                   I.f64_view(wl.w_head), wl.bias, I.to_f64(wl.w_proj), I.f64_view(wl.pred_book),
+                                   I.f64_view(wl.succ_book), wl.anchors[blocks], wl.K, [depths[b] for b in blocks])
     return O.block_tail(I.to_f64(wl.x0)[blocks], sites, I.to_f64(wl.final_norm_w), wl.eps, wl.gs,
                         I.f64_view(wl.w_head), wl.bias, I.to_f64(wl.w_proj), I.f64_view(wl.pred_book),
                         I.f64_view(wl.succ_book), wl.anchors[blocks], wl.K)
 
 
-def time_oracle(wl, n_blocks, repeats):
+def time_oracle(wl, n_blocks, repeats, depths=None):
     times = []
     for r in range(repeats):
         blocks = [(r * n_blocks + i) % wl.B for i in range(n_blocks)]
         t0 = time.perf_counter()
-        oracle_block_tail(wl, blocks)
+        oracle_block_tail(wl, blocks, depths)
         times.append(time.perf_counter() - t0)
     return times
 
@@ -362,10 +375,11 @@ def reference_arm(args, wl_name):
     from synth import inputs as I
     cfg, B = WORKLOADS[wl_name]
     wl = I.make_config(cfg, B=B)
+    depths = ragged_depths(B, wl.steps) if wl_name in RAGGED else None
     n_blocks = args.ref_blocks
     for _ in range(args.warmup):
-        time_oracle(wl, n_blocks, 1)
-    times = time_oracle(wl, n_blocks, args.steps)
+        time_oracle(wl, n_blocks, 1, depths)
+    times = time_oracle(wl, n_blocks, args.steps, depths)
     total = sum(times)
     value = n_blocks * args.steps / total
     cores = oracle_cores()
@@ -414,9 +428,15 @@ def our_arm(args, wl_name):
     anchors = to_device(wl.anchors, dev) if wl.anchors is not None else None
     h_in = to_device(wl.h, dev) if (wl.h is not None and not wl.sites) else None
     stream = torch.cuda.current_stream()
+    rag = None
+    if wl_name in RAGGED:
+        rag = d.dflash2_ragged_offsets(ragged_depths(B, wl.steps), wl.G, dev)
+    M = rag[1] if rag is not None else B * wl.steps
 
     def step():
-        if full_tail:
+        if full_tail and rag is not None:
+            run.full_ragged(x0, ys, anchors, *rag)
+        elif full_tail:
             run.full(x0, ys, anchors)
         elif wl.sites:
             run.conv_chain(x0, ys, emit_h=False)
@@ -430,17 +450,24 @@ def our_arm(args, wl_name):
     h_src = run.h if (wl.sites and run.with_selector) else h_in
 
     # One step = conv chain -> head (the dominant kernel, timed on its own) -> edge scores + walk.
+    if rag is not None and d.dflash2_head_topk_workspace_bytes(M, wl.H, wl.V, wl.K, wl.R) > run.head_ws.numel():
+        run.head_ws = torch.empty(d.dflash2_head_topk_workspace_bytes(M, wl.H, wl.V, wl.K, wl.R), dtype=torch.uint8,
+                                  device=dev)
+
     def part_conv():
         if wl.sites:
-            run.conv_chain(x0, ys, emit_h=run.with_selector)
+            run.conv_chain(x0, ys, emit_h=run.with_selector, ragged=rag)
 
     def part_head():
         if run.with_selector:
-            d.dflash2_head_topk(h_src.view(Bh * wl.steps, wl.H), run.w_head, wl.K, bias=run.bias, w_proj=run.w_proj,
-                                cand=run.cand, unary=run.unary, z=run.z, workspace=run.head_ws)
+            d.dflash2_head_topk(h_src.view(-1, wl.H)[:M], run.w_head, wl.K, bias=run.bias, w_proj=run.w_proj,
+                                cand=run.cand[:M], unary=run.unary[:M], z=run.z[:M], workspace=run.head_ws)
 
     def part_select():
-        if run.with_selector:
+        if run.with_selector and rag is not None:
+            d.dflash2_score_edges_ragged(run.cand[:M], run.unary[:M], run.z[:M], anchors, run.pred, run.succ, rag[0],
+                                         wl.steps, S=run.S.view(-1, wl.K, wl.K)[:M], path=run.path)
+        elif run.with_selector:
             d.dflash2_score_edges(run.cand.view(Bh, wl.steps, wl.K), run.unary.view(Bh, wl.steps, wl.K),
                                   run.z.view(Bh, wl.steps, wl.R), anchors, run.pred, run.succ, S=run.S, path=run.path)
 
@@ -500,7 +527,7 @@ def our_arm(args, wl_name):
     e2e_ms = []
     # the full tail with host inputs as one CUDA graph: the copies are graph nodes on a branch of
     # their own, each site's finish waiting only for its own sublayer output
-    e2e_graph = run.capture(run.full_from_host, h_x0, h_ys, h_anchors, x0, ys, anchors) \
+    e2e_graph = run.capture(run.full_from_host, h_x0, h_ys, h_anchors, x0, ys, anchors, ragged=rag) \
         if (full_tail and args.graph) else None
     for i in range(args.warmup + args.steps):
         flush.zero_()
@@ -511,7 +538,7 @@ def our_arm(args, wl_name):
             e2e_graph.replay()
         elif full_tail:
             # inputs copied on a copy stream; each site waits only for its own sublayer output
-            run.full_from_host(h_x0, h_ys, h_anchors, x0, ys, anchors)
+            run.full_from_host(h_x0, h_ys, h_anchors, x0, ys, anchors, ragged=rag)
         else:
             if h_x0 is not None:
                 x0.copy_(h_x0, non_blocking=True)
@@ -534,7 +561,6 @@ def our_arm(args, wl_name):
     e2e_value, _, e2e_total = aggregate_throughput(B * args.steps, e2e_total, device=dev)
 
     pk = peaks()
-    M = B * wl.steps
     roofline = None
     if head_ms:
         # the head runs in ~1.4 ms windows timed on their own: the burst tensor peak applies
@@ -558,8 +584,9 @@ def our_arm(args, wl_name):
                         "avg_launch_ms": head_avg_s * 1e3}
         roofline.update(head_traffic(wl_name))
 
-    calls = per_call_timing(d, run, wl, x0, ys, anchors, h_in, stream, flush) if rank == 0 else None
-    targets = kernel_targets(d, run, wl, calls, stream, flush, dev) if (rank == 0 and full_tail) else None
+    calls = per_call_timing(d, run, wl, x0, ys, anchors, h_in, stream, flush) if (rank == 0 and rag is None) else None
+    targets = kernel_targets(d, run, wl, calls, stream, flush, dev) if (rank == 0 and full_tail and rag is None) \
+        else None
     launches = run.launches_per_pass(conv=bool(wl.sites), selector=run.with_selector,
                                      emit_h=run.with_selector)
     line = {
@@ -569,8 +596,9 @@ def our_arm(args, wl_name):
         "config": {"workload": wl_name, "blocks_per_gpu": B, "G": wl.G, "hidden": wl.H, "conv_sites": len(wl.sites),
                    "vocab": wl.V or None, "top_k": wl.K or None, "rank": wl.R or None,
                    "parallelism": f"dp{world} (independent blocks, no collective)",
-                   "l2": "flushed between timed steps (256 MB write) and head weight 2.54 GB > L2"},
-        "rows_per_s": value * (wl.steps if run.with_selector else wl.G),
+                   "l2": "flushed between timed steps (256 MB write) and head weight 2.54 GB > L2",
+                   "head_rows": M, "depths": "seeded uniform in [1, 15]" if rag is not None else "all 15"},
+        "rows_per_s": value * (M / B if run.with_selector else wl.G),
         "head_ms": statistics.mean(head_ms) if head_ms else None,
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": "blocks/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -584,12 +612,12 @@ def our_arm(args, wl_name):
         n = min(args.cpu_blocks, B)
         blocks = list(range(n))
         t0 = time.perf_counter()
-        ref = oracle_block_tail(wl, blocks)
+        ref = oracle_block_tail(wl, blocks, ragged_depths(B, wl.steps) if rag is not None else None)
         t_cpu = time.perf_counter() - t0
         line["cpu_baseline"] = {"value": n / t_cpu, "unit": "blocks/s", "cores": oracle_cores(),
                                 "kind": "oracle",
                                 "sample": f"blocks 0..{n - 1} of the {wl_name} workload, float64 numpy, one run"}
-        if run.with_selector and isinstance(ref, dict):
+        if run.with_selector and isinstance(ref, dict) and rag is None:
             line["parity"] = parity_counts(run, wl, blocks, ref)
     if rank == 0:
         print(json.dumps(line), flush=True)

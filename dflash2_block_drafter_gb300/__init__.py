@@ -22,6 +22,7 @@ __all__ = [
     "dflash2_conv_prepare", "dflash2_conv_finish",
     "dflash2_head_topk_workspace_bytes", "dflash2_head_topk", "dflash2_score_edges",
     "dflash2_select_path", "dflash2_selftest_bounded_wait", "dflash2_head_topk_noalloc", "dflash2_head_topk_vocab", "dflash2_score_edges_depths", "dflash2_select_path_depths",
+    "dflash2_ragged_offsets", "dflash2_conv_finish_ragged", "dflash2_score_edges_ragged",
     "DTYPE_CODES",
 ]
 
@@ -56,6 +57,10 @@ _SIGNATURES = {
     "dflash2_select_path_depths": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
     "dflash2_head_topk_vocab": (_i, [_vp, _i, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz,
                                      _vp]),
+    "dflash2_conv_finish_ragged": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _f, _vp, _i, _vp, _i,
+                                        _vp]),
+    "dflash2_score_edges_ragged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp,
+                                        _vp]),
 }
 
 
@@ -335,3 +340,62 @@ def dflash2_select_path_depths(S, cand, depths, path=None, stream=None):
                                                 _dev(depths, "depths", torch.int32), B, steps, K,
                                                 _dev(path, "path", torch.int32), _stream(stream)))
     return path
+
+
+def dflash2_ragged_offsets(depths, G, device="cuda"):
+    """Row offsets of a ragged batch from the per-block requested depths (host ints): block b
+    drafts d_b = min(G - 1, max(1, depths[b])) tokens (dflash2.ts blockColumns), so its head rows
+    are [offsets[b], offsets[b + 1]). Returns (offsets int32 [B + 1] on `device`, m_rows). Host-side
+    scheduling metadata: the row count sizes the head call."""
+    d = [min(G - 1, max(1, int(x))) for x in depths]
+    off = [0]
+    for x in d:
+        off.append(off[-1] + x)
+    return torch.tensor(off, dtype=torch.int32, device=device), off[-1]
+
+
+def dflash2_conv_finish_ragged(y, coef1, base, group_size, row_offsets, m_rows, next_norm_w, residual=None, out=None,
+                               eps=1e-6, next_n=None, next_row0=1, stream=None, taps=2):
+    """dflash2_conv_finish whose next norm is written only for each block's drafted rows, packed at
+    row_offsets (next_n [m_rows, H]). Returns (out, next_n)."""
+    B, G, H = y.shape
+    dt = y.dtype
+    if row_offsets.numel() != B + 1:
+        raise ValueError(f"row_offsets holds {row_offsets.numel()} entries, expected B + 1 = {B + 1}")
+    out = torch.empty_like(y) if out is None else out
+    if next_n is None:
+        next_n = torch.empty((m_rows, H), dtype=dt, device=y.device)
+    if next_n.numel() < m_rows * H:
+        raise ValueError(f"next_n holds {next_n.numel()} elements, fewer than m_rows * H = {m_rows * H}")
+    _check(library().dflash2_conv_finish_ragged(
+        _dev(y, "y", dt), _dev(coef1, "coef1", dt), _dev(base, "base", torch.float32), B, G, H, group_size, taps,
+        _code(y), _dev(residual, "residual", dt, True), _dev(out, "out", dt), _dev(next_norm_w, "next_norm_w", dt),
+        eps, _dev(next_n, "next_n", dt), next_row0, _dev(row_offsets, "row_offsets", torch.int32), m_rows,
+        _stream(stream)))
+    return out, next_n
+
+
+def dflash2_score_edges_ragged(cand, unary, z, anchors, pred_book, succ_book, row_offsets, steps, want_S=True, S=None,
+                               path=None, stream=None):
+    """Edge scores + the greedy walk of a ragged batch: cand/unary [m_rows, K], z [m_rows, R], block b's
+    slots at rows row_offsets[b] .. row_offsets[b + 1] - 1. Returns (S [m_rows, K, K] or None,
+    path [B, steps] with -1 past each block's rows)."""
+    m_rows, K = cand.shape
+    R = z.shape[-1]
+    V = pred_book.shape[0]
+    B = row_offsets.numel() - 1
+    dev = cand.device
+    if unary.numel() < m_rows * K or z.numel() < m_rows * R:
+        raise ValueError("unary and z must hold m_rows rows")
+    if want_S and S is None:
+        S = torch.empty((m_rows, K, K), dtype=torch.float32, device=dev)
+    path = torch.empty((B, steps), dtype=torch.int32, device=dev) if path is None else path
+    if path.numel() < B * steps or (S is not None and S.numel() < m_rows * K * K):
+        raise ValueError("path must hold B * steps entries and S m_rows * K * K")
+    _check(library().dflash2_score_edges_ragged(
+        _dev(cand, "cand", torch.int32), _dev(unary, "unary", torch.float32), _dev(z, "z", torch.float32),
+        _dev(anchors, "anchors", torch.int32), _dev(pred_book, "pred_book", pred_book.dtype),
+        _dev(succ_book, "succ_book", pred_book.dtype), _dev(row_offsets, "row_offsets", torch.int32), B, steps, K, R,
+        V, m_rows, _code(pred_book), _dev(S, "S", torch.float32, True), _dev(path, "path", torch.int32),
+        _stream(stream)))
+    return S, path

@@ -180,6 +180,26 @@ int dflash2_conv_finish(const void* y, const void* coef1, const float* base, int
                            static_cast<cudaStream_t>(stream));
 }
 
+int dflash2_conv_finish_ragged(const void* y, const void* coef1, const float* base, int B, int G, int H,
+                               int group_size, int taps, int dtype, const void* residual, void* out,
+                               const void* next_norm_w, float eps, void* next_n, int next_row0,
+                               const int32_t* row_offsets, int m_rows, void* stream) {
+  REQUIRE(row_offsets != nullptr, "row_offsets is NULL (use dflash2_conv_finish for dense rows)");
+  REQUIRE(next_norm_w != nullptr && next_n != nullptr, "the ragged finish needs next_norm_w and next_n");
+  REQUIRE(m_rows >= 1, "m_rows=%d must be >= 1", m_rows);
+  int rc = check_conv_shape(B, G, H, group_size, taps, dtype);
+  if (rc != DFLASH2_OK) return rc;
+  REQUIRE(y && coef1 && base && out, "a required pointer is NULL");
+  REQUIRE(aligned16(y) && aligned16(base) && aligned16(out) && (!residual || aligned16(residual)) &&
+              aligned16(next_norm_w) && aligned16(next_n),
+          "y, base, residual, out, next_norm_w and next_n must be 16-byte aligned");
+  REQUIRE(next_row0 >= 0 && next_row0 < G, "next_row0=%d must be in [0, G)", next_row0);
+  REQUIRE(H / 8 <= 1024, "H=%d: the fused norm needs H <= 8192", H);
+  const ConvShape s{B, G, H, group_size, H / group_size, dtype};
+  return launch_conv_side1(s, y, coef1, base, residual, out, next_norm_w, eps, next_n, next_row0,
+                           static_cast<cudaStream_t>(stream), row_offsets, m_rows);
+}
+
 size_t dflash2_head_topk_workspace_bytes(int M, int H, int V, int K, int R) {
   if (M < 1 || H < 64 || V < 1 || K < 1 || R < 0) return 0;
   return head_workspace(M, V, K, R, sm_count());
@@ -264,6 +284,23 @@ int dflash2_score_edges_depths(const int32_t* cand, const float* unary, const fl
   REQUIRE(aligned16(z) && aligned16(pred_book) && aligned16(succ_book), "z and the codebooks must be 16-byte aligned");
   return launch_score_edges(cand, unary, z, anchors, pred_book, succ_book, B, steps, K, R, V, dtype, S, path,
                             static_cast<cudaStream_t>(stream), depths);
+}
+
+int dflash2_score_edges_ragged(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
+                               const void* pred_book, const void* succ_book, const int32_t* row_offsets, int B,
+                               int steps, int K, int R, int V, int m_rows, int dtype, float* S, int32_t* path,
+                               void* stream) {
+  REQUIRE(row_offsets != nullptr, "row_offsets is NULL (use dflash2_score_edges for dense blocks)");
+  REQUIRE(dtype == DFLASH2_BF16 || dtype == DFLASH2_F32, "dtype=%d is not DFLASH2_BF16 or DFLASH2_F32", dtype);
+  REQUIRE(B >= 1 && steps >= 1 && steps <= 63, "B=%d, steps=%d: need B >= 1 and 1 <= steps <= 63", B, steps);
+  REQUIRE(m_rows >= 1, "m_rows=%d must be >= 1", m_rows);
+  REQUIRE(K == 16 && (R == 16 || R == 32 || (R == 64 && dtype == DFLASH2_BF16)),
+          "ragged rows need K = 16 and R in {16, 32, 64} (bf16) or {16, 32} (f32); got K=%d, R=%d", K, R);
+  REQUIRE(V >= 1, "V=%d must be >= 1", V);
+  REQUIRE(cand && unary && z && anchors && pred_book && succ_book && path, "a required pointer is NULL");
+  REQUIRE(aligned16(z) && aligned16(pred_book) && aligned16(succ_book), "z and the codebooks must be 16-byte aligned");
+  return launch_score_edges(cand, unary, z, anchors, pred_book, succ_book, B, steps, K, R, V, dtype, S, path,
+                            static_cast<cudaStream_t>(stream), nullptr, row_offsets, m_rows);
 }
 
 int dflash2_select_path_depths(const float* S, const int32_t* cand, const int32_t* depths, int B, int steps, int K,

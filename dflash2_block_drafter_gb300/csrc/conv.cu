@@ -117,10 +117,29 @@ __host__ __device__ inline int vectors_per_cta(int G) {
 #endif
 constexpr int kNormRows = DFL_NORM_ROWS;
 
+// Output rows of block b: rows_out dense rows at b * rows_out, or (row_off given) the
+// row_off[b + 1] - row_off[b] rows at row_off[b] of an output of m_out rows. A span that is not
+// inside [0, m_out), or that holds more rows than the block, records DFLASH2_ERR_INVALID_ARG (when
+// err is given) and writes nothing.
+struct RowSpan {
+  size_t first;
+  int n;
+};
+__device__ __forceinline__ RowSpan out_rows(const int32_t* row_off, int b, int rows_out, int m_out, int* err) {
+  if (row_off == nullptr) return RowSpan{static_cast<size_t>(b) * rows_out, rows_out};
+  const int lo = row_off[b];
+  const int n = row_off[b + 1] - lo;
+  if (lo < 0 || n < 0 || n > rows_out || lo > m_out - n) {
+    if (err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_INVALID_ARG));
+    return RowSpan{0, 0};
+  }
+  return RowSpan{static_cast<size_t>(lo), n};
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kNormThreads)
     rms_rows_kernel(const T* __restrict__ x, const T* __restrict__ w, float eps, T* __restrict__ n, int G, int row0,
-                    int H, int total_rows) {
+                    int H, int total_rows, const int32_t* __restrict__ row_off, int m_out, int* err) {
   __shared__ float warp_ss[kNormRows][32];
   __shared__ float row_r[kNormRows];
   pdl_trigger();
@@ -169,11 +188,15 @@ __global__ void __launch_bounds__(kNormThreads)
   for (int k = 0; k < kNormRows; ++k) {
     const int o = blockIdx.x * kNormRows + k;
     if (o >= total_rows) break;
+    const int b = o / rows_out;
+    const int i = o % rows_out;
+    const RowSpan span = out_rows(row_off, b, rows_out, m_out, (threadIdx.x == 0 && i == 0) ? err : nullptr);
+    if (i >= span.n) continue;
     const float r = row_r[k];
     float v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = f[k][i] * r * g[i];
-    store8(n + static_cast<size_t>(o) * H + c, v);
+    for (int j = 0; j < 8; ++j) v[j] = f[k][j] * r * g[j];
+    store8(n + (span.first + i) * H + c, v);
   }
 }
 
@@ -479,7 +502,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
     conv_finish_norm_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmR,
                             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmW, T* out, T* next_n, float eps, int G, int H,
-                            int gs, int spc, int csize, int has_res, int next_row0, int stage_bytes, int* err) {
+                            int gs, int spc, int csize, int has_res, int next_row0, int stage_bytes,
+                            const int32_t* __restrict__ row_off, int m_out, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int es = static_cast<int>(sizeof(T));
@@ -608,11 +632,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   cluster_sync_all();  // every partial has arrived in every CTA
 
   if (warp < kStreamConsumers && *abort_flag == 0) {
-    // ---- pass 2: n = x * r * w for rows next_row0 .. G-1
+    // ---- pass 2: n = x * r * w for rows next_row0 .. G-1 (with row_off: the first
+    // row_off[b + 1] - row_off[b] of them, at rows row_off[b] + ...)
     const int v = lane;
     const int rows_out = G - next_row0;
+    const RowSpan span = out_rows(row_off, b, rows_out, m_out, warp == 0 && lane == 0 && rank == 0 ? err : nullptr);
     for (int t = warp; t < G; t += kStreamConsumers) {
-      if (t < next_row0) continue;
+      if (t < next_row0 || t - next_row0 >= span.n) continue;
       float tot = 0.f;
       for (int q = 0; q < csize; ++q) tot += ss_all[q * G + t];
       const float r = rsqrtf(tot / static_cast<float>(H) + eps);
@@ -631,7 +657,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
           o[2 * i] = y2.x;
           o[2 * i + 1] = y2.y;
         }
-        store8(next_n + (static_cast<size_t>(b) * rows_out + (t - next_row0)) * H + (strip0 + s) * kStreamSW + v * 8, o);
+        store8(next_n + (span.first + (t - next_row0)) * H + (strip0 + s) * kStreamSW + v * 8, o);
       }
     }
   }
@@ -927,23 +953,23 @@ size_t conv_prepare_workspace(const ConvShape& s, int sms) {
 
 template <typename T>
 static int rms_rows_typed(const void* x, const void* w, float eps, void* n, int B, int G, int row0, int H,
-                          cudaStream_t st) {
+                          cudaStream_t st, const int32_t* row_off, int m_out) {
   const int threads = std::min(kNormThreads, ((H / 8 + 31) / 32) * 32);
   const int total = B * (G - row0);
   const cudaError_t e = launch_pdl(rms_rows_kernel<T>, dim3((total + kNormRows - 1) / kNormRows), dim3(threads), 0,
                                    st, nullptr, 0, static_cast<const T*>(x), static_cast<const T*>(w), eps,
-                                   static_cast<T*>(n), G, row0, H, total);
+                                   static_cast<T*>(n), G, row0, H, total, row_off, m_out, device_error_word());
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "rmsnorm launch failed: %s", cudaGetErrorString(e));
 }
 
 int launch_rmsnorm_rows(const void* x, const void* w, float eps, void* n, int B, int G, int row0, int H, int dtype,
-                        cudaStream_t st) {
-  if (dtype == DFLASH2_F32) return rms_rows_typed<float>(x, w, eps, n, B, G, row0, H, st);
-  return rms_rows_typed<__nv_bfloat16>(x, w, eps, n, B, G, row0, H, st);
+                        cudaStream_t st, const int32_t* row_off, int m_out) {
+  if (dtype == DFLASH2_F32) return rms_rows_typed<float>(x, w, eps, n, B, G, row0, H, st, row_off, m_out);
+  return rms_rows_typed<__nv_bfloat16>(x, w, eps, n, B, G, row0, H, st, row_off, m_out);
 }
 
 int launch_rmsnorm(const void* x, const void* w, float eps, void* n, int rows, int H, int dtype, cudaStream_t st) {
-  return launch_rmsnorm_rows(x, w, eps, n, rows, 1, 0, H, dtype, st);
+  return launch_rmsnorm_rows(x, w, eps, n, rows, 1, 0, H, dtype, st, nullptr, 0);
 }
 
 #ifndef DFL_STREAM0
@@ -1094,7 +1120,7 @@ static int finish_norm_cluster(const ConvShape& s) {
 template <typename T>
 static int launch_finish_norm(const ConvShape& s, int csize, const void* y, const void* coef1, const float* base,
                               const void* residual, void* out, const void* next_w, float eps, void* next_n,
-                              int next_row0, cudaStream_t st) {
+                              int next_row0, cudaStream_t st, const int32_t* row_off, int m_out) {
   const int dt = s.dtype;
   const int es = static_cast<int>(sizeof(T));
   const uint64_t rows = static_cast<uint64_t>(s.B) * s.G;
@@ -1129,7 +1155,7 @@ static int launch_finish_norm(const ConvShape& s, int csize, const void* y, cons
   const cudaError_t e = launch_pdl(conv_finish_norm_kernel<T>, dim3(s.B * csize), dim3(kStreamThreads), smem, st, cl, 1,
                                    mY, mR, mC, mB, mW, static_cast<T*>(out), static_cast<T*>(next_n), eps, s.G, s.H,
                                    s.gs, spc, csize, residual != nullptr ? 1 : 0, next_row0,
-                                   finish_norm_stage_bytes(s), device_error_word());
+                                   finish_norm_stage_bytes(s), row_off, m_out, device_error_word());
   return e == cudaSuccess ? DFLASH2_OK
                           : fail(DFLASH2_ERR_CUDA, "finish + norm launch failed: %s", cudaGetErrorString(e));
 }
@@ -1139,19 +1165,21 @@ static int launch_finish_norm(const ConvShape& s, int csize, const void* y, cons
 #endif
 
 int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, const float* base, const void* residual,
-                      void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st) {
+                      void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st,
+                      const int32_t* row_off, int m_out) {
   const int csize = (DFL_FINISH_NORM && next_n != nullptr) ? finish_norm_cluster(s) : 0;
   if (csize > 0)
     return s.dtype == DFLASH2_F32
-               ? launch_finish_norm<float>(s, csize, y, coef1, base, residual, out, next_w, eps, next_n, next_row0, st)
+               ? launch_finish_norm<float>(s, csize, y, coef1, base, residual, out, next_w, eps, next_n, next_row0, st,
+                                           row_off, m_out)
                : launch_finish_norm<__nv_bfloat16>(s, csize, y, coef1, base, residual, out, next_w, eps, next_n,
-                                                   next_row0, st);
+                                                   next_row0, st, row_off, m_out);
   if (side1_streamable(s)) {
     const int rc = s.dtype == DFLASH2_F32 ? launch_side1_stream<float>(s, y, coef1, base, residual, out, st)
                                           : launch_side1_stream<__nv_bfloat16>(s, y, coef1, base, residual, out, st);
     if (rc != DFLASH2_OK) return rc;
     if (next_n == nullptr) return DFLASH2_OK;
-    return launch_rmsnorm_rows(out, next_w, eps, next_n, s.B, s.G, next_row0, s.H, s.dtype, st);
+    return launch_rmsnorm_rows(out, next_w, eps, next_n, s.B, s.G, next_row0, s.H, s.dtype, st, row_off, m_out);
   }
   const int vpc = vectors_per_cta(s.G);
   const dim3 grid((s.H / 8 + vpc - 1) / vpc, s.B);
@@ -1170,7 +1198,7 @@ int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, cons
   if (next_n == nullptr) return DFLASH2_OK;
   // The next RMSNorm as its own row-per-CTA pass: measured faster than fusing it into the
   // apply pass, whose row-per-CTA layout loses the L1 reuse of the previous row.
-  return launch_rmsnorm_rows(out, next_w, eps, next_n, s.B, s.G, next_row0, s.H, s.dtype, st);
+  return launch_rmsnorm_rows(out, next_w, eps, next_n, s.B, s.G, next_row0, s.H, s.dtype, st, row_off, m_out);
 }
 
 int conv_prepare_kernels(const ConvShape& s, bool with_norm) {

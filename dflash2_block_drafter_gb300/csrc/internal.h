@@ -87,8 +87,11 @@ int launch_conv_side0(const ConvShape& s, const void* n, const float* part, int 
 // pass) and one finish call (the fused finish + next norm, or the side-1 pass and the norm).
 int conv_prepare_kernels(const ConvShape& s, bool with_norm);
 int conv_finish_kernels(const ConvShape& s, bool with_next_norm);
+// row_off (nullable): the next norm's output rows of block b are the first row_off[b + 1] -
+// row_off[b] rows from next_row0 on, written at rows row_off[b] .. of an m_out-row output.
 int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, const float* base, const void* residual,
-                      void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st);
+                      void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st,
+                      const int32_t* row_off = nullptr, int m_out = 0);
 
 // ---------------------------------------------------------------- tensor-core GEMM (gemm.cu)
 // C[m, n] = sum_k A[m, k] * Bw[n, k] over rows m < M of A ([M, K]) and the virtual column range
@@ -125,9 +128,12 @@ int launch_wait_selftest(int limit_us, cudaStream_t st);
 
 // ---------------------------------------------------------------- selector (selector.cu)
 // depths (nullable): per-block draft length of a mixed-depth batch; slots past it get path -1.
+// row_off (nullable): a ragged batch, block b's slots are rows row_off[b] .. row_off[b + 1] - 1 of
+// the m_rows-row inputs (cand, unary, z, S); path stays [B, steps] with -1 past each block's rows.
 int launch_score_edges(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
                        const void* pred, const void* succ, int B, int steps, int K, int R, int V, int dtype,
-                       float* S, int32_t* path, cudaStream_t st, const int32_t* depths = nullptr);
+                       float* S, int32_t* path, cudaStream_t st, const int32_t* depths = nullptr,
+                       const int32_t* row_off = nullptr, int m_rows = 0);
 int launch_select_path(const float* S, const int32_t* cand, int B, int steps, int K, int32_t* path,
                        cudaStream_t st, const int32_t* depths = nullptr);
 

@@ -58,6 +58,25 @@ __device__ __forceinline__ int block_depth(const int32_t* depths, int b, int ste
   return min(steps, max(1, static_cast<int>(depths[b])));
 }
 
+// Rows of block b: `steps` slots at b * steps, or (row_off given, a ragged batch) the
+// row_off[b + 1] - row_off[b] slots at row_off[b] of an m_rows-row input. A block whose span is not
+// inside [0, m_rows) or holds outside [1, steps] slots records DFLASH2_ERR_INVALID_ARG (when err is
+// given) and is skipped (its path is all -1).
+struct SlotSpan {
+  size_t first;
+  int n;
+};
+__device__ __forceinline__ SlotSpan block_slots(const int32_t* row_off, int b, int steps, int m_rows, int* err) {
+  if (row_off == nullptr) return SlotSpan{static_cast<size_t>(b) * steps, steps};
+  const int lo = row_off[b];
+  const int n = row_off[b + 1] - lo;
+  if (lo < 0 || n < 1 || n > steps || lo > m_rows - n) {
+    if (err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_INVALID_ARG));
+    return SlotSpan{0, 0};
+  }
+  return SlotSpan{static_cast<size_t>(lo), n};
+}
+
 // Slots are processed in chunks of `lchunk` (all of them at once at the drafter's shape).
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
@@ -403,7 +422,7 @@ __global__ void __launch_bounds__(512)
                            const float* __restrict__ z, const int32_t* __restrict__ anchors,
                            const T* __restrict__ pred, const T* __restrict__ succ, int steps, int V,
                            float* __restrict__ S, int32_t* __restrict__ path, const int32_t* __restrict__ depths,
-                           int* err) {
+                           const int32_t* __restrict__ row_off, int m_rows, int* err) {
   using P = K16Slot<T, R>;
   constexpr int PS = P::PS, E = P::E, NS = P::NS, HR = P::HR, WS = P::WS;
   extern __shared__ float sm[];
@@ -419,7 +438,9 @@ __global__ void __launch_bounds__(512)
   float* sS = sm;            // [steps][16][16]
   float* wt = sm + steps * 256 + warp * 16 * WS;  // [16][2 halves][HR + 4] pred rows * z
   const int anchor = __ldg(anchors + b);
-  const size_t slot0 = static_cast<size_t>(b) * steps;
+  const SlotSpan span = block_slots(row_off, b, steps, m_rows, threadIdx.x == 0 ? err : nullptr);
+  const size_t slot0 = span.first;
+  const int nst = span.n;
   bool bad = false;
 
   int l = warp;
@@ -427,7 +448,7 @@ __global__ void __launch_bounds__(512)
   uint4 rs[PS], rp[PS];
   float zc[E];
   float un = 0.f;
-  if (l < steps) {
+  if (l < nst) {
     k16_ids<T, R>(cand, anchor, slot0 + l, l, lane, cid, pid);
     bad |= k16_rows<T, R>(pred, succ, V, lane, cid, pid, rs, rp);
 #pragma unroll
@@ -438,15 +459,15 @@ __global__ void __launch_bounds__(512)
     un = __ldg(unary + (slot0 + l) * 16 + c);
   }
   int cidn = 0, pidn[PS] = {};
-  if (l + W < steps) k16_ids<T, R>(cand, anchor, slot0 + l + W, l + W, lane, cidn, pidn);
+  if (l + W < nst) k16_ids<T, R>(cand, anchor, slot0 + l + W, l + W, lane, cidn, pidn);
 
-  for (; l < steps; l += W) {
+  for (; l < nst; l += W) {
     const int ln = l + W;
     // next slot's rows, z and unary; the ids one slot further
     uint4 rsn[PS], rpn[PS];
     float zn[E];
     float unn = 0.f;
-    if (ln < steps) {
+    if (ln < nst) {
       bad |= k16_rows<T, R>(pred, succ, V, lane, cidn, pidn, rsn, rpn);
 #pragma unroll
       for (int e = 0; e < E; e += 4) {
@@ -454,7 +475,7 @@ __global__ void __launch_bounds__(512)
         zn[e] = v.x; zn[e + 1] = v.y; zn[e + 2] = v.z; zn[e + 3] = v.w;
       }
       unn = __ldg(unary + (slot0 + ln) * 16 + c);
-      if (ln + W < steps) k16_ids<T, R>(cand, anchor, slot0 + ln + W, ln + W, lane, cidn, pidn);
+      if (ln + W < nst) k16_ids<T, R>(cand, anchor, slot0 + ln + W, ln + W, lane, cidn, pidn);
     }
     // predecessor rows times z into the warp's tile
 #pragma unroll
@@ -513,7 +534,7 @@ __global__ void __launch_bounds__(512)
   if (bad && err != nullptr) atomicCAS(err, 0, static_cast<int>(DFLASH2_ERR_BAD_INDEX));
   __syncthreads();
   if (path != nullptr && warp == 0) {
-    const int d = block_depth(depths, b, steps);
+    const int d = row_off != nullptr ? nst : block_depth(depths, b, steps);
     int p = 0, pos_lo = 0, pos_hi = 0;
     for (int t = 0; t < d; ++t) {
       const float v = lane < 16 ? sS[(t * 16 + p) * 16 + lane] : -INFINITY;
@@ -525,7 +546,7 @@ __global__ void __launch_bounds__(512)
     for (int h2 = 0; h2 < 2; ++h2) {
       const int t = lane + 32 * h2;
       if (t >= steps) break;
-      path[slot0 + t] = t < d ? __ldg(cand + (slot0 + t) * 16 + (h2 == 0 ? pos_lo : pos_hi)) : -1;
+      path[static_cast<size_t>(b) * steps + t] = t < d ? __ldg(cand + (slot0 + t) * 16 + (h2 == 0 ? pos_lo : pos_hi)) : -1;
     }
   }
 }
@@ -572,7 +593,8 @@ __global__ void __launch_bounds__(512, 2)
                            const float* __restrict__ z, const int32_t* __restrict__ anchors,
                            const __nv_bfloat16* __restrict__ pred, const __nv_bfloat16* __restrict__ succ, int steps,
                            int V, float* __restrict__ S, int32_t* __restrict__ path,
-                           const int32_t* __restrict__ depths, int* err) {
+                           const int32_t* __restrict__ depths, const int32_t* __restrict__ row_off, int m_rows,
+                           int* err) {
   constexpr int Q = R / 4;   // r values per lane and row
   constexpr int NV = Q / 8;  // 16-byte vectors per lane and row
   constexpr int KS = R / 8;  // MMA k-steps
@@ -589,9 +611,11 @@ __global__ void __launch_bounds__(512, 2)
   int* sId = reinterpret_cast<int*>(sm);                       // [steps][16] candidate ids, then [steps] path
   uint8_t* sBest = reinterpret_cast<uint8_t*>(sId + steps * 17);  // [steps][16] best successor of each row
   const int anchor = __ldg(anchors + b);
-  const size_t slot0 = static_cast<size_t>(b) * steps;
+  const SlotSpan span = block_slots(row_off, b, steps, m_rows, threadIdx.x == 0 ? err : nullptr);
+  const size_t slot0 = span.first;
+  const int nst = span.n;
   bool bad = false;
-  for (int l = warp; l < steps; l += W) {
+  for (int l = warp; l < nst; l += W) {
     const size_t slot = slot0 + l;
     // this lane's rows: successors g and g + 8 of the slot, predecessors g and g + 8
     int cs[2], ps[2];
@@ -687,7 +711,7 @@ __global__ void __launch_bounds__(512, 2)
     // the walk follows the best-successor table: c_l = best[l][c_{l-1}], c_{-1} = 0
     int* sPath = sId + steps * 16;
     if (lane == 0) {
-      const int d = block_depth(depths, b, steps);
+      const int d = row_off != nullptr ? nst : block_depth(depths, b, steps);
       int p = 0;
       for (int tt = 0; tt < steps; ++tt) {
         if (tt < d) {
@@ -699,45 +723,47 @@ __global__ void __launch_bounds__(512, 2)
       }
     }
     __syncwarp();
-    for (int tt = lane; tt < steps; tt += 32) path[slot0 + tt] = sPath[tt];
+    for (int tt = lane; tt < steps; tt += 32) path[static_cast<size_t>(b) * steps + tt] = sPath[tt];
   }
 }
 
 template <int R>
 cudaError_t launch_mma_t(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
                          const void* pred, const void* succ, int B, int steps, int V, float* S, int32_t* path,
-                         cudaStream_t st, const int32_t* depths, int W, size_t smem) {
+                         cudaStream_t st, const int32_t* depths, const int32_t* row_off, int m_rows, int W,
+                         size_t smem) {
   static unsigned done = 0;
   if (!ensure_smem_attr(score_edges_mma_kernel<R>, kSmemBudget, &done)) return cudaErrorInvalidValue;
   return launch_pdl(score_edges_mma_kernel<R>, dim3(B), dim3(32 * W), smem, st, nullptr, 0, cand, unary, z, anchors,
                     static_cast<const __nv_bfloat16*>(pred), static_cast<const __nv_bfloat16*>(succ), steps, V, S,
-                    path, depths, device_error_word());
+                    path, depths, row_off, m_rows, device_error_word());
 }
 
 template <typename T, int R>
 cudaError_t launch_k16_t(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
                          const void* pred, const void* succ, int B, int steps, int V, float* S, int32_t* path,
-                         cudaStream_t st, const int32_t* depths, int W, size_t smem) {
+                         cudaStream_t st, const int32_t* depths, const int32_t* row_off, int m_rows, int W,
+                         size_t smem) {
   static unsigned done = 0;
   if (!ensure_smem_attr(score_edges_k16_kernel<T, R>, kSmemBudget, &done)) return cudaErrorInvalidValue;
   return launch_pdl(score_edges_k16_kernel<T, R>, dim3(B), dim3(32 * W), smem, st, nullptr, 0, cand, unary, z,
                     anchors, static_cast<const T*>(pred), static_cast<const T*>(succ), steps, V, S, path, depths,
-                    device_error_word());
+                    row_off, m_rows, device_error_word());
 }
 
 int launch_k16(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors, const void* pred,
                const void* succ, int B, int steps, int R, int V, int dtype, float* S, int32_t* path,
-               cudaStream_t st, const int32_t* depths, int W, size_t smem) {
+               cudaStream_t st, const int32_t* depths, const int32_t* row_off, int m_rows, int W, size_t smem) {
   if (smem > static_cast<size_t>(kSmemBudget))
     return fail(DFLASH2_ERR_INVALID_ARG, "score_edges: steps=%d needs %zu bytes of shared memory", steps, smem);
   cudaError_t e = cudaErrorInvalidValue;
 #define DFL_K16(TT, RR)                                                                                      \
-  e = launch_k16_t<TT, RR>(cand, unary, z, anchors, pred, succ, B, steps, V, S, path, st, depths, W, smem)
+  e = launch_k16_t<TT, RR>(cand, unary, z, anchors, pred, succ, B, steps, V, S, path, st, depths, row_off, m_rows, W, \
+                           smem)
   if (dtype == DFLASH2_F32) {
     if (R == 16) DFL_K16(float, 16); else DFL_K16(float, 32);
   } else {
-    if (R == 16) DFL_K16(__nv_bfloat16, 16); else if (R == 32) DFL_K16(__nv_bfloat16, 32);
-    else DFL_K16(__nv_bfloat16, 64);
+    DFL_K16(__nv_bfloat16, 16);
   }
 #undef DFL_K16
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "score_edges launch failed: %s", cudaGetErrorString(e));
@@ -749,7 +775,8 @@ int launch_k16(const int32_t* cand, const float* unary, const float* z, const in
 
 int launch_score_edges(const int32_t* cand, const float* unary, const float* z, const int32_t* anchors,
                        const void* pred, const void* succ, int B, int steps, int K, int R, int V, int dtype,
-                       float* S, int32_t* path, cudaStream_t st, const int32_t* depths) {
+                       float* S, int32_t* path, cudaStream_t st, const int32_t* depths, const int32_t* row_off,
+                       int m_rows) {
   if (K == 16 && dtype == DFLASH2_BF16 && (R == 32 || R == 64)) {
     // tensor-core edge terms; W warps per block: every CTA resident at once at 32 warps per SM
     // where B allows (a slot per warp at small B), down to 4 warps at large B
@@ -759,13 +786,16 @@ int launch_score_edges(const int32_t* cand, const float* unary, const float* z, 
     W = std::max(1, std::min(W, steps));
     const size_t smem = static_cast<size_t>(steps) * (17 * sizeof(int) + 16);
     const cudaError_t e =
-        R == 32 ? launch_mma_t<32>(cand, unary, z, anchors, pred, succ, B, steps, V, S, path, st, depths, W, smem)
-                : launch_mma_t<64>(cand, unary, z, anchors, pred, succ, B, steps, V, S, path, st, depths, W, smem);
+        R == 32 ? launch_mma_t<32>(cand, unary, z, anchors, pred, succ, B, steps, V, S, path, st, depths, row_off,
+                                   m_rows, W, smem)
+                : launch_mma_t<64>(cand, unary, z, anchors, pred, succ, B, steps, V, S, path, st, depths, row_off,
+                                   m_rows, W, smem);
     return e == cudaSuccess ? DFLASH2_OK
                             : fail(DFLASH2_ERR_CUDA, "score_edges launch failed: %s", cudaGetErrorString(e));
   }
-  // (the shapes whose registers fit without spills: bf16 rows up to R = 64, f32 up to R = 32)
-  if (K == 16 && (R == 16 || R == 32 || (R == 64 && dtype == DFLASH2_BF16))) {
+  // the register-tiled FMA kernel for the other K = 16 shapes whose registers fit (f32 rows up to
+  // R = 32, bf16 rows of R = 16)
+  if (K == 16 && (R == 16 || (R == 32 && dtype == DFLASH2_F32))) {
     // W warps per block: as many as keep every CTA resident in one wave at 16 warps per SM (a
     // slot per warp at small B, for latency), down to 2 at large B (pipelined slots per warp)
     const int sms = sm_count();
@@ -773,8 +803,12 @@ int launch_score_edges(const int32_t* cand, const float* unary, const float* z, 
     while (W > 2 && static_cast<long long>(B) * W > 16LL * sms) W >>= 1;
     W = std::max(1, std::min(W, steps));
     const size_t smem = sizeof(float) * (static_cast<size_t>(steps) * 256 + static_cast<size_t>(W) * 16 * (R + 8));
-    return launch_k16(cand, unary, z, anchors, pred, succ, B, steps, R, V, dtype, S, path, st, depths, W, smem);
+    return launch_k16(cand, unary, z, anchors, pred, succ, B, steps, R, V, dtype, S, path, st, depths, row_off,
+                      m_rows, W, smem);
   }
+  if (row_off != nullptr)
+    return fail(DFLASH2_ERR_UNSUPPORTED,
+                "ragged rows need K = 16 and R in {16, 32, 64} (bf16) or {16, 32} (f32); got K=%d, R=%d", K, R);
   {
     // warp-per-slot kernel when its scores and at least a few warps' rows fit in shared memory
     const size_t s_floats = (static_cast<size_t>(steps) * K * K + 3) & ~static_cast<size_t>(3);

@@ -19,9 +19,9 @@ from typing import List, Optional
 import numpy as np
 import torch
 
-from . import (dflash2_conv_finish, dflash2_conv_finish_launches, dflash2_conv_prepare,
+from . import (dflash2_conv_finish, dflash2_conv_finish_launches, dflash2_conv_finish_ragged, dflash2_conv_prepare,
                dflash2_conv_prepare_launches, dflash2_conv_prepare_workspace_bytes, dflash2_head_topk,
-               dflash2_head_topk_workspace_bytes, dflash2_score_edges)
+               dflash2_head_topk_workspace_bytes, dflash2_score_edges, dflash2_score_edges_ragged)
 
 
 def to_device(a: np.ndarray, device="cuda") -> torch.Tensor:
@@ -84,10 +84,11 @@ class TailRunner:
             self.head_ws = torch.empty(max(hw, 256), dtype=torch.uint8, device=device)
 
     # ------------------------------------------------------------------ passes
-    def conv_chain(self, x0: torch.Tensor, ys: List[torch.Tensor], emit_h: bool, before_finish=None):
+    def conv_chain(self, x0: torch.Tensor, ys: List[torch.Tensor], emit_h: bool, before_finish=None, ragged=None):
         """Every site in order, starting from x0 (left unchanged); returns the final residual stream (self.x).
         ``before_finish(i)``, if given, runs before site i's finish call is issued (full_from_host
-        makes the compute stream wait there for y_i's copy)."""
+        makes the compute stream wait there for y_i's copy). ``ragged`` = (row_offsets, m_rows): the
+        final norm writes only each block's drafted rows, packed (h rows [0, m_rows))."""
         wl = self.wl
         nsites = len(self.sites)
         for i, s in enumerate(self.sites):
@@ -103,6 +104,11 @@ class TailRunner:
             if i + 1 < nsites:
                 dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=residual, out=self.x,
                                     next_norm_w=self.sites[i + 1].norm_w, eps=wl.eps, next_n=self.n, next_row0=0)
+            elif emit_h and ragged is not None:
+                off, m_rows = ragged
+                dflash2_conv_finish_ragged(ys[i], self.coef1, s.base, wl.gs, off, m_rows, self.final_norm_w,
+                                           residual=residual, out=self.x, eps=wl.eps,
+                                           next_n=self.h.view(-1, wl.H)[:m_rows], next_row0=1)
             elif emit_h:
                 dflash2_conv_finish(ys[i], self.coef1, s.base, wl.gs, residual=residual, out=self.x,
                                     next_norm_w=self.final_norm_w, eps=wl.eps, next_n=self.h, next_row0=1)
@@ -142,8 +148,32 @@ class TailRunner:
         self.conv_chain(x0, ys, emit_h=True)
         return self.selector(self.h, anchors, want_S=want_S)
 
+    def full_ragged(self, x0: torch.Tensor, ys: List[torch.Tensor], anchors: torch.Tensor, row_offsets: torch.Tensor,
+                    m_rows: int, want_S: bool = True):
+        """The whole block tail of a ragged batch (``dflash2_ragged_offsets``): every conv site runs
+        over the dense blocks, then only block b's drafted rows row_offsets[b] .. row_offsets[b + 1]
+        - 1 go through the final norm, the head and the selector. cand, unary, z and S hold the packed
+        rows [0, m_rows); returns path [B, steps] int32 (-1 past each block's rows)."""
+        self.conv_chain(x0, ys, emit_h=True, ragged=(row_offsets, m_rows))
+        return self.selector_ragged(anchors, row_offsets, m_rows, want_S=want_S)
+
+    def selector_ragged(self, anchors: torch.Tensor, row_offsets: torch.Tensor, m_rows: int, want_S: bool = True):
+        """Head + top-K + z over the packed rows h[0, m_rows), then the ragged edge scores and walk."""
+        wl = self.wl
+        need = dflash2_head_topk_workspace_bytes(m_rows, wl.H, wl.V, wl.K, wl.R)
+        if need > self.head_ws.numel():
+            self.head_ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        h = self.h.view(-1, wl.H)[:m_rows]
+        dflash2_head_topk(h, self.w_head, wl.K, bias=self.bias, w_proj=self.w_proj, cand=self.cand[:m_rows],
+                          unary=self.unary[:m_rows], z=self.z[:m_rows], workspace=self.head_ws)
+        S = self.S.view(-1, wl.K, wl.K)[:m_rows] if want_S else None
+        dflash2_score_edges_ragged(self.cand[:m_rows], self.unary[:m_rows], self.z[:m_rows], anchors, self.pred,
+                                   self.succ, row_offsets, wl.steps, want_S=want_S, S=S, path=self.path)
+        return self.path
+
     def full_from_host(self, h_x0: torch.Tensor, h_ys: List[torch.Tensor], h_anchors: torch.Tensor,
-                       x0: torch.Tensor, ys: List[torch.Tensor], anchors: torch.Tensor, want_S: bool = True):
+                       x0: torch.Tensor, ys: List[torch.Tensor], anchors: torch.Tensor, want_S: bool = True,
+                       ragged=None):
         """The whole block tail with its inputs in pinned host memory. Every input is copied into
         the given device buffers on a copy stream, one event per input; the compute stream waits
         for x0 before the first site, for y_i only before site i's finish and for the anchors
@@ -151,7 +181,8 @@ class TailRunner:
         or four copy streams were measured slower: concurrent host-to-device copies contend.) The
         pass can be captured with ``capture``: the copies become graph nodes on a forked branch
         whose events join it where each input is needed, and the host buffers are read at replay
-        time (refresh them in place). Returns path [B, steps] int32 (device)."""
+        time (refresh them in place). ``ragged`` = (row_offsets, m_rows) runs ``full_ragged``'s
+        selector instead. Returns path [B, steps] int32 (device)."""
         comp = torch.cuda.current_stream()
         if getattr(self, "_copy_stream", None) is None:
             self._copy_stream = torch.cuda.Stream(device=comp.device)
@@ -169,9 +200,12 @@ class TailRunner:
             anchors.copy_(h_anchors, non_blocking=True)
             self._ev_anchors.record(cs)
         comp.wait_event(self._ev_x0)
-        self.conv_chain(x0, ys, emit_h=True, before_finish=lambda i: comp.wait_event(self._ev_y[i]))
+        self.conv_chain(x0, ys, emit_h=True, before_finish=lambda i: comp.wait_event(self._ev_y[i]), ragged=ragged)
         comp.wait_event(self._ev_anchors)
-        path = self.selector(self.h, anchors, want_S=want_S)
+        if ragged is not None:
+            path = self.selector_ragged(anchors, *ragged, want_S=want_S)
+        else:
+            path = self.selector(self.h, anchors, want_S=want_S)
         if not torch.cuda.is_current_stream_capturing():
             for t in [x0, anchors] + list(ys):  # the copy stream wrote them: keep the allocator honest
                 t.record_stream(cs)

@@ -247,6 +247,33 @@ DFLASH2_API int dflash2_score_edges_depths(const int32_t* cand, const float* una
 DFLASH2_API int dflash2_select_path_depths(const float* S, const int32_t* cand, const int32_t* depths, int B, int steps,
                                            int K, int32_t* path, void* stream);
 
+/* ------------------------------------------------------------------------------------
+ * Ragged batches: only the rows a block drafts go through the head and the selector.
+ * (dflash2.ts blockColumns / #block: a block asked to draft `depth` tokens runs over its anchor
+ * and d = min(G - 1, max(1, depth)) mask rows, and only those rows reach the head and #select.)
+ * In a dense [B, G, ...] batch the conv runs over all G rows of every block (the rows past d + 1
+ * are padding that never reaches an earlier row: the conv looks one row back); the head's rows
+ * are then packed per block:
+ *   row_offsets [B + 1] int32 (device): row_offsets[0] = 0 and row_offsets[b + 1] - row_offsets[b]
+ *                  = d_b, the rows block b drafts, in [1, G - 1]; m_rows = row_offsets[B] (host).
+ * dflash2_conv_finish_ragged is dflash2_conv_finish with the next norm written only for block b's
+ * first d_b rows from next_row0 on, at rows row_offsets[b] .. of next_n [m_rows, H] (next_norm_w
+ * and next_n required). dflash2_head_topk then runs over M = m_rows rows as usual, and
+ * dflash2_score_edges_ragged reads block b's slots at rows row_offsets[b] .. of cand, unary, z
+ * ([m_rows, K], [m_rows, K], [m_rows, R]) and S ([m_rows, K, K] or NULL), and writes path
+ * [B, steps] (required) with -1 past d_b. It supports K = 16 with R in {16, 32, 64} (bf16) or
+ * {16, 32} (f32). A block whose span is not inside [0, m_rows) or holds outside [1, G - 1]
+ * (finish) / [1, steps] (edges) rows records DFLASH2_ERR_INVALID_ARG in the device error word and
+ * is skipped (nothing written for it; its path stays -1). */
+DFLASH2_API int dflash2_conv_finish_ragged(const void* y, const void* coef1, const float* base, int B, int G, int H,
+                                           int group_size, int taps, int dtype, const void* residual, void* out,
+                                           const void* next_norm_w, float eps, void* next_n, int next_row0,
+                                           const int32_t* row_offsets, int m_rows, void* stream);
+DFLASH2_API int dflash2_score_edges_ragged(const int32_t* cand, const float* unary, const float* z,
+                                           const int32_t* anchors, const void* pred_book, const void* succ_book,
+                                           const int32_t* row_offsets, int B, int steps, int K, int R, int V,
+                                           int m_rows, int dtype, float* S, int32_t* path, void* stream);
+
 /* Self-test of the bounded-wait machinery: launches one block that waits on an mbarrier that
  * nothing completes, with a limit of `limit_us` microseconds (1..1000000). The wait gives up,
  * records DFLASH2_ERR_TIMEOUT in the device error word and the kernel returns; read it with

@@ -338,3 +338,38 @@ def block_tail(x0, sites, final_norm_w, eps, group_size, w_head, bias, w_proj,
     path, pos = select_path(S, cand)
     return dict(x=x, trace=trace, h=h, logits=logits, cand=cand, unary=unary, z=z, S=S,
                 path=path, pos=pos)
+
+
+def block_tail_ragged(x0, sites, final_norm_w, eps, group_size, w_head, bias, w_proj,
+                      pred_book, succ_book, anchors, K: int, depths):
+    """The block tail of a batch whose blocks draft different numbers of tokens, with only the
+    drafted rows going through the head and the selector.
+
+    [ts] ``blockColumns`` / ``#block``: block b runs over ``block_columns(depths[b], G)`` rows, so
+    rows 1..d_b (d_b = that minus one) go through the final norm, the head, top-K, z and
+    ``#select``, whose walk has d_b slots. The conv sites run over the whole dense block (rows past
+    d_b + 1 are padding that no earlier row reads). Rows of all blocks are packed in block order.
+    Returns a dict: offsets [B + 1]; h, logits, cand, unary, z, S over the packed rows; path and
+    pos [B, G - 1] with -1 past each block's d_b.
+    """
+    x, _ = conv_chain(x0, sites, eps, group_size)
+    B, G, _ = x.shape
+    steps = G - 1
+    offsets = [0]
+    hs, logits, cands, unaries, zs, Ss = [], [], [], [], [], []
+    path = np.full((B, steps), -1, dtype=np.int64)
+    pos = np.full((B, steps), -1, dtype=np.int64)
+    for b in range(B):
+        d = block_columns(depths[b], G) - 1
+        offsets.append(offsets[-1] + d)
+        h = rms_norm(x[b, 1:1 + d, :], final_norm_w, eps)           # [d, H]
+        lg = head_logits(h, w_head, bias)
+        c, u = top_k(lg, K)
+        zz = hidden_projection(h, w_proj)
+        S = score_edges(c[None], u[None], zz[None], np.asarray(anchors)[b:b + 1], pred_book, succ_book)
+        pth, ps = select_path(S, c[None])
+        path[b, :d], pos[b, :d] = pth[0], ps[0]
+        hs.append(h); logits.append(lg); cands.append(c); unaries.append(u); zs.append(zz); Ss.append(S[0])
+    return dict(offsets=np.asarray(offsets), h=np.concatenate(hs), logits=np.concatenate(logits),
+                cand=np.concatenate(cands), unary=np.concatenate(unaries), z=np.concatenate(zs),
+                S=np.concatenate(Ss), path=path, pos=pos)

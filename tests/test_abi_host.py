@@ -196,3 +196,19 @@ def test_head_bindings_reject_mismatched_shapes_before_the_library(entry):
     if extra:
         with pytest.raises(ValueError):
             fn(h, good["w"], extra[0][:V - 1], K, w_proj=good["w_proj"])
+
+
+def test_ragged_entry_points_reject_bad_arguments(lib):
+    f = lib.dflash2_conv_finish_ragged
+    #        y     coef  base  B   G   H     gs  taps dt resid out   nw    eps   nn    row0 off   m   stream
+    assert f(FAKE, FAKE, FAKE, 4, 16, 5120, 16, 2, 0, None, FAKE, FAKE, 1e-6, FAKE, 1, None, 30, None) == -1  # offsets
+    assert f(FAKE, FAKE, FAKE, 4, 16, 5120, 16, 2, 0, None, FAKE, None, 1e-6, FAKE, 1, FAKE, 30, None) == -1  # no norm
+    assert f(FAKE, FAKE, FAKE, 4, 16, 5120, 16, 2, 0, None, FAKE, FAKE, 1e-6, FAKE, 1, FAKE, 0, None) == -1   # m_rows
+    assert f(FAKE, FAKE, FAKE, 4, 16, 5120, 16, 3, 0, None, FAKE, FAKE, 1e-6, FAKE, 1, FAKE, 30, None) == -2  # taps
+    g = lib.dflash2_score_edges_ragged
+    #        cand  un    z     anch  pred  succ  off   B  st  K   R   V     m   dt S     path  stream
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 4, 15, 16, 64, 1000, 30, 0, None, FAKE, None) == -1  # offsets
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 15, 8, 64, 1000, 30, 0, None, FAKE, None) == -1   # K != 16
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 15, 16, 64, 1000, 30, 1, None, FAKE, None) == -1  # f32 R=64
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 15, 16, 64, 1000, 30, 0, None, None, None) == -1  # no path
+    assert b"path" in lib.dflash2_last_error_message() or b"NULL" in lib.dflash2_last_error_message()

@@ -523,3 +523,30 @@ def test_conv_rows_past_depth_do_not_reach_earlier_rows():
     fin_s = O.conv_finish(y[:, :d + 1], d1_s, base, gs, residual=x[:, :d + 1])
     assert np.array_equal(out[:, :d + 1], out_s)
     assert np.array_equal(fin[:, :d + 1], fin_s)
+
+
+def test_ragged_tail_is_the_dense_tail_restricted_to_the_drafted_rows():
+    # Rows never interact in the head, top-K and z, and a block's walk is causal, so the ragged
+    # tail equals the dense tail's rows 1..d_b of each block and select_path_depths' walk.
+    B, G, H, gs, V, K, R = 4, 6, 32, 16, 40, 4, 8
+    x0 = _rand(B, G, H)
+
+    class Site:
+        pass
+    s = Site()
+    s.w_kp, s.base, s.norm_w, s.y = _rand(4 * H // gs, H, scale=0.2), _rand(2, 2, H), np.ones(H), _rand(B, G, H)
+    w_head, w_proj = _rand(V, H), _rand(R, H)
+    pred, succ = _rand(V, R), _rand(V, R)
+    anchors = RNG.integers(0, V, size=B)
+    depths = np.array([5, 0, 2, 9])
+    dense = O.block_tail(x0, [s], np.ones(H), 1e-6, gs, w_head, None, w_proj, pred, succ, anchors, K)
+    rag = O.block_tail_ragged(x0, [s], np.ones(H), 1e-6, gs, w_head, None, w_proj, pred, succ, anchors, K, depths)
+    d = [5, 1, 2, 5]
+    assert list(rag["offsets"]) == [0, 5, 6, 8, 13]
+    rows = [(b, l) for b in range(B) for l in range(d[b])]
+    for i, (b, l) in enumerate(rows):
+        np.testing.assert_allclose(rag["h"][i], dense["h"][b, l], rtol=1e-12, atol=1e-12)
+        np.testing.assert_array_equal(rag["cand"][i], dense["cand"][b, l])
+        np.testing.assert_allclose(rag["S"][i], dense["S"][b, l], rtol=1e-12, atol=1e-12)
+    want, _ = O.select_path_depths(dense["S"], dense["cand"], depths)
+    np.testing.assert_array_equal(rag["path"], want)
