@@ -271,7 +271,7 @@ def bandwidth_sweep(kind, iters=10):
     if kind == "edges":
         for B in (64, 256, 1024, 4096):
             points.append(edges_point(d, B, gen, dev, time_call, pk))
-    else:
+    elif kind == "conv":
         G, H, gs = 16, 5120, 16
         groups = H // gs
         w_kp = (torch.randn(4 * groups, H, generator=gen, device=dev) / H ** 0.5).to(torch.bfloat16)
@@ -301,10 +301,88 @@ def bandwidth_sweep(kind, iters=10):
                            "prepare_tflops": 2.0 * rows * 4 * groups * H / (ms_p / 1e3) / 1e12,
                            "finish_ms": ms_f, "finish_gbs": bf / (ms_f / 1e3) / 1e9,
                            "finish_frac_hbm": bf / (ms_f / 1e3) / 1e9 / pk["hbm_gbs"]})
+    elif kind == "proj":
+        points = proj_sweep(d, gen, dev, time_call, pk)
     print(json.dumps({"sweep": kind, "peak_hbm_gbs": pk["hbm_gbs"], "peak_source": pk["source"],
                       "timing": "median of CUDA-event times of single calls, 256 MB L2 flush before each",
                       "points": points}), flush=True)
     return 0
+
+
+def proj_sweep(d, gen, dev, time_call, pk, G=16, H=5120, gs=16, N=5120):
+    """One conv site around stand-in sublayer projections (input H -> N, output N -> H, seeded
+    N(0, 1/sqrt(fan_in)) weights) at B = 1, 8, 64 blocks: the unfused sequence (prepare writes the
+    side-0 output, the projection reads it; the output projection writes y, finish reads it)
+    against the fused one (coefficients, then the conv's side 0 inside the input projection's
+    operand producer and side 1 + the residual inside the output projection's epilogue), and the
+    bf16 projection against the affine 4-bit one. Times are medians of single-call sequences with
+    an L2 flush before each."""
+    import torch
+    groups = H // gs
+    w_kp = (torch.randn(4 * groups, H, generator=gen, device=dev) / H ** 0.5).to(torch.bfloat16)
+    base = torch.zeros(2, 2, H, device=dev)
+    base[:, 0] = 1.0
+    base += 0.1 * torch.randn(2, 2, H, generator=gen, device=dev)
+    w_in = (torch.randn(N, H, generator=gen, device=dev) / H ** 0.5).to(torch.bfloat16)
+    w_out = (torch.randn(H, N, generator=gen, device=dev) / N ** 0.5).to(torch.bfloat16)
+    q_in = torch.randint(0, 2 ** 31 - 1, (N, H // 8), generator=gen, device=dev, dtype=torch.int32)
+    s_in = (torch.rand(N, H // 64, generator=gen, device=dev) / 64).to(torch.bfloat16)
+    b_in = (torch.randn(N, H // 64, generator=gen, device=dev) / 128).to(torch.bfloat16)
+    points = []
+    for B in (1, 8, 64):
+        M = B * G
+        n = torch.randn(B, G, H, generator=gen, device=dev).to(torch.bfloat16)
+        x = torch.randn(M, H, generator=gen, device=dev).to(torch.bfloat16)
+        a = torch.empty_like(n)
+        coef1 = torch.empty(B, G, 2, groups, dtype=torch.bfloat16, device=dev)
+        d0 = torch.empty(M, 2, groups, dtype=torch.float32, device=dev)
+        c1 = torch.empty(M, 2, groups, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(d.dflash2_conv_prepare_workspace_bytes(B, G, H, gs, torch.bfloat16), dtype=torch.uint8,
+                         device=dev)
+        u = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+        out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+
+        def in_unfused():
+            d.dflash2_conv_prepare(n, None, 1e-6, w_kp, base, gs, out=a, coef1=coef1, workspace=ws)
+            d.dflash2_proj(a.view(M, H), w_in, out=u)
+
+        def in_fused():
+            d.dflash2_conv_coefficients(n, None, 1e-6, w_kp, gs, d0=d0, coef1=c1, workspace=ws)
+            d.dflash2_proj_conv_in(n.view(M, H), d0, base, G, gs, w_in, out=u)
+
+        def out_unfused():
+            d.dflash2_proj(u, w_out, out=y)
+            d.dflash2_conv_finish(y.view(B, G, H), coef1, base, gs, residual=x.view(B, G, H), out=out.view(B, G, H))
+
+        def out_fused():
+            d.dflash2_proj_conv_out(u, w_out, c1, base, G, gs, residual=x, out=out)
+
+        t = {name: time_call(fn) for name, fn in (("in_unfused", in_unfused), ("in_fused", in_fused),
+                                                  ("out_unfused", out_unfused), ("out_fused", out_fused))}
+        t["proj_bf16"] = time_call(lambda: d.dflash2_proj(n.view(M, H), w_in, out=u))
+        t["proj_w4"] = time_call(lambda: d.dflash2_proj(n.view(M, H), q_in, w_scales=s_in, w_biases=b_in, out=u))
+        e = 2.0  # bf16 bytes
+        # algorithmic bytes of each sequence (every tensor read or written once per call)
+        act_h, act_n = M * H * e, M * N * e
+        kp_w, c_bytes = 4 * groups * H * e, M * 2 * groups * e
+        win, wout = N * H * e, H * N * e
+        b_in_unf = (act_h + kp_w + act_h + c_bytes) + (act_h + win + act_n)
+        b_in_fus = (act_h + kp_w + M * 2 * groups * 4 + c_bytes) + (act_h + M * 2 * groups * 4 + win + act_n)
+        b_out_unf = (act_n + wout + act_h) + (act_h + c_bytes + act_h + act_h)
+        b_out_fus = act_n + wout + c_bytes + act_h + act_h
+        flops = 2.0 * M * N * H
+        points.append({
+            "B": B, "rows": M, "N": N,
+            "ms": t,
+            "bytes": {"in_unfused": b_in_unf, "in_fused": b_in_fus, "out_unfused": b_out_unf, "out_fused": b_out_fus,
+                      "proj_bf16": act_h + win + act_n, "proj_w4": act_h + N * H / 2 + N * H // 64 * 4 + act_n},
+            "proj_bf16_tflops": flops / (t["proj_bf16"] / 1e3) / 1e12,
+            "proj_bf16_frac_of_burst": flops / (t["proj_bf16"] / 1e3) / 1e12 / pk["bf16_tflops"],
+            "fused_saving_in": 1.0 - t["in_fused"] / t["in_unfused"],
+            "fused_saving_out": 1.0 - t["out_fused"] / t["out_unfused"],
+        })
+    return points
 
 
 def conv_site_bytes(B, G, H, groups):
@@ -729,7 +807,7 @@ def main():
     ap.add_argument("--graph", dest="graph", action="store_true", default=True,
                     help="replay each part of a timed step as a CUDA graph (default)")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
-    ap.add_argument("--sweep", choices=["edges", "conv"], default=None,
+    ap.add_argument("--sweep", choices=["edges", "conv", "proj"], default=None,
                     help="instead of the step benchmark: one call's bandwidth as the batch grows")
     args = ap.parse_args()
     if args.sweep is not None:

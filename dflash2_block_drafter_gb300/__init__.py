@@ -23,6 +23,7 @@ __all__ = [
     "dflash2_head_topk_workspace_bytes", "dflash2_head_topk", "dflash2_score_edges",
     "dflash2_select_path", "dflash2_selftest_bounded_wait", "dflash2_head_topk_noalloc", "dflash2_head_topk_vocab", "dflash2_score_edges_depths", "dflash2_select_path_depths",
     "dflash2_ragged_offsets", "dflash2_conv_finish_ragged", "dflash2_score_edges_ragged",
+    "dflash2_conv_coefficients", "dflash2_proj", "dflash2_proj_conv_in", "dflash2_proj_conv_out",
     "DTYPE_CODES",
 ]
 
@@ -61,6 +62,10 @@ _SIGNATURES = {
                                         _vp]),
     "dflash2_score_edges_ragged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp,
                                         _vp]),
+    "dflash2_conv_coefficients": (_i, [_vp, _vp, _f, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "dflash2_proj": (_i, [_vp, _i, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
+    "dflash2_proj_conv_in": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
+    "dflash2_proj_conv_out": (_i, [_vp, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _vp, _i, _vp, _vp]),
 }
 
 
@@ -399,3 +404,91 @@ def dflash2_score_edges_ragged(cand, unary, z, anchors, pred_book, succ_book, ro
         V, m_rows, _code(pred_book), _dev(S, "S", torch.float32, True), _dev(path, "path", torch.int32),
         _stream(stream)))
     return S, path
+
+
+def _proj_weight(w, w_scales, w_biases, K):
+    """(pointer args, wbits, N) of a projection weight: bf16 [N, K], or 4-bit words [N, K/8] (int32 or
+    uint32 storage) with bf16 scales / biases [N, K/64]."""
+    if w_scales is None and w_biases is None:
+        if w.dim() != 2 or w.shape[1] != K:
+            raise ValueError(f"w must be [N, {K}] bf16, got shape {tuple(w.shape)}")
+        return (_dev(w, "w", torch.bfloat16), None, None), 16, w.shape[0]
+    if w_scales is None or w_biases is None:
+        raise ValueError("4-bit weights need both w_scales and w_biases")
+    if w.dim() != 2 or w.shape[1] * 8 != K or w.element_size() != 4:
+        raise ValueError(f"packed 4-bit w must be [N, {K // 8}] 32-bit words, got {tuple(w.shape)} {w.dtype}")
+    N = w.shape[0]
+    for t, name in ((w_scales, "w_scales"), (w_biases, "w_biases")):
+        if tuple(t.shape) != (N, K // 64):
+            raise ValueError(f"{name} must be [{N}, {K // 64}], got {tuple(t.shape)}")
+    return (_dev(w, "w"), _dev(w_scales, "w_scales", torch.bfloat16), _dev(w_biases, "w_biases", torch.bfloat16)), 4, N
+
+
+def dflash2_conv_coefficients(x, norm_w, eps, w_kp, group_size, n_out=None, d0=None, coef1=None, workspace=None,
+                              stream=None, taps=2):
+    """Prepare without the side-0 output: returns (n [B*G, H] (x itself when norm_w is None), d0
+    [B*G, 2, groups] fp32, coef1 [B*G, 2, groups])."""
+    B, G, H = x.shape
+    groups = H // group_size
+    dt = x.dtype
+    if norm_w is not None and n_out is None:
+        n_out = torch.empty((B * G, H), dtype=dt, device=x.device)
+    d0 = torch.empty((B * G, 2, groups), dtype=torch.float32, device=x.device) if d0 is None else d0
+    coef1 = torch.empty((B * G, 2, groups), dtype=dt, device=x.device) if coef1 is None else coef1
+    for t, n, name in ((d0, B * G * 2 * groups, "d0"), (coef1, B * G * 2 * groups, "coef1")):
+        if t.numel() < n:
+            raise ValueError(f"{name} holds {t.numel()} elements, fewer than {n}")
+    nbytes = library().dflash2_conv_prepare_workspace_bytes(B, G, H, group_size, _code(x))
+    workspace = _workspace(nbytes, x.device, workspace)
+    _check(library().dflash2_conv_coefficients(
+        _dev(x, "x", dt), _dev(norm_w, "norm_w", dt, True), eps, _dev(w_kp, "w_kp", dt), B, G, H, group_size, taps,
+        _code(x), _dev(n_out, "n_out", dt, True), _dev(d0, "d0", torch.float32), _dev(coef1, "coef1", dt),
+        _dev(workspace, "workspace"), workspace.numel(), _stream(stream)))
+    return (n_out if norm_w is not None else x.view(B * G, H)), d0, coef1
+
+
+def _proj_out(out, M, N, dev):
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if out is None else out
+    if out.numel() < M * N:
+        raise ValueError(f"out holds {out.numel()} elements, fewer than M * N = {M * N}")
+    return out
+
+
+def dflash2_proj(a, w, w_scales=None, w_biases=None, out=None, stream=None):
+    """out [M, N] = a [M, K] . W^T (bf16; W bf16 [N, K] or affine 4-bit with scales / biases)."""
+    M, K = a.shape
+    wp, wbits, N = _proj_weight(w, w_scales, w_biases, K)
+    out = _proj_out(out, M, N, a.device)
+    _check(library().dflash2_proj(_dev(a, "a", torch.bfloat16), M, K, *wp, wbits, N, BF16,
+                                  _dev(out, "out", torch.bfloat16), _stream(stream)))
+    return out
+
+
+def dflash2_proj_conv_in(n, d0, base, G, group_size, w, w_scales=None, w_biases=None, out=None, stream=None):
+    """out = Conv_0(n) . W^T with the conv's side 0 computed inside the GEMM (n [M, K = H])."""
+    M, K = n.shape
+    wp, wbits, N = _proj_weight(w, w_scales, w_biases, K)
+    if d0.numel() < M * 2 * (K // group_size) or base.numel() < 4 * K:
+        raise ValueError("d0 must hold [M, 2, K / group_size] and base [2, 2, K]")
+    out = _proj_out(out, M, N, n.device)
+    _check(library().dflash2_proj_conv_in(
+        _dev(n, "n", torch.bfloat16), _dev(d0, "d0", torch.float32), _dev(base, "base", torch.float32), G, group_size,
+        M, K, *wp, wbits, N, BF16, _dev(out, "out", torch.bfloat16), _stream(stream)))
+    return out
+
+
+def dflash2_proj_conv_out(a, w, coef1, base, G, group_size, residual=None, w_scales=None, w_biases=None, out=None,
+                          stream=None):
+    """out = residual + Conv_1(a . W^T) with the conv's side 1 (and the residual add) in the GEMM's epilogue."""
+    M, K = a.shape
+    wp, wbits, N = _proj_weight(w, w_scales, w_biases, K)
+    if coef1.numel() < M * 2 * (N // group_size) or base.numel() < 4 * N:
+        raise ValueError("coef1 must hold [M, 2, N / group_size] and base [2, 2, N]")
+    if residual is not None and residual.numel() < M * N:
+        raise ValueError("residual must hold [M, N]")
+    out = _proj_out(out, M, N, a.device)
+    _check(library().dflash2_proj_conv_out(
+        _dev(a, "a", torch.bfloat16), M, K, *wp, wbits, N, _dev(coef1, "coef1", torch.bfloat16),
+        _dev(base, "base", torch.float32), G, group_size, _dev(residual, "residual", torch.bfloat16, True), BF16,
+        _dev(out, "out", torch.bfloat16), _stream(stream)))
+    return out

@@ -200,6 +200,100 @@ int dflash2_conv_finish_ragged(const void* y, const void* coef1, const float* ba
                            static_cast<cudaStream_t>(stream), row_offsets, m_rows);
 }
 
+int dflash2_conv_coefficients(const void* x, const void* norm_w, float eps, const void* w_kp, int B, int G, int H,
+                              int group_size, int taps, int dtype, void* n_out, float* d0, void* coef1,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_conv_shape(B, G, H, group_size, taps, dtype);
+  if (rc != DFLASH2_OK) return rc;
+  REQUIRE(x && w_kp && d0 && coef1 && workspace, "a required pointer is NULL");
+  REQUIRE(norm_w == nullptr || n_out != nullptr, "n_out is required when norm_w is given");
+  REQUIRE(aligned16(x) && aligned16(w_kp) && (!norm_w || aligned16(norm_w)) && (!n_out || aligned16(n_out)),
+          "x, norm_w, w_kp and n_out must be 16-byte aligned");
+  REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "workspace must be 256-byte aligned");
+  const ConvShape s{B, G, H, group_size, H / group_size, dtype};
+  const int sms = sm_count();
+  const size_t need = conv_prepare_workspace(s, sms);
+  if (workspace_bytes < need)
+    return fail(DFLASH2_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", workspace_bytes,
+                need);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const GemmPlan plan = kp_plan(s, sms);
+  const size_t es = dtype == DFLASH2_F32 ? 4 : 2;
+  size_t n_bytes = static_cast<size_t>(s.rows()) * H * es;
+  n_bytes = (n_bytes + 255) & ~static_cast<size_t>(255);
+  const void* n = x;
+  if (norm_w != nullptr) {
+    rc = launch_rmsnorm(x, norm_w, eps, n_out, s.rows(), H, dtype, st);
+    if (rc != DFLASH2_OK) return rc;
+    n = n_out;
+  }
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + n_bytes);
+  const GemmProblem gp{n, w_kp, nullptr, s.rows(), H, 4 * s.groups, 0, dtype};
+  rc = launch_gemm_store(gp, plan, part, st);
+  if (rc != DFLASH2_OK) return rc;
+  return launch_conv_coefficients(part, plan.k_splits, s.rows(), s.groups, dtype, d0, coef1, st);
+}
+
+static int check_proj(const void* a, int M, int K, const void* w, const void* w_scales, const void* w_biases, int wbits,
+                      int N, int dtype, void* out) {
+  if (dtype != DFLASH2_BF16) return fail(DFLASH2_ERR_UNSUPPORTED, "the projections run in bf16 only (dtype=%d)", dtype);
+  REQUIRE(a && w && out, "a required pointer is NULL");
+  REQUIRE(M >= 1, "M=%d must be >= 1", M);
+  REQUIRE(K >= 64 && K % 64 == 0, "K=%d must be a positive multiple of 64", K);
+  REQUIRE(N >= 8 && N % 8 == 0, "N=%d must be a positive multiple of 8", N);
+  REQUIRE(wbits == 16 || wbits == 4, "wbits=%d must be 16 (bf16) or 4 (affine 4-bit, groups of 64)", wbits);
+  if (wbits == 4) REQUIRE(w_scales && w_biases, "4-bit weights need w_scales and w_biases");
+  REQUIRE(aligned16(a) && aligned16(w) && aligned16(out), "a, w and out must be 16-byte aligned");
+  return DFLASH2_OK;
+}
+
+int dflash2_proj(const void* a, int M, int K, const void* w, const void* w_scales, const void* w_biases, int wbits,
+                 int N, int dtype, void* out, void* stream) {
+  const int rc = check_proj(a, M, K, w, w_scales, w_biases, wbits, N, dtype, out);
+  if (rc != DFLASH2_OK) return rc;
+  ProjSpec p{};
+  p.a = a; p.w = w; p.scales = w_scales; p.qbias = w_biases; p.wbits = wbits;
+  p.M = M; p.N = N; p.K = K; p.out = out;
+  return launch_proj(p, static_cast<cudaStream_t>(stream));
+}
+
+int dflash2_proj_conv_in(const void* n, const float* d0, const float* base, int G, int group_size, int M, int K,
+                         const void* w, const void* w_scales, const void* w_biases, int wbits, int N, int dtype,
+                         void* out, void* stream) {
+  const int rc = check_proj(n, M, K, w, w_scales, w_biases, wbits, N, dtype, out);
+  if (rc != DFLASH2_OK) return rc;
+  REQUIRE(d0 && base, "d0 and base are required");
+  REQUIRE(G >= 2 && G <= 64 && 128 % G == 0, "G=%d must divide 128 (blocks must not straddle a 128-row tile)", G);
+  REQUIRE(M % G == 0, "M=%d must be a whole number of %d-row blocks", M, G);
+  REQUIRE(group_size == 8 || group_size == 16 || group_size == 32 || group_size == 64,
+          "group_size=%d must be 8, 16, 32 or 64", group_size);
+  REQUIRE(K % group_size == 0, "K=%d must be a multiple of group_size=%d", K, group_size);
+  REQUIRE(aligned16(base), "base must be 16-byte aligned");
+  ProjSpec p{};
+  p.a = n; p.w = w; p.scales = w_scales; p.qbias = w_biases; p.wbits = wbits;
+  p.M = M; p.N = N; p.K = K; p.out = out;
+  p.d0 = d0; p.base = base; p.G = G; p.gs = group_size; p.groups = K / group_size;
+  return launch_proj(p, static_cast<cudaStream_t>(stream));
+}
+
+int dflash2_proj_conv_out(const void* a, int M, int K, const void* w, const void* w_scales, const void* w_biases,
+                          int wbits, int N, const void* coef1, const float* base, int G, int group_size,
+                          const void* residual, int dtype, void* out, void* stream) {
+  const int rc = check_proj(a, M, K, w, w_scales, w_biases, wbits, N, dtype, out);
+  if (rc != DFLASH2_OK) return rc;
+  REQUIRE(coef1 && base, "coef1 and base are required");
+  REQUIRE(G >= 2 && G <= 32 && 32 % G == 0, "G=%d must divide 32 (a block's rows must share a warp)", G);
+  REQUIRE(M % G == 0, "M=%d must be a whole number of %d-row blocks", M, G);
+  REQUIRE(group_size == 8 || group_size == 16 || group_size == 32, "group_size=%d must be 8, 16 or 32", group_size);
+  REQUIRE(N % group_size == 0 && N % 32 == 0, "N=%d must be a multiple of 32 and of group_size", N);
+  REQUIRE(aligned16(base) && (!residual || aligned16(residual)), "base and residual must be 16-byte aligned");
+  ProjSpec p{};
+  p.a = a; p.w = w; p.scales = w_scales; p.qbias = w_biases; p.wbits = wbits;
+  p.M = M; p.N = N; p.K = K; p.out = out;
+  p.coef1 = coef1; p.base = base; p.residual = residual; p.G = G; p.gs = group_size; p.groups = N / group_size;
+  return launch_proj(p, static_cast<cudaStream_t>(stream));
+}
+
 size_t dflash2_head_topk_workspace_bytes(int M, int H, int V, int K, int R) {
   if (M < 1 || H < 64 || V < 1 || K < 1 || R < 0) return 0;
   return head_workspace(M, V, K, R, sm_count());

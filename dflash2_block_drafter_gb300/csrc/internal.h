@@ -126,6 +126,36 @@ int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bi
                      const int32_t* ids_map = nullptr);
 int launch_wait_selftest(int limit_us, cudaStream_t st);
 
+// bf16 row-major [rows, cols] operand for tcgen05: box of 64 elements (128 bytes) x box_rows rows,
+// 128-byte swizzle (defined in gemm.cu).
+bool make_tmap_sw128(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+// ---------------------------------------------------------------- sublayer projections (proj.cu)
+// out[M, N] = A[M, K] W[N, K]^T (bf16 in and out, fp32 accumulation), with optional fusions:
+//   d0 (non-null): A = Conv_0(a) with side-0 deltas d0 [M][2][groups] fp32 and base [2][2][K];
+//   coef1 (non-null): out = residual + Conv_1(A W^T) with side-1 deltas coef1 [M][2][groups] bf16 and
+//                     base [2][2][N] (residual may be null);
+//   wbits = 4: w is packed affine 4-bit [N][K / 8] 32-bit words (value k at bits 4 (k % 8) of word
+//              k / 8), scales / qbias [N][K / 64] bf16; wbits = 16: w is bf16 [N][K].
+struct ProjSpec {
+  const void* a;
+  const void* w;
+  const void* scales;
+  const void* qbias;
+  int wbits;
+  int M, N, K;
+  const float* d0;
+  const float* base;
+  int G, gs, groups;
+  const void* coef1;
+  const void* residual;
+  void* out;
+};
+int launch_proj(const ProjSpec& p, cudaStream_t st);
+// D from kernel_projection's split-K partials: d0 = side 0's deltas (fp32), coef1 = side 1's (dtype).
+int launch_conv_coefficients(const float* part, int k_splits, int M, int groups, int dtype, float* d0, void* coef1,
+                             cudaStream_t st);
+
 // ---------------------------------------------------------------- selector (selector.cu)
 // depths (nullable): per-block draft length of a mixed-depth batch; slots past it get path -1.
 // row_off (nullable): a ragged batch, block b's slots are rows row_off[b] .. row_off[b + 1] - 1 of

@@ -274,6 +274,48 @@ DFLASH2_API int dflash2_score_edges_ragged(const int32_t* cand, const float* una
                                            const int32_t* row_offsets, int B, int steps, int K, int R, int V,
                                            int m_rows, int dtype, float* S, int32_t* path, void* stream);
 
+/* ------------------------------------------------------------------------------------
+ * The sublayer projections around a conv site, with the conv fused into them.
+ * (dflash2.ts #block: a = #conv(n, coef, 0) feeds q/k/v (attention) or gate/up (MLP); o or down's
+ * output goes through #conv(., coef, 1) and is added to the residual in fp32. MAX
+ * DFlash2TransformerBlock: h = conv.prepare(norm(r)); h = sublayer(h); r += conv.finish(h).)
+ * bf16 only (DFLASH2_BF16; anything else returns DFLASH2_ERR_UNSUPPORTED). fp32 accumulation on the
+ * tensor cores; outputs rounded once to bf16.
+ *
+ * dflash2_conv_coefficients: prepare without the side-0 output. Optional RMSNorm (norm_w given:
+ *   n_out [B*G, H] receives n; else n = x and n_out may be NULL), kernel_projection, then
+ *   d0 [B*G, 2, groups] fp32 = side 0's deltas D[t, 0, tap, g] and coef1 [B*G, 2, groups] dtype =
+ *   side 1's (as dflash2_conv_prepare's coef1). Workspace as dflash2_conv_prepare_workspace_bytes.
+ *
+ * dflash2_proj: out [M, N] = a [M, K] . W^T.
+ * dflash2_proj_conv_in: out = Conv_0(n) . W^T, Conv_0(n)[m, k] = (base[0,0,k] + d0[m,0,k/gs]) n[m, k]
+ *   + (base[0,1,k] + d0[m,1,k/gs]) n[m-1, k], n[m-1] = 0 at each block's first row (m % G == 0);
+ *   the side-0 output is computed in the GEMM's operand producer and never written. K = H;
+ *   base [2, 2, K] fp32; G divides 128, M % G == 0, group_size in {8, 16, 32, 64}.
+ * dflash2_proj_conv_out: out = residual + Conv_1(a . W^T) (residual may be NULL), Conv_1 with the
+ *   side-1 deltas coef1 [M, 2, N/gs] (bf16) and base[1] over the N = H output channels, computed in
+ *   the GEMM's epilogue (fp32 add, one rounding). G divides 32, M % G == 0, group_size in {8, 16, 32},
+ *   N % 32 == 0. out may not alias residual.
+ *
+ * Weights: wbits = 16: w is bf16 [N, K] (out, in). wbits = 4: affine 4-bit weights in groups of 64
+ * along K (dflash2.ts quantizedWeight: quantize(w, 64, bits), mode "affine"): w is [N, K/8] uint32,
+ * value k of row n in bits 4 (k % 8) .. 4 (k % 8) + 3 of word k / 8 (an unsigned q in [0, 15]);
+ * w_scales and w_biases are bf16 [N, K/64]; W[n, k] = w_scales[n, k/64] * q + w_biases[n, k/64],
+ * rounded once to bf16 before the MMA. K % 64 == 0, N % 8 == 0, M >= 1; a, w, out, residual and base
+ * 16-byte aligned.
+ * ---------------------------------------------------------------------------------- */
+DFLASH2_API int dflash2_conv_coefficients(const void* x, const void* norm_w, float eps, const void* w_kp, int B, int G,
+                                          int H, int group_size, int taps, int dtype, void* n_out, float* d0,
+                                          void* coef1, void* workspace, size_t workspace_bytes, void* stream);
+DFLASH2_API int dflash2_proj(const void* a, int M, int K, const void* w, const void* w_scales, const void* w_biases,
+                             int wbits, int N, int dtype, void* out, void* stream);
+DFLASH2_API int dflash2_proj_conv_in(const void* n, const float* d0, const float* base, int G, int group_size, int M,
+                                     int K, const void* w, const void* w_scales, const void* w_biases, int wbits, int N,
+                                     int dtype, void* out, void* stream);
+DFLASH2_API int dflash2_proj_conv_out(const void* a, int M, int K, const void* w, const void* w_scales,
+                                      const void* w_biases, int wbits, int N, const void* coef1, const float* base,
+                                      int G, int group_size, const void* residual, int dtype, void* out, void* stream);
+
 /* Self-test of the bounded-wait machinery: launches one block that waits on an mbarrier that
  * nothing completes, with a limit of `limit_us` microseconds (1..1000000). The wait gives up,
  * records DFLASH2_ERR_TIMEOUT in the device error word and the kernel returns; read it with

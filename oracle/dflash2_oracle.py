@@ -373,3 +373,44 @@ def block_tail_ragged(x0, sites, final_norm_w, eps, group_size, w_head, bias, w_
     return dict(offsets=np.asarray(offsets), h=np.concatenate(hs), logits=np.concatenate(logits),
                 cand=np.concatenate(cands), unary=np.concatenate(unaries), z=np.concatenate(zs),
                 S=np.concatenate(Ss), path=path, pos=pos)
+
+
+# --------------------------------------------------------------------------- sublayer projections
+
+def affine_dequantize(q, scales, biases, group: int = 64) -> np.ndarray:
+    """W[n, k] = scales[n, k // group] * q[n, k] + biases[n, k // group] (affine quantisation).
+
+    [ts] ``quantizedWeight`` (``quantize(source, 64, bits)``, ``QuantizedLinear`` with
+    ``groupSize: 64, mode: "affine"``): a 4-bit code per weight and one scale and bias per row and
+    group of 64 input channels. q: [N, K] integer codes; scales, biases: [N, K // group].
+    """
+    q = _f64(q)
+    return q * np.repeat(_f64(scales), group, axis=1) + np.repeat(_f64(biases), group, axis=1)
+
+
+def projection(a, W) -> np.ndarray:
+    """y = a @ Wᵀ, W stored [out, in]. [ts] ``Bf16Projection.forward`` (a matmul against the stored
+    transpose) and the sublayers' q/k/v/o and gate/up/down projections."""
+    return _f64(a) @ _f64(W).T
+
+
+def sublayer_in(n, d_side0, base, group_size: int, W) -> np.ndarray:
+    """An input projection of the sublayer applied to prepare's output: Conv_0(n) @ Wᵀ.
+
+    [ts] ``#block`` (a = #conv(n, coef, 0), then q/k/v = projection(a) or gate/up = projection(m's
+    conv)); [max] ``DFlash2TransformerBlock`` (h = conv.prepare(norm(r)); h feeds the sublayer).
+    n: [B, G, H]; d_side0: [B, G, 2, groups] (side 0's deltas); base [2, 2, H]; W [N, H].
+    """
+    coef0 = coefficients(d_side0, base[0], group_size)                   # [B, G, 2, H]
+    a = conv_apply(n, coef0[..., 0, :], coef0[..., 1, :])
+    return projection(a, W)
+
+
+def sublayer_out(a, W, d_side1, base, group_size: int, residual=None) -> np.ndarray:
+    """The sublayer's output projection followed by finish: residual + Conv_1(a @ Wᵀ).
+
+    [ts] ``#block`` (out = o.forward(attn) or down.forward(prod); x = x + #conv(out, coef, 1));
+    [max] ``DFlash2TransformerBlock`` (r += conv.finish(sublayer output)).
+    a: [B, G, K]; W: [H, K]; d_side1: [B, G, 2, groups].
+    """
+    return conv_finish(projection(a, W), d_side1, base, group_size, residual=residual)

@@ -184,6 +184,52 @@ def zipf_bias(V: int, s: float = 1.1) -> np.ndarray:
     return (-s * np.log(np.arange(1, V + 1, dtype=np.float64))).astype(np.float32)
 
 
+def pack_int4(q: np.ndarray) -> np.ndarray:
+    """Storage of 4-bit codes q [N, K] (values 0..15): [N, K/8] uint32 words, code k in bits
+    4 (k % 8) .. 4 (k % 8) + 3 of word k / 8."""
+    q = np.asarray(q, dtype=np.uint32)
+    N, K = q.shape
+    w = np.zeros((N, K // 8), dtype=np.uint32)
+    for j in range(8):
+        w |= q[:, j::8] << np.uint32(4 * j)
+    return w
+
+
+def unpack_int4(w: np.ndarray, K: int) -> np.ndarray:
+    """The codes [N, K] (uint8) held by pack_int4's words."""
+    w = np.asarray(w, dtype=np.uint32)
+    q = np.empty((w.shape[0], K), dtype=np.uint8)
+    for j in range(8):
+        q[:, j::8] = (w >> np.uint32(4 * j)) & np.uint32(15)
+    return q
+
+
+@dataclass
+class Affine4:
+    """A seeded affine 4-bit weight [N, K] in groups of 64 along K: codes q, packed words, and
+    bf16 scales / biases [N, K/64] (bf16 bit patterns)."""
+    q: np.ndarray
+    packed: np.ndarray
+    scales: np.ndarray
+    biases: np.ndarray
+
+
+def affine4_weight(config_seed: int, name: str, N: int, K: int, exact: bool = False) -> Affine4:
+    """Uniform codes in [0, 15]. exact=False: scales ~ U(0.5, 1.5) / 64 and biases ~ N(0, 1/128).
+    exact=True: scales in {1/4, 1/8, 1/16} and biases in {-8..8} / 64, so that every
+    scale * q + bias (|.| < 4, a multiple of 1/64) is exactly a bf16 value."""
+    g = np.random.Generator(np.random.PCG64(_seed_for(config_seed, name)))
+    q = g.integers(0, 16, size=(N, K), dtype=np.int64).astype(np.uint8)
+    G = K // 64
+    if exact:
+        sc = np.float32(2.0) ** -g.integers(2, 5, size=(N, G)).astype(np.float32)
+        bi = g.integers(-8, 9, size=(N, G)).astype(np.float32) / np.float32(64.0)
+    else:
+        sc = g.uniform(0.5, 1.5, size=(N, G)).astype(np.float32) / np.float32(64.0)
+        bi = g.standard_normal((N, G)).astype(np.float32) / np.float32(128.0)
+    return Affine4(q=q, packed=pack_int4(q), scales=round_to_bf16_bits(sc), biases=round_to_bf16_bits(bi))
+
+
 # --------------------------------------------------------------------------- workloads
 
 @dataclass

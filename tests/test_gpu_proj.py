@@ -1,0 +1,201 @@
+"""GPU parity of the sublayer projections around a conv site (tcgen05 GEMM with the conv fused into
+its operand producer or its epilogue, bf16 or affine 4-bit weights) against the float64 oracle."""
+import numpy as np
+import pytest
+
+from oracle import dflash2_oracle as O
+from synth import inputs as I
+from tests.parity import REL_TOL, assert_close_scaled, record
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    from tests.gpu_util import require_gpu
+    return require_gpu()
+
+
+def _dev(a):
+    from dflash2_block_drafter_gb300.tail import to_device
+    return to_device(a)
+
+
+def _u32(packed):
+    import torch
+    return torch.from_numpy(packed.view(np.int32)).cuda()
+
+
+def _bound(a64, W64):
+    """fp32 accumulation over K of exact bf16 products, then one bf16 rounding of the output."""
+    K = a64.shape[-1]
+    s = np.abs(a64) @ np.abs(W64).T
+    return K * 2.0 ** -24 * s + 2.0 ** -8 * np.abs(a64 @ W64.T)
+
+
+def _conv_case(seed, B, G, H, gs):
+    n = I.normal(seed, "n", (B * G, H), 1.0)
+    d = I.normal(seed, "d", (B * G, 2, 2, H // gs), 0.2, dtype="f32")
+    base = np.zeros((2, 2, H), np.float32)
+    base[:, 0] = 1.0
+    base += I.normal(seed, "base", (2, 2, H), 0.1, dtype="f32")
+    return n, d, base
+
+
+@pytest.mark.parametrize("M,K,N", [(16, 256, 256), (300, 512, 264), (1024, 5120, 512), (129, 128, 1000)])
+def test_proj_bf16(torch, M, K, N):
+    import dflash2_block_drafter_gb300 as d
+    a = I.normal(M, "a", (M, K), 1.0)
+    W = I.normal(M, "W", (N, K), K ** -0.5)
+    y = d.dflash2_proj(_dev(a), _dev(W))
+    assert d.dflash2_poll_error() == 0
+    got = y.float().cpu().numpy().astype(np.float64)
+    ref = O.projection(I.to_f64(a), I.to_f64(W))
+    assert_close_scaled(got, ref, what="projection")
+    assert np.all(np.abs(got - ref) <= _bound(I.to_f64(a), I.to_f64(W))), "outside the fp32-accumulation bound"
+
+
+@pytest.mark.parametrize("M,K,N", [(48, 256, 128), (272, 5120, 520)])
+def test_proj_w4_exact_codes_equal_the_bf16_weight(torch, M, K, N):
+    """4-bit weights whose scale * q + bias are bf16 values: the dequantised operand is exact, so the
+    W4 GEMM equals the bf16 GEMM on that weight bit for bit (same tiles, same accumulation order)."""
+    import dflash2_block_drafter_gb300 as d
+    q = I.affine4_weight(M + N, "w4", N, K, exact=True)
+    W = O.affine_dequantize(q.q, I.to_f64(q.scales), I.to_f64(q.biases))
+    W_bf16 = I.round_to_bf16_bits(W.astype(np.float32))
+    assert np.array_equal(I.to_f64(W_bf16), W)       # exactly representable
+    a = _dev(I.normal(M, "a", (M, K), 1.0))
+    y4 = d.dflash2_proj(a, _u32(q.packed), w_scales=_dev(q.scales), w_biases=_dev(q.biases))
+    y16 = d.dflash2_proj(a, _dev(W_bf16))
+    assert d.dflash2_poll_error() == 0
+    assert torch.equal(y4, y16)
+
+
+def test_proj_w4_parity(torch):
+    import dflash2_block_drafter_gb300 as d
+    M, K, N = 200, 1024, 384
+    q = I.affine4_weight(7, "w4", N, K)
+    a = I.normal(7, "a", (M, K), 1.0)
+    y = d.dflash2_proj(_dev(a), _u32(q.packed), w_scales=_dev(q.scales), w_biases=_dev(q.biases))
+    assert d.dflash2_poll_error() == 0
+    W = O.affine_dequantize(q.q, I.to_f64(q.scales), I.to_f64(q.biases))
+    ref = O.projection(I.to_f64(a), W)
+    got = y.float().cpu().numpy().astype(np.float64)
+    assert_close_scaled(got, ref, what="W4 projection")
+    # the weight is rounded to bf16 once (relative 2^-9) before exact products and fp32 sums
+    assert np.all(np.abs(got - ref) <= _bound(I.to_f64(a), W) + 2.0 ** -9 * np.abs(I.to_f64(a)) @ np.abs(W).T)
+
+
+@pytest.mark.parametrize("B,G,H,gs,N", [(2, 16, 256, 16, 256), (9, 16, 5120, 16, 512), (5, 8, 512, 8, 136)])
+def test_proj_conv_in(torch, B, G, H, gs, N):
+    import dflash2_block_drafter_gb300 as d
+    n, D, base = _conv_case(B * G, B, G, H, gs)
+    W = I.normal(B, "W", (N, H), H ** -0.5)
+    d0 = np.ascontiguousarray(D[:, 0])                   # [M, 2, groups] side 0's deltas
+    y = d.dflash2_proj_conv_in(_dev(n), _dev(d0), _dev(base), G, gs, _dev(W))
+    assert d.dflash2_poll_error() == 0
+    ref = O.sublayer_in(I.to_f64(n).reshape(B, G, H), D.reshape(B, G, 2, 2, -1)[:, :, 0].astype(np.float64),
+                        base.astype(np.float64), gs, I.to_f64(W)).reshape(B * G, N)
+    rel = assert_close_scaled(y.float().cpu().numpy(), ref, what="conv side 0 + projection")
+    record(f"proj conv-in B={B} G={G} H={H} N={N}", max_rel_err=f"{rel:.2e}")
+    # identity coefficients: the fused operand is n itself, so the result is the plain GEMM's exactly
+    ident = np.zeros((2, 2, H), np.float32)
+    ident[0, 0] = 1.0
+    y_id = d.dflash2_proj_conv_in(_dev(n), _dev(np.zeros_like(d0)), _dev(ident), G, gs, _dev(W))
+    assert torch.equal(y_id, d.dflash2_proj(_dev(n), _dev(W)))
+
+
+@pytest.mark.parametrize("B,G,K,H,gs,res", [(2, 16, 256, 256, 16, True), (9, 16, 512, 5120, 16, True),
+                                            (12, 8, 128, 96, 8, False)])
+def test_proj_conv_out(torch, B, G, K, H, gs, res):
+    import dflash2_block_drafter_gb300 as d
+    M = B * G
+    a = I.normal(M, "a", (M, K), 1.0)
+    W = I.normal(M, "W", (H, K), K ** -0.5)
+    d1 = I.normal(M, "d1", (M, 2, H // gs), 0.2)          # bf16 side-1 deltas, as prepare stores them
+    base = np.zeros((2, 2, H), np.float32)
+    base[:, 0] = 1.0
+    base += I.normal(M, "base", (2, 2, H), 0.1, dtype="f32")
+    residual = I.normal(M, "res", (M, H), 1.0) if res else None
+    out = d.dflash2_proj_conv_out(_dev(a), _dev(W), _dev(d1), _dev(base), G, gs,
+                                  residual=_dev(residual) if res else None)
+    assert d.dflash2_poll_error() == 0
+    ref = O.sublayer_out(I.to_f64(a).reshape(B, G, K), I.to_f64(W), I.to_f64(d1).reshape(B, G, 2, -1),
+                         base.astype(np.float64), gs,
+                         residual=I.to_f64(residual).reshape(B, G, H) if res else None).reshape(M, H)
+    rel = assert_close_scaled(out.float().cpu().numpy(), ref, what="projection + conv side 1 + residual")
+    record(f"proj conv-out B={B} G={G} K={K} H={H}", max_rel_err=f"{rel:.2e}")
+
+
+def test_proj_conv_out_matches_finish_on_an_identity_weight(torch):
+    """With W = I the GEMM returns a exactly, so the fused epilogue must agree with
+    dflash2_conv_finish on the same rows to one bf16 rounding."""
+    import dflash2_block_drafter_gb300 as d
+    B, G, H, gs = 4, 16, 256, 16
+    M = B * G
+    a = I.normal(3, "a", (M, H), 1.0)
+    d1 = I.normal(3, "d1", (M, 2, H // gs), 0.2)
+    base = np.zeros((2, 2, H), np.float32)
+    base[:, 0] = 1.0
+    base += I.normal(3, "base", (2, 2, H), 0.1, dtype="f32")
+    residual = I.normal(3, "res", (M, H), 1.0)
+    eye = I.round_to_bf16_bits(np.eye(H, dtype=np.float32))
+    fused = d.dflash2_proj_conv_out(_dev(a), _dev(eye), _dev(d1), _dev(base), G, gs, residual=_dev(residual))
+    plain, _ = d.dflash2_conv_finish(_dev(a).view(B, G, H), _dev(d1).view(B, G, 2, H // gs), _dev(base), gs,
+                                     residual=_dev(residual).view(B, G, H))
+    assert d.dflash2_poll_error() == 0
+    f = fused.float().cpu().numpy()
+    p = plain.float().cpu().numpy().reshape(M, H)
+    assert np.all(np.abs(f - p) <= 2.0 ** -7 * np.maximum(np.abs(f), np.abs(p)) + 1e-6)
+
+
+def test_fused_site_equals_the_unfused_sequence(torch):
+    """One conv site around stand-in projections at the drafter's width, both ways: prepare ->
+    projection, projection -> finish (four launches with the conv's output and input in memory)
+    against coefficients -> fused input projection, fused output projection."""
+    import dflash2_block_drafter_gb300 as d
+    B, G, H, gs, N = 8, 16, 5120, 16, 1024
+    M = B * G
+    site = I.conv_site(11, "site", B, G, H, gs, "bf16")
+    x = _dev(I.normal(11, "x", (B, G, H), 1.0))
+    w_in = _dev(I.normal(11, "w_in", (N, H), H ** -0.5))
+    w_out = _dev(I.normal(11, "w_out", (H, N), N ** -0.5))
+    w_kp, base, norm_w = _dev(site.w_kp), _dev(site.base), _dev(site.norm_w)
+    # unfused
+    a, coef1 = d.dflash2_conv_prepare(x, norm_w, 1e-6, w_kp, base, gs)
+    u = d.dflash2_proj(a.view(M, H), w_in)
+    ref_out, _ = d.dflash2_conv_finish(d.dflash2_proj(u, w_out).view(B, G, H), coef1, base, gs, residual=x)
+    # fused
+    n, d0, c1 = d.dflash2_conv_coefficients(x, norm_w, 1e-6, w_kp, gs)
+    u2 = d.dflash2_proj_conv_in(n, d0, base, G, gs, w_in)
+    out = d.dflash2_proj_conv_out(u2, w_out, c1, base, G, gs, residual=x.view(M, H))
+    assert d.dflash2_poll_error() == 0
+    assert torch.equal(c1.view(-1), coef1.view(-1))
+    assert_close_scaled(u2.float().cpu().numpy(), u.float().cpu().numpy(), rel=1e-2, what="input projection")
+    assert_close_scaled(out.float().cpu().numpy(), ref_out.view(M, H).float().cpu().numpy(), rel=1e-2,
+                        what="site output")
+
+
+def test_proj_w4_with_both_conv_fusions(torch):
+    import dflash2_block_drafter_gb300 as d
+    B, G, H, gs, N = 4, 16, 512, 16, 256
+    M = B * G
+    n, D, base = _conv_case(5, B, G, H, gs)
+    q_in = I.affine4_weight(5, "w_in", N, H)
+    q_out = I.affine4_weight(5, "w_out", H, N)
+    d0 = np.ascontiguousarray(D[:, 0])
+    d1 = I.round_to_bf16_bits(np.ascontiguousarray(D[:, 1]))
+    u = d.dflash2_proj_conv_in(_dev(n), _dev(d0), _dev(base), G, gs, _u32(q_in.packed), w_scales=_dev(q_in.scales),
+                               w_biases=_dev(q_in.biases))
+    out = d.dflash2_proj_conv_out(u, _u32(q_out.packed), _dev(d1), _dev(base), G, gs, w_scales=_dev(q_out.scales),
+                                  w_biases=_dev(q_out.biases))
+    assert d.dflash2_poll_error() == 0
+    W_in = O.affine_dequantize(q_in.q, I.to_f64(q_in.scales), I.to_f64(q_in.biases))
+    W_out = O.affine_dequantize(q_out.q, I.to_f64(q_out.scales), I.to_f64(q_out.biases))
+    u_ref = O.sublayer_in(I.to_f64(n).reshape(B, G, H), D.reshape(B, G, 2, 2, -1)[:, :, 0].astype(np.float64),
+                          base.astype(np.float64), gs, W_in)
+    assert_close_scaled(u.float().cpu().numpy(), u_ref.reshape(M, N), what="W4 conv-in")
+    # the output side on the GPU's own (bf16) u, as the next GEMM sees it
+    out_ref = O.sublayer_out(u.float().cpu().numpy().astype(np.float64).reshape(B, G, N), W_out,
+                             I.to_f64(d1).reshape(B, G, 2, -1), base.astype(np.float64), gs)
+    assert_close_scaled(out.float().cpu().numpy(), out_ref.reshape(M, H), what="W4 conv-out")

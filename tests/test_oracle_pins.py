@@ -550,3 +550,56 @@ def test_ragged_tail_is_the_dense_tail_restricted_to_the_drafted_rows():
         np.testing.assert_allclose(rag["S"][i], dense["S"][b, l], rtol=1e-12, atol=1e-12)
     want, _ = O.select_path_depths(dense["S"], dense["cand"], depths)
     np.testing.assert_array_equal(rag["path"], want)
+
+
+def test_affine_dequantize_closed_forms():
+    # q = 0 gives the bias, q = 15 gives 15 * scale + bias, per row and per group of 64 channels;
+    # values worked by hand
+    q = np.zeros((2, 128), dtype=np.int64)
+    q[0, :64] = 15
+    q[1, 64:] = 3
+    scales = np.array([[0.5, 2.0], [0.25, 1.5]])
+    biases = np.array([[-1.0, 0.25], [0.0, -2.0]])
+    W = O.affine_dequantize(q, scales, biases)
+    assert np.all(W[0, :64] == 6.5) and np.all(W[0, 64:] == 0.25)
+    assert np.all(W[1, :64] == 0.0) and np.all(W[1, 64:] == 2.5)
+
+
+def test_int4_storage_roundtrip():
+    from synth import inputs as I
+    q = RNG.integers(0, 16, size=(5, 64))
+    w = I.pack_int4(q)
+    assert w.shape == (5, 8) and w.dtype == np.uint32
+    # code k of a row lives in bits 4 (k % 8) of word k / 8
+    assert (w[2, 3] >> 4 * 5) & 15 == q[2, 8 * 3 + 5]
+    np.testing.assert_array_equal(I.unpack_int4(w, 64), q)
+
+
+def test_sublayer_in_identity_and_shift_conv():
+    B, G, H, gs, N = 3, 4, 32, 16, 12
+    n = _rand(B, G, H)
+    W = _rand(N, H)
+    d0 = np.zeros((B, G, 2, H // gs))
+    ident = np.stack([np.stack([np.ones(H), np.zeros(H)]), np.zeros((2, H))])
+    np.testing.assert_allclose(O.sublayer_in(n, d0, ident, gs, W), n @ W.T, rtol=1e-13, atol=1e-13)
+    shift = np.stack([np.stack([np.zeros(H), np.ones(H)]), np.zeros((2, H))])
+    prev = np.zeros_like(n)
+    for b in range(B):             # the previous row of each block, a zero row before the block
+        for t in range(1, G):
+            prev[b, t] = n[b, t - 1]
+    np.testing.assert_allclose(O.sublayer_in(n, d0, shift, gs, W), prev @ W.T, rtol=1e-13, atol=1e-13)
+
+
+def test_sublayer_out_applies_the_projection_before_the_conv():
+    # With W a permutation of the channels, the conv acts on the permuted channels (the projection
+    # comes first); a zero W leaves the residual.
+    B, G, H, gs = 2, 5, 32, 16
+    a = _rand(B, G, H)
+    d1 = _rand(B, G, 2, H // gs, scale=0.3)
+    base = _rand(2, 2, H)
+    perm = RNG.permutation(H)
+    P = np.eye(H)[perm]            # (a @ P.T)[..., j] = a[..., perm[j]]
+    got = O.sublayer_out(a, P, d1, base, gs)
+    np.testing.assert_allclose(got, O.conv_finish(a[..., perm], d1, base, gs), rtol=1e-12, atol=1e-12)
+    res = _rand(B, G, H)
+    np.testing.assert_array_equal(O.sublayer_out(a, np.zeros((H, H)), d1, base, gs, residual=res), res)
