@@ -326,8 +326,8 @@ def proj_sweep(d, gen, dev, time_call, pk, G=16, H=5120, gs=16, N=5120):
     w_in = (torch.randn(N, H, generator=gen, device=dev) / H ** 0.5).to(torch.bfloat16)
     w_out = (torch.randn(H, N, generator=gen, device=dev) / N ** 0.5).to(torch.bfloat16)
     q_in = torch.randint(0, 2 ** 31 - 1, (N, H // 8), generator=gen, device=dev, dtype=torch.int32)
-    s_in = (torch.rand(N, H // 64, generator=gen, device=dev) / 64).to(torch.bfloat16)
-    b_in = (torch.randn(N, H // 64, generator=gen, device=dev) / 128).to(torch.bfloat16)
+    s_in = (torch.rand(H // 64, N, generator=gen, device=dev) / 64).to(torch.bfloat16)
+    b_in = (torch.randn(H // 64, N, generator=gen, device=dev) / 128).to(torch.bfloat16)
     points = []
     for B in (1, 8, 64):
         M = B * G
@@ -335,7 +335,7 @@ def proj_sweep(d, gen, dev, time_call, pk, G=16, H=5120, gs=16, N=5120):
         x = torch.randn(M, H, generator=gen, device=dev).to(torch.bfloat16)
         a = torch.empty_like(n)
         coef1 = torch.empty(B, G, 2, groups, dtype=torch.bfloat16, device=dev)
-        d0 = torch.empty(M, 2, groups, dtype=torch.float32, device=dev)
+        d0 = torch.empty(2, groups, M, dtype=torch.float32, device=dev)
         c1 = torch.empty(M, 2, groups, dtype=torch.bfloat16, device=dev)
         ws = torch.empty(d.dflash2_conv_prepare_workspace_bytes(B, G, H, gs, torch.bfloat16), dtype=torch.uint8,
                          device=dev)

@@ -408,7 +408,7 @@ def dflash2_score_edges_ragged(cand, unary, z, anchors, pred_book, succ_book, ro
 
 def _proj_weight(w, w_scales, w_biases, K):
     """(pointer args, wbits, N) of a projection weight: bf16 [N, K], or 4-bit words [N, K/8] (int32 or
-    uint32 storage) with bf16 scales / biases [N, K/64]."""
+    uint32 storage) with bf16 scales / biases [K/64, N] (group-major)."""
     if w_scales is None and w_biases is None:
         if w.dim() != 2 or w.shape[1] != K:
             raise ValueError(f"w must be [N, {K}] bf16, got shape {tuple(w.shape)}")
@@ -419,21 +419,21 @@ def _proj_weight(w, w_scales, w_biases, K):
         raise ValueError(f"packed 4-bit w must be [N, {K // 8}] 32-bit words, got {tuple(w.shape)} {w.dtype}")
     N = w.shape[0]
     for t, name in ((w_scales, "w_scales"), (w_biases, "w_biases")):
-        if tuple(t.shape) != (N, K // 64):
-            raise ValueError(f"{name} must be [{N}, {K // 64}], got {tuple(t.shape)}")
+        if tuple(t.shape) != (K // 64, N):
+            raise ValueError(f"{name} must be [{K // 64}, {N}] (group-major), got {tuple(t.shape)}")
     return (_dev(w, "w"), _dev(w_scales, "w_scales", torch.bfloat16), _dev(w_biases, "w_biases", torch.bfloat16)), 4, N
 
 
 def dflash2_conv_coefficients(x, norm_w, eps, w_kp, group_size, n_out=None, d0=None, coef1=None, workspace=None,
                               stream=None, taps=2):
     """Prepare without the side-0 output: returns (n [B*G, H] (x itself when norm_w is None), d0
-    [B*G, 2, groups] fp32, coef1 [B*G, 2, groups])."""
+    [2, groups, B*G] fp32 (side 0's deltas, tap-and-group major), coef1 [B*G, 2, groups])."""
     B, G, H = x.shape
     groups = H // group_size
     dt = x.dtype
     if norm_w is not None and n_out is None:
         n_out = torch.empty((B * G, H), dtype=dt, device=x.device)
-    d0 = torch.empty((B * G, 2, groups), dtype=torch.float32, device=x.device) if d0 is None else d0
+    d0 = torch.empty((2, groups, B * G), dtype=torch.float32, device=x.device) if d0 is None else d0
     coef1 = torch.empty((B * G, 2, groups), dtype=dt, device=x.device) if coef1 is None else coef1
     for t, n, name in ((d0, B * G * 2 * groups, "d0"), (coef1, B * G * 2 * groups, "coef1")):
         if t.numel() < n:
@@ -465,7 +465,8 @@ def dflash2_proj(a, w, w_scales=None, w_biases=None, out=None, stream=None):
 
 
 def dflash2_proj_conv_in(n, d0, base, G, group_size, w, w_scales=None, w_biases=None, out=None, stream=None):
-    """out = Conv_0(n) . W^T with the conv's side 0 computed inside the GEMM (n [M, K = H])."""
+    """out = Conv_0(n) . W^T with the conv's side 0 computed inside the GEMM (n [M, K = H]; d0
+    [2, K / 16, M] fp32 as dflash2_conv_coefficients returns it)."""
     M, K = n.shape
     wp, wbits, N = _proj_weight(w, w_scales, w_biases, K)
     if d0.numel() < M * 2 * (K // group_size) or base.numel() < 4 * K:

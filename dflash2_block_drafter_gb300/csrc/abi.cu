@@ -242,7 +242,9 @@ static int check_proj(const void* a, int M, int K, const void* w, const void* w_
   REQUIRE(K >= 64 && K % 64 == 0, "K=%d must be a positive multiple of 64", K);
   REQUIRE(N >= 8 && N % 8 == 0, "N=%d must be a positive multiple of 8", N);
   REQUIRE(wbits == 16 || wbits == 4, "wbits=%d must be 16 (bf16) or 4 (affine 4-bit, groups of 64)", wbits);
-  if (wbits == 4) REQUIRE(w_scales && w_biases, "4-bit weights need w_scales and w_biases");
+  if (wbits == 4)
+    REQUIRE(w_scales && w_biases && aligned16(w_scales) && aligned16(w_biases),
+            "4-bit weights need 16-byte aligned w_scales and w_biases");
   REQUIRE(aligned16(a) && aligned16(w) && aligned16(out), "a, w and out must be 16-byte aligned");
   return DFLASH2_OK;
 }
@@ -265,10 +267,9 @@ int dflash2_proj_conv_in(const void* n, const float* d0, const float* base, int 
   REQUIRE(d0 && base, "d0 and base are required");
   REQUIRE(G >= 2 && G <= 64 && 128 % G == 0, "G=%d must divide 128 (blocks must not straddle a 128-row tile)", G);
   REQUIRE(M % G == 0, "M=%d must be a whole number of %d-row blocks", M, G);
-  REQUIRE(group_size == 8 || group_size == 16 || group_size == 32 || group_size == 64,
-          "group_size=%d must be 8, 16, 32 or 64", group_size);
-  REQUIRE(K % group_size == 0, "K=%d must be a multiple of group_size=%d", K, group_size);
-  REQUIRE(aligned16(base), "base must be 16-byte aligned");
+  REQUIRE(group_size == 16, "group_size=%d: the fused side 0 is built for groups of 16 channels", group_size);
+  REQUIRE(M % 4 == 0, "M=%d must be a multiple of 4 (rows of the side-0 deltas are loaded in 16-byte units)", M);
+  REQUIRE(aligned16(base) && aligned16(d0), "base and d0 must be 16-byte aligned");
   ProjSpec p{};
   p.a = n; p.w = w; p.scales = w_scales; p.qbias = w_biases; p.wbits = wbits;
   p.M = M; p.N = N; p.K = K; p.out = out;

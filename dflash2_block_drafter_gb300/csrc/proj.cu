@@ -22,10 +22,12 @@
 // swizzled row, as TMA writes it, and the producer warps write their tiles in the same layout
 // (16-byte chunk c of row r at chunk position c ^ (r & 7) of the row, 1024-byte aligned tiles).
 // Warp roles: 0 TMA, 1 TMEM + MMA issue (one lane), 2-5 epilogue (TMEM lanes 32 (w % 4) ..),
-// then 4 conv-producer warps (one tile row per thread) and/or 4 dequant warps (two weight rows
-// per thread). The accumulator is double-buffered in TMEM (2 x 256 columns). Every wait is
-// bounded: a timeout raises a CTA-wide abort flag, records DFLASH2_ERR_TIMEOUT, drains the copies
-// and MMAs in flight and frees TMEM before the kernel returns.
+// then 8 conv-producer warps and/or 8 dequant warps (a 16-byte chunk of a few rows per thread,
+// packed fp32 or bf16 pair arithmetic). Producer and epilogue warps wait with suspending
+// try_waits, leaving the issue slots to the warps that work. The accumulator is double-buffered
+// in TMEM (2 x 256 columns). Every wait is bounded: a timeout raises a CTA-wide abort flag,
+// records DFLASH2_ERR_TIMEOUT, drains the copies and MMAs in flight and frees TMEM before the
+// kernel returns.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -37,39 +39,58 @@ namespace dfl {
 namespace {
 
 constexpr int kPM = 128;                     // rows per tile
-constexpr int kPN = 256;                     // columns per tile
 constexpr int kPK = 64;                      // K per stage (one 128-byte bf16 row)
 constexpr int kAOp = kPM * 128;              // A operand tile bytes
-constexpr int kBOp = kPN * 128;              // B operand tile bytes
-constexpr int kARaw = kPM * 128 + 1024;      // normed rows + side-0 base chunk (2 x 64 fp32), padded
-constexpr int kBRaw = kPN * 32;              // 64 packed 4-bit values per weight row
 constexpr int kQGroup = 64;                  // quantisation group along K
 constexpr uint64_t kPDrainNs = 100000000ull; // 100 ms
 constexpr int kPSmemLimit = 232448;
 
-template <int AM, int BM, int EM>
+// Stage layout (every part 1024-byte aligned): the A operand (AM: the normed rows n land there
+// and the producer warps turn them into Conv_0(n) in place), the B operand, then (AM) side 0's base
+// kernel [2][64] fp32 and the rows' side-0 deltas [2 taps][4 groups][128 rows] fp32 (group size 16),
+// then (BM) the
+// packed codes [NT][8 words] and the scales and biases [NT] of the stage's group.
+template <int AM, int BM, int NT>
+struct PLayout {
+  static constexpr int kBOp = NT * 128;
+  static constexpr int kOffBase = kAOp + kBOp;
+  static constexpr int kOffD0 = kOffBase + 1024;
+  static constexpr int kARaw = AM ? 1024 + kPM * 2 * 4 * 4 : 0;
+  static constexpr int kOffBRaw = kOffBase + kARaw;
+  static constexpr int kOffScale = kOffBRaw + NT * 32;
+  static constexpr int kOffBias = kOffScale + NT * 2;
+  static constexpr int kBRaw = BM ? ((NT * 32 + NT * 4 + 1023) / 1024) * 1024 : 0;
+  static constexpr int kStageBytes = kAOp + kBOp + kARaw + kBRaw;
+};
+
+template <int AM, int BM, int EM, int NT>
 struct PCfg {
-  static constexpr int kProdWarps = (AM ? 4 : 0) + (BM ? 4 : 0);
+  static constexpr int kConvWarps = AM ? 8 : 0;
+  static constexpr int kDeqWarps = BM ? 8 : 0;
+  static constexpr int kProdWarps = kConvWarps + kDeqWarps;
   static constexpr int kThreads = 64 + 128 + 32 * kProdWarps;
-  static constexpr int kStageBytes = kAOp + kBOp + (AM ? kARaw : 0) + (BM ? kBRaw : 0);
+  static constexpr int kStageBytes = PLayout<AM, BM, NT>::kStageBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kFit = (kPSmemLimit - 1024 - kBarBytes) / kStageBytes;
-  static constexpr int kStages = kFit > 6 ? 6 : kFit;
+  static constexpr int kStages = kFit > 8 ? 8 : kFit;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kTmemCols = NT == 256 ? 512 : 128;  // two accumulator buffers
 };
 
 struct ProjArgs {
   int M, N, K;
+  int a_rows;                  // rows of the A box (up to 128: fewer when M is small)
   int tiles_m, tiles_n;
-  int G, gs, groups;           // conv shape (G rows per block, group size, H / group size)
-  const float* d0;             // AM: side-0 deltas [M][2][groups] fp32
+  int G, gs, groups;           // conv shape (G rows per block, group size, channels / group size)
   const __nv_bfloat16* coef1;  // EM: side-1 deltas [M][2][groups] bf16
-  const float* base;           // [2][2][H] fp32 (AM: side 0 over K; EM: side 1 over N)
+  const float* base;           // EM: [2][2][N] fp32 (side 1 is used)
   const __nv_bfloat16* residual;  // EM: [M][N] or null
-  const __nv_bfloat16* scales;    // BM: [N][K / 64]
-  const __nv_bfloat16* qbias;     // BM: [N][K / 64]
   __nv_bfloat16* out;          // [M][N]
   int* err;
+};
+
+struct ProjMaps {
+  CUtensorMap a, b, base, d0, scales, biases;
 };
 
 __device__ __forceinline__ void p_abort(volatile int* abort_flag, int* err) {
@@ -97,11 +118,33 @@ __device__ __forceinline__ uint4 f32x8_to_bf16(const float (&f)[8]) {
   return u;
 }
 
-template <int AM, int BM, int EM>
-__global__ void __launch_bounds__(PCfg<AM, BM, EM>::kThreads, 1)
-    proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmBase, const ProjArgs a) {
-  using C = PCfg<AM, BM, EM>;
+// The epilogue operands of one 32-column chunk of one row (conv side 1 + residual).
+struct EpiChunk {
+  uint4 res[4];   // residual, bf16
+  float d[2][4];  // side-1 deltas of the chunk's groups (up to 4: gs >= 8)
+};
+__device__ __forceinline__ void load_epi_chunk(EpiChunk& e, const ProjArgs& a, bool valid, int row, int col0) {
+  const bool in = valid && col0 < a.N;
+#pragma unroll
+  for (int v = 0; v < 4; ++v)
+    e.res[v] = (in && a.residual != nullptr)
+                   ? __ldg(reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(row) * a.N + col0 + 8 * v))
+                   : make_uint4(0u, 0u, 0u, 0u);
+  const int gpc = 32 / a.gs;
+#pragma unroll
+  for (int tap = 0; tap < 2; ++tap)
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi)
+      e.d[tap][gi] = (in && gi < gpc) ? __bfloat162float(
+                                            a.coef1[(static_cast<size_t>(row) * 2 + tap) * a.groups + col0 / a.gs + gi])
+                                      : 0.f;
+}
+
+template <int AM, int BM, int EM, int NT>
+__global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
+    proj_kernel(const __grid_constant__ ProjMaps maps, const ProjArgs a) {
+  using C = PCfg<AM, BM, EM, NT>;
+  using L = PLayout<AM, BM, NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* bar_area = smem + C::kStages * C::kStageBytes;
@@ -118,6 +161,7 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int k_stages = a.K / kPK;
   const int n_tiles = a.tiles_m * a.tiles_n;
+  const int gpc = AM ? kPK / 16 : 1;  // groups per stage (conv side 0 over K, group size 16)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -132,12 +176,19 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM>::kThreads, 1)
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
-    if (AM) prefetch_tmap(&tmBase);
+    prefetch_tmap(&maps.a);
+    prefetch_tmap(&maps.b);
+    if (AM) {
+      prefetch_tmap(&maps.base);
+      prefetch_tmap(&maps.d0);
+    }
+    if (BM) {
+      prefetch_tmap(&maps.scales);
+      prefetch_tmap(&maps.biases);
+    }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -152,12 +203,14 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM>::kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_a = policy_evict_last();   // activations: re-read by every column tile
       const uint64_t pol_w = policy_evict_normal(); // weights: shared by the CTAs of one column tile
+      const uint32_t bytes = static_cast<uint32_t>(a.a_rows * 128 + (BM ? NT * 32 + NT * 4 : NT * 128) +
+                                                   (AM ? 2 * kPK * 4 + a.a_rows * 2 * gpc * 4 : 0));
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         const int m0 = (t % a.tiles_m) * kPM;
-        const int n0 = (t / a.tiles_m) * kPN;
+        const int n0 = (t / a.tiles_m) * NT;
         for (int kb = 0; kb < k_stages; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
@@ -165,12 +218,19 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM>::kThreads, 1)
           }
           const uint32_t fb = smem_u32(&full[stage]);
           uint8_t* st = smem + stage * C::kStageBytes;
-          uint8_t* a_dst = AM ? st + kAOp + kBOp : st;                             // raw rows or the operand
-          uint8_t* b_dst = BM ? st + kAOp + kBOp + (AM ? kARaw : 0) : st + kAOp;  // packed or the operand
-          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kPM * 128 + (AM ? 2 * kPK * 4 : 0) + (BM ? kBRaw : kBOp)));
-          tma_load_2d(smem_u32(a_dst), &tmA, fb, kb * kPK, m0, pol_a);
-          if (AM) tma_load_2d(smem_u32(a_dst + kPM * 128), &tmBase, fb, kb * kPK, 0, pol_a);
-          tma_load_2d(smem_u32(b_dst), &tmB, fb, BM ? kb * (kPK / 8) : kb * kPK, n0, pol_w);
+          mbar_arrive_expect_tx(fb, bytes);
+          tma_load_2d(smem_u32(st), &maps.a, fb, kb * kPK, m0, pol_a);
+          if (AM) {
+            tma_load_2d(smem_u32(st + L::kOffBase), &maps.base, fb, kb * kPK, 0, pol_a);
+            tma_load_3d(smem_u32(st + L::kOffD0), &maps.d0, fb, m0, kb * gpc, 0, pol_a);
+          }
+          if (BM) {
+            tma_load_2d(smem_u32(st + L::kOffBRaw), &maps.b, fb, kb * (kPK / 8), n0, pol_w);
+            tma_load_2d(smem_u32(st + L::kOffScale), &maps.scales, fb, n0, kb, pol_w);
+            tma_load_2d(smem_u32(st + L::kOffBias), &maps.biases, fb, n0, kb, pol_w);
+          } else {
+            tma_load_2d(smem_u32(st + kAOp), &maps.b, fb, kb * kPK, n0, pol_w);
+          }
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -201,7 +261,7 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM>::kThreads, 1)
       int stage = 0, tile_i = 0;
       uint32_t phase = 0;
       bool ok = true, any = false;
-      const uint32_t idesc = make_idesc(false, kPM, kPN);
+      const uint32_t idesc = make_idesc(false, kPM, NT);
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++tile_i) {
         const int ab = tile_i & 1;
         const uint32_t acc_par = static_cast<uint32_t>(tile_i >> 1) & 1u;
@@ -222,7 +282,7 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM>::kThreads, 1)
           const uint64_t bdesc = desc_kmajor_swizzled<128>(sa + kAOp);
 #pragma unroll
           for (int k = 0; k < 4; ++k)  // 16-element (32-byte) steps along the swizzled row
-            mma_f16(tmem_base + static_cast<uint32_t>(ab * kPN), adesc + static_cast<uint64_t>(2 * k),
+            mma_f16(tmem_base + static_cast<uint32_t>(ab * NT), adesc + static_cast<uint64_t>(2 * k),
                     bdesc + static_cast<uint64_t>(2 * k), idesc, (kb > 0 || k > 0) ? 1u : 0u);
           mma_commit(smem_u32(&empty[stage]));
           any = true;
@@ -249,77 +309,63 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM>::kThreads, 1)
     int tile_i = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_i) {
       const int m0 = (t % a.tiles_m) * kPM;
-      const int n0 = (t / a.tiles_m) * kPN;
+      const int n0 = (t / a.tiles_m) * NT;
       const int row = m0 + q * 32 + lane;
       const bool valid = row < a.M;
       const int ab = tile_i & 1;
       const uint32_t acc_par = static_cast<uint32_t>(tile_i >> 1) & 1u;
-      if (!mbar_wait_bounded(smem_u32(&acc_full[ab]), acc_par, abort_flag, kWaitLimitNs)) {
+      const int trow = row % a.G;  // EM: the row's position in its block
+      EpiChunk nxt;
+      if (EM) load_epi_chunk(nxt, a, valid, row, n0);  // the first chunk's operands, before the wait
+      if (!mbar_wait_bounded_suspend(smem_u32(&acc_full[ab]), acc_par, abort_flag, kWaitLimitNs)) {
         if (lane == 0) p_abort(abort_flag, a.err);
         break;
       }
       tc_fence_after();
-      const int trow = row % a.G;  // EM: the row's position in its block
-      for (int cc = 0; cc < kPN / 32; ++cc) {
+      for (int cc = 0; cc < NT / 32; ++cc) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ab * kPN + cc * 32),
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ab * NT + cc * 32),
                            r);
-        tmem_ld_wait();
         const int col0 = n0 + cc * 32;
+        EpiChunk cur;
+        if (EM) {
+          cur = nxt;
+          if (cc + 1 < NT / 32) load_epi_chunk(nxt, a, valid, row, col0 + 32);  // in flight during this chunk
+        }
+        tmem_ld_wait();
         float y[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(r[j]);
         if (EM) {
-          // x = residual + (b10 + d10) * y[m] + (b11 + d11) * y[m - 1]; y[m - 1] is lane - 1's value
+          // x = residual + (b10 + d10) y[m] + (b11 + d11) y[m - 1]; y[m - 1] is lane - 1's value
           // (lane 0's row 32w starts a block, as G divides 32)
-          float d[2][32 / 8];
-          const int gpc = 32 / a.gs;  // groups in these 32 columns (gs >= 8)
-#pragma unroll
-          for (int tap = 0; tap < 2; ++tap)
-#pragma unroll
-            for (int gi = 0; gi < 4; ++gi)
-              d[tap][gi] = (valid && gi < gpc)
-                               ? __bfloat162float(a.coef1[(static_cast<size_t>(row) * 2 + tap) * a.groups +
-                                                          col0 / a.gs + gi])
-                               : 0.f;
-          // side 1's base kernel of these columns (the same for every lane: broadcast loads)
-          float b1[2][32];
-#pragma unroll
-          for (int tap = 0; tap < 2; ++tap)
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const float4 f4 = col0 + 4 * v < a.N
-                                    ? __ldg(reinterpret_cast<const float4*>(a.base + (2 + tap) * static_cast<size_t>(a.N) +
-                                                                            col0 + 4 * v))
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-              b1[tap][4 * v] = f4.x;
-              b1[tap][4 * v + 1] = f4.y;
-              b1[tap][4 * v + 2] = f4.z;
-              b1[tap][4 * v + 3] = f4.w;
-            }
-          float res[32];
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            float f[8];
-            if (valid && a.residual != nullptr && col0 + 8 * v < a.N) {
-              bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(row) * a.N +
-                                                                 col0 + 8 * v)),
-                            f);
-            } else {
+            float res[8];
+            bf16x8_to_f32(cur.res[v], res);
+            const bool in = col0 + 8 * v < a.N;
+            const float4 b0a = in ? __ldg(reinterpret_cast<const float4*>(a.base + 2 * static_cast<size_t>(a.N) +
+                                                                          col0 + 8 * v))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 b0b = in ? __ldg(reinterpret_cast<const float4*>(a.base + 2 * static_cast<size_t>(a.N) +
+                                                                          col0 + 8 * v + 4))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 b1a = in ? __ldg(reinterpret_cast<const float4*>(a.base + 3 * static_cast<size_t>(a.N) +
+                                                                          col0 + 8 * v))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 b1b = in ? __ldg(reinterpret_cast<const float4*>(a.base + 3 * static_cast<size_t>(a.N) +
+                                                                          col0 + 8 * v + 4))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float bb0[8] = {b0a.x, b0a.y, b0a.z, b0a.w, b0b.x, b0b.y, b0b.z, b0b.w};
+            const float bb1[8] = {b1a.x, b1a.y, b1a.z, b1a.w, b1b.x, b1b.y, b1b.z, b1b.w};
 #pragma unroll
-              for (int e = 0; e < 8; ++e) f[e] = 0.f;
+            for (int e = 0; e < 8; ++e) {
+              const int j = 8 * v + e;
+              float yp = __shfl_up_sync(0xffffffffu, y[j], 1);
+              if (lane == 0 || trow == 0) yp = 0.f;
+              const int gi = j / a.gs;
+              y[j] = res[e] + ((bb0[e] + cur.d[0][gi]) * y[j] + (bb1[e] + cur.d[1][gi]) * yp);
             }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) res[8 * v + e] = f[e];
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float yp = __shfl_up_sync(0xffffffffu, y[j], 1);
-            if (lane == 0 || trow == 0) yp = 0.f;
-            const int gi = j / a.gs;
-            const float c0 = b1[0][j] + d[0][gi];
-            const float c1 = b1[1][j] + d[1][gi];
-            y[j] = res[j] + (c0 * y[j] + c1 * yp);
           }
         }
         if (valid) {
@@ -338,52 +384,87 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
     }
-  } else if (AM && warp < 10) {
+  } else if (AM && warp < 6 + C::kConvWarps) {
     // ------------------------------------------------------------------ conv side-0 producer
-    // Thread r owns tile row r: A[r, k] = (b00[k] + d00) n[r, k] + (b01[k] + d01) n[r - 1, k].
-    const int r = threadIdx.x - 192;
+    // Thread (rg, c) owns 16-byte chunk c (8 channels, inside one 16-channel group) of the tile rows
+    // rg * rpt .. rg * rpt + rpt - 1 (32 row groups over the A box's rows, rpt <= 4), turned in place
+    // into A[r, k] = (b00[k] + d00[r]) n[r, k] + (b01[k] + d01[r]) n[r - 1, k] (n[r - 1] = 0 at a
+    // block start). Every load of the stage is issued before any arithmetic. The row before a
+    // thread's first row belongs to another thread: it is read before the producer warps' barrier,
+    // and every write follows it.
+    const int pt = threadIdx.x - 192;
+    const int c = pt & 7;
+    const int rg = pt >> 3;
+    const int rpt = (a.a_rows + 31) / 32;
+    const int r_first = rg * rpt;
+    const int nr = max(0, min(rpt, a.a_rows - r_first));
+    const int gi = c >> 1;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
       const int m0 = (t % a.tiles_m) * kPM;
-      const int row = m0 + r;
-      const bool first = (row % a.G) == 0 || row >= a.M;
+      const int row_first = m0 + r_first;
+      const int t_first = row_first % a.G;
       for (int kb = 0; kb < k_stages; ++kb) {
-        // this row's side-0 deltas of the stage's groups (at most 8: gs >= 8)
-        const int gpc = kPK / a.gs;
-        float d0[2][8];
-#pragma unroll
-        for (int tap = 0; tap < 2; ++tap)
-#pragma unroll
-          for (int gi = 0; gi < 8; ++gi)
-            d0[tap][gi] = (row < a.M && gi < gpc)
-                              ? __ldg(a.d0 + (static_cast<size_t>(row) * 2 + tap) * a.groups + kb * gpc + gi)
-                              : 0.f;
-        if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait_bounded_suspend(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs, 200)) {
           ok = false;
           break;
         }
         uint8_t* st = smem + stage * C::kStageBytes;
-        const uint8_t* raw = st + kAOp + kBOp;
-        const float* b0 = reinterpret_cast<const float*>(raw + kPM * 128);  // [2][64]
+        uint4 raw[5];  // raw[0]: the row before the first; raw[1 + i]: row r_first + i
+        raw[0] = (nr > 0 && t_first != 0) ? *reinterpret_cast<const uint4*>(st + sw128(r_first - 1, c))
+                                          : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float cur[8], prv[8], o[8];
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(raw + sw128(r, c)), cur);
-          if (!first) {
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(raw + sw128(r - 1, c)), prv);
+        for (int i = 0; i < 4; ++i)
+          raw[1 + i] = i < nr ? *reinterpret_cast<const uint4*>(st + sw128(r_first + i, c)) : make_uint4(0u, 0u, 0u, 0u);
+        asm volatile("bar.sync 1, 256;" ::: "memory");  // every row this stage needs is read before any write
+        if (nr > 0) {
+          const float* b0 = reinterpret_cast<const float*>(st + L::kOffBase);  // [2][64]
+          const float* d0s = reinterpret_cast<const float*>(st + L::kOffD0);   // [2][4][a_rows]
+          const float4 x0 = *reinterpret_cast<const float4*>(b0 + 8 * c);
+          const float4 x1 = *reinterpret_cast<const float4*>(b0 + 8 * c + 4);
+          const float4 y0 = *reinterpret_cast<const float4*>(b0 + kPK + 8 * c);
+          const float4 y1 = *reinterpret_cast<const float4*>(b0 + kPK + 8 * c + 4);
+          // the thread's rows' deltas: r_first is a multiple of rpt, and rpt divides 4 when it is 4
+          float dd0[4], dd1[4];
+          if (rpt == 4) {
+            const float4 u0 = *reinterpret_cast<const float4*>(d0s + gi * a.a_rows + r_first);
+            const float4 u1 = *reinterpret_cast<const float4*>(d0s + (4 + gi) * a.a_rows + r_first);
+            dd0[0] = u0.x; dd0[1] = u0.y; dd0[2] = u0.z; dd0[3] = u0.w;
+            dd1[0] = u1.x; dd1[1] = u1.y; dd1[2] = u1.z; dd1[3] = u1.w;
           } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) prv[e] = 0.f;
+            for (int i = 0; i < 4; ++i) {
+              dd0[i] = i < nr ? d0s[gi * a.a_rows + r_first + i] : 0.f;
+              dd1[i] = i < nr ? d0s[(4 + gi) * a.a_rows + r_first + i] : 0.f;
+            }
           }
+          const float2 k0[4] = {make_float2(x0.x, x0.y), make_float2(x0.z, x0.w), make_float2(x1.x, x1.y),
+                                make_float2(x1.z, x1.w)};
+          const float2 k1[4] = {make_float2(y0.x, y0.y), make_float2(y0.z, y0.w), make_float2(y1.x, y1.y),
+                                make_float2(y1.z, y1.w)};
+          int trow = t_first;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int k = 8 * c + e;
-            const int gi = k / a.gs;
-            o[e] = (b0[k] + d0[0][gi]) * cur[e] + (b0[kPK + k] + d0[1][gi]) * prv[e];
+          for (int i = 0; i < 4; ++i) {
+            if (i < nr) {
+              const __nv_bfloat162* hc = reinterpret_cast<const __nv_bfloat162*>(&raw[1 + i]);
+              const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
+              const float2 d0p = make_float2(dd0[i], dd0[i]), d1p = make_float2(dd1[i], dd1[i]);
+              const float2 keep = trow == 0 ? make_float2(0.f, 0.f) : make_float2(1.f, 1.f);
+              uint4 o;
+              __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 cur = __bfloat1622float2(hc[e]);
+                const float2 prv = __fmul2_rn(__bfloat1622float2(hp[e]), keep);  // 0 at a block start
+                const float2 v = __ffma2_rn(__fadd2_rn(k0[e], d0p), cur, __fmul2_rn(__fadd2_rn(k1[e], d1p), prv));
+                oh[e] = __floats2bfloat162_rn(v.x, v.y);
+              }
+              *reinterpret_cast<uint4*>(st + sw128(r_first + i, c)) = o;
+              if (++trow == a.G) trow = 0;
+            }
           }
-          *reinterpret_cast<uint4*>(st + sw128(r, c)) = f32x8_to_bf16(o);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -397,55 +478,42 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM>::kThreads, 1)
     if (!ok && lane == 0) p_abort(abort_flag, a.err);
   } else if (BM) {
     // ------------------------------------------------------------------ W4A16 dequant producer
-    // Thread i owns weight rows i and i + 128 of the tile: W = scale * q + bias in bf16 (one
-    // rounding of the exact value), written as swizzled 128-byte rows of the B operand.
-    const int i = threadIdx.x - 192 - (AM ? 128 : 0);
-    const int kq = a.K / kQGroup;
+    // Chunk jobs (row, c): the 8 codes of word c of a weight row become 8 bf16 values
+    // scale * q + bias (one rounding of the exact value), a 16-byte chunk of the swizzled operand.
+    const int pt = threadIdx.x - 192 - 32 * C::kConvWarps;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
     for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
-      const int n0 = (t / a.tiles_m) * kPN;
       for (int kb = 0; kb < k_stages; ++kb) {
-        __nv_bfloat162 sc2[2], bi2[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int n = n0 + i + 128 * h;
-          const __nv_bfloat16 s = n < a.N ? a.scales[static_cast<size_t>(n) * kq + kb] : __float2bfloat16(0.f);
-          const __nv_bfloat16 b = n < a.N ? a.qbias[static_cast<size_t>(n) * kq + kb] : __float2bfloat16(0.f);
-          sc2[h] = __halves2bfloat162(s, s);
-          bi2[h] = __halves2bfloat162(b, b);
-        }
-        if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+        if (!mbar_wait_bounded_suspend(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs, 200)) {
           ok = false;
           break;
         }
         uint8_t* st = smem + stage * C::kStageBytes;
-        const uint8_t* raw = st + kAOp + kBOp + (AM ? kARaw : 0);
-        const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
+        const uint32_t* words = reinterpret_cast<const uint32_t*>(st + L::kOffBRaw);  // [NT][8]
+        const __nv_bfloat16* sc = reinterpret_cast<const __nv_bfloat16*>(st + L::kOffScale);
+        const __nv_bfloat16* bi = reinterpret_cast<const __nv_bfloat16*>(st + L::kOffBias);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int rr = i + 128 * h;
-          const uint4 p0 = *reinterpret_cast<const uint4*>(raw + rr * 32);
-          const uint4 p1 = *reinterpret_cast<const uint4*>(raw + rr * 32 + 16);
-          const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        for (int i = 0; i < NT / 32; ++i) {
+          const int job = pt + 256 * i;
+          const int rr = job >> 3;
+          const int c = job & 7;
+          const uint32_t w = words[rr * 8 + c];
+          const __nv_bfloat162 s2 = __halves2bfloat162(sc[rr], sc[rr]);
+          const __nv_bfloat162 b2 = __halves2bfloat162(bi[rr], bi[rr]);
+          uint32_t o[4];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {  // word c holds k = 8c .. 8c + 7, nibble j = k - 8c
-            const uint32_t w = words[c];
-            uint32_t o[4];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              // bf16 pair (128 + q[2jj], 128 + q[2jj + 1]): 0x4300 | nibble is 128 + nibble exactly
-              const uint32_t lo = (w >> (8 * jj)) & 0xFu;
-              const uint32_t hi = (w >> (8 * jj + 4)) & 0xFu;
-              const uint32_t pair = 0x43004300u | lo | (hi << 16);
-              __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pair);
-              v = __hsub2(v, k128);              // exact: q
-              v = __hfma2(sc2[h], v, bi2[h]);    // scale * q + bias, one rounding
-              o[jj] = *reinterpret_cast<const uint32_t*>(&v);
-            }
-            *reinterpret_cast<uint4*>(st + kAOp + sw128(rr, c)) = make_uint4(o[0], o[1], o[2], o[3]);
+          for (int jj = 0; jj < 4; ++jj) {
+            // bf16 pair (128 + q[2jj], 128 + q[2jj + 1]): 0x4300 | nibble is 128 + nibble exactly
+            const uint32_t pair = 0x43004300u | ((w >> (8 * jj)) & 0xFu) | (((w >> (8 * jj + 4)) & 0xFu) << 16);
+            __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pair);
+            v = __hsub2(v, k128);      // exact: q
+            v = __hfma2(s2, v, b2);    // scale * q + bias, one rounding
+            o[jj] = *reinterpret_cast<const uint32_t*>(&v);
           }
+          *reinterpret_cast<uint4*>(st + kAOp + sw128(rr, c)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -463,12 +531,13 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM>::kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
+    tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
-// Sums the split-K partial sums of kernel_projection into the side-0 deltas (fp32) and the side-1
-// deltas (activation dtype) of every row: D[m, side, tap, g] = sum_s part[s][m][(side*2+tap)*groups + g].
+// Sums the split-K partial sums of kernel_projection into the side-0 deltas (fp32, [tap][group][row],
+// the layout the fused input projection loads) and the side-1 deltas (activation dtype,
+// [row][tap][group], as prepare stores them): D[m, side, tap, g] = sum_s part[s][m][(side*2+tap)*groups + g].
 template <typename T>
 __global__ void __launch_bounds__(256)
     conv_coef_kernel(const float* __restrict__ part, int k_splits, int M, int groups, float* __restrict__ d0,
@@ -485,8 +554,8 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int c = 0; c < 4; ++c) d[c] += p[c * groups];
   }
-  d0[(m * 2 + 0) * groups + g] = d[0];
-  d0[(m * 2 + 1) * groups + g] = d[1];
+  d0[(0 * static_cast<size_t>(groups) + g) * M + m] = d[0];
+  d0[(1 * static_cast<size_t>(groups) + g) * M + m] = d[1];
   if (sizeof(T) == 2) {
     reinterpret_cast<__nv_bfloat16*>(coef1)[(m * 2 + 0) * groups + g] = __float2bfloat16_rn(d[2]);
     reinterpret_cast<__nv_bfloat16*>(coef1)[(m * 2 + 1) * groups + g] = __float2bfloat16_rn(d[3]);
@@ -498,70 +567,89 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-template <int AM, int BM, int EM>
+template <int AM, int BM, int EM, int NT>
 static int launch_proj_t(const ProjSpec& p, cudaStream_t st) {
-  using C = PCfg<AM, BM, EM>;
+  using C = PCfg<AM, BM, EM, NT>;
   static_assert(C::kStages >= 2, "at least two pipeline stages");
-  CUtensorMap mA, mB, mBase;
-  if (!make_tmap_sw128(&mA, p.a, static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K), kPM))
+  ProjMaps maps;
+  const int a_rows = std::min(kPM, (p.M + 15) / 16 * 16);  // a small M loads only its own rows
+  if (!make_tmap_sw128(&maps.a, p.a, static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K),
+                       static_cast<uint32_t>(a_rows)))
     return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (projection A)");
+  maps.b = maps.base = maps.d0 = maps.scales = maps.biases = maps.a;
   if (BM) {
-    // packed weights [N][K / 8] 32-bit words, a box of 8 words (64 values) x 256 rows
+    // packed codes [N][K / 8] 32-bit words: a box of 8 words (64 codes) x NT rows; scales and
+    // biases [K / 64][N] bf16: a box of NT values of one group
     const uint64_t dims[2] = {static_cast<uint64_t>(p.K / 8), static_cast<uint64_t>(p.N)};
     const uint64_t strides[1] = {static_cast<uint64_t>(p.K / 8) * 4};
-    const uint32_t box[2] = {8, static_cast<uint32_t>(kPN)};
-    if (!make_tmap_plain(&mB, p.w, DFLASH2_F32, 2, dims, strides, box))
-      return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (packed weights)");
-  } else if (!make_tmap_sw128(&mB, p.w, static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K), kPN)) {
+    const uint32_t box[2] = {8, static_cast<uint32_t>(NT)};
+    const uint64_t sdims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K / kQGroup)};
+    const uint64_t sstr[1] = {static_cast<uint64_t>(p.N) * 2};
+    const uint32_t sbox[2] = {static_cast<uint32_t>(NT), 1};
+    if (!make_tmap_plain(&maps.b, p.w, DFLASH2_F32, 2, dims, strides, box) ||
+        !make_tmap_plain(&maps.scales, p.scales, DFLASH2_BF16, 2, sdims, sstr, sbox) ||
+        !make_tmap_plain(&maps.biases, p.qbias, DFLASH2_BF16, 2, sdims, sstr, sbox))
+      return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (4-bit weights)");
+  } else if (!make_tmap_sw128(&maps.b, p.w, static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K), NT)) {
     return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (projection W)");
   }
   if (AM) {
-    // base [2][2][K] fp32 as [4][K]: rows 0, 1 are side 0's taps; a box of 64 channels x 2 rows
+    // base [2][2][K] fp32 as [4][K]: rows 0, 1 are side 0's taps, a box of 64 channels x 2 rows;
+    // d0 [2][groups][M] fp32: a box of the A box's rows x the stage's 4 groups x 2 taps
     const uint64_t dims[2] = {static_cast<uint64_t>(p.K), 4};
     const uint64_t strides[1] = {static_cast<uint64_t>(p.K) * 4};
     const uint32_t box[2] = {static_cast<uint32_t>(kPK), 2};
-    if (!make_tmap_plain(&mBase, p.base, DFLASH2_F32, 2, dims, strides, box))
-      return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (base kernel)");
-  } else {
-    mBase = mA;
+    const uint64_t ddims[3] = {static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.groups), 2};
+    const uint64_t dstr[2] = {static_cast<uint64_t>(p.M) * 4, static_cast<uint64_t>(p.M) * p.groups * 4};
+    const uint32_t dbox[3] = {static_cast<uint32_t>(a_rows), static_cast<uint32_t>(kPK / 16), 2};
+    if (!make_tmap_plain(&maps.base, p.base, DFLASH2_F32, 2, dims, strides, box) ||
+        !make_tmap_plain(&maps.d0, p.d0, DFLASH2_F32, 3, ddims, dstr, dbox))
+      return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (conv side 0)");
   }
   ProjArgs args{};
   args.M = p.M;
   args.N = p.N;
   args.K = p.K;
+  args.a_rows = a_rows;
   args.tiles_m = (p.M + kPM - 1) / kPM;
-  args.tiles_n = (p.N + kPN - 1) / kPN;
+  args.tiles_n = (p.N + NT - 1) / NT;
   args.G = p.G > 0 ? p.G : 1;
   args.gs = p.gs > 0 ? p.gs : 8;
-  args.groups = p.groups;
-  args.d0 = p.d0;
+  args.groups = p.groups > 0 ? p.groups : 1;
   args.coef1 = static_cast<const __nv_bfloat16*>(p.coef1);
   args.base = p.base;
   args.residual = static_cast<const __nv_bfloat16*>(p.residual);
-  args.scales = static_cast<const __nv_bfloat16*>(p.scales);
-  args.qbias = static_cast<const __nv_bfloat16*>(p.qbias);
   args.out = static_cast<__nv_bfloat16*>(p.out);
   args.err = device_error_word();
   const int tiles = args.tiles_m * args.tiles_n;
   const int grid = std::min(tiles, sm_count());
   static unsigned done = 0;
-  auto kern = proj_kernel<AM, BM, EM>;
+  auto kern = proj_kernel<AM, BM, EM, NT>;
   if (!ensure_smem_attr(kern, C::kSmem, &done))
     return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed (projection)");
-  const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, st, nullptr, 0, mA, mB, mBase, args);
+  const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, st, nullptr, 0, maps, args);
   return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "projection launch failed: %s", cudaGetErrorString(e));
+}
+
+// 256-column tiles, or 64-column ones when the 256-column tiles would leave more than half the
+// SMs without a tile (few rows: the weight stream then spreads over four times as many CTAs).
+template <int AM, int BM, int EM>
+static int launch_proj_nt(const ProjSpec& p, cudaStream_t st) {
+  const long long tiles256 = static_cast<long long>((p.M + kPM - 1) / kPM) * ((p.N + 255) / 256);
+  if (2 * tiles256 < sm_count()) return launch_proj_t<AM, BM, EM, 64>(p, st);
+  return launch_proj_t<AM, BM, EM, 256>(p, st);
 }
 
 int launch_proj(const ProjSpec& p, cudaStream_t st) {
   const bool am = p.d0 != nullptr, bm = p.wbits == 4, em = p.coef1 != nullptr;
-  if (am && bm && em) return launch_proj_t<1, 1, 1>(p, st);
-  if (am && bm) return launch_proj_t<1, 1, 0>(p, st);
-  if (am && em) return launch_proj_t<1, 0, 1>(p, st);
-  if (bm && em) return launch_proj_t<0, 1, 1>(p, st);
-  if (am) return launch_proj_t<1, 0, 0>(p, st);
-  if (bm) return launch_proj_t<0, 1, 0>(p, st);
-  if (em) return launch_proj_t<0, 0, 1>(p, st);
-  return launch_proj_t<0, 0, 0>(p, st);
+  if (am && bm && em) return launch_proj_nt<1, 1, 1>(p, st);
+  if (am && bm) return launch_proj_nt<1, 1, 0>(p, st);
+  if (am && em) return launch_proj_nt<1, 0, 1>(p, st);
+  if (bm && em) return launch_proj_nt<0, 1, 1>(p, st);
+  if (am) return launch_proj_nt<1, 0, 0>(p, st);
+  if (bm) return launch_proj_nt<0, 1, 0>(p, st);
+  if (em) return launch_proj_nt<0, 0, 1>(p, st);
+  return launch_proj_nt<0, 0, 0>(p, st);
 }
 
 int launch_conv_coefficients(const float* part, int k_splits, int M, int groups, int dtype, float* d0, void* coef1,

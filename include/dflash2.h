@@ -284,14 +284,15 @@ DFLASH2_API int dflash2_score_edges_ragged(const int32_t* cand, const float* una
  *
  * dflash2_conv_coefficients: prepare without the side-0 output. Optional RMSNorm (norm_w given:
  *   n_out [B*G, H] receives n; else n = x and n_out may be NULL), kernel_projection, then
- *   d0 [B*G, 2, groups] fp32 = side 0's deltas D[t, 0, tap, g] and coef1 [B*G, 2, groups] dtype =
- *   side 1's (as dflash2_conv_prepare's coef1). Workspace as dflash2_conv_prepare_workspace_bytes.
+ *   d0 [2, groups, B*G] fp32 = side 0's deltas, d0[tap, g, m] = D[m, 0, tap, g] (tap-and-group
+ *   major, the layout the fused input projection loads), and coef1 [B*G, 2, groups] dtype = side
+ *   1's (as dflash2_conv_prepare's coef1). Workspace as dflash2_conv_prepare_workspace_bytes.
  *
  * dflash2_proj: out [M, N] = a [M, K] . W^T.
- * dflash2_proj_conv_in: out = Conv_0(n) . W^T, Conv_0(n)[m, k] = (base[0,0,k] + d0[m,0,k/gs]) n[m, k]
- *   + (base[0,1,k] + d0[m,1,k/gs]) n[m-1, k], n[m-1] = 0 at each block's first row (m % G == 0);
+ * dflash2_proj_conv_in: out = Conv_0(n) . W^T, Conv_0(n)[m, k] = (base[0,0,k] + d0[0,k/gs,m]) n[m, k]
+ *   + (base[0,1,k] + d0[1,k/gs,m]) n[m-1, k], n[m-1] = 0 at each block's first row (m % G == 0);
  *   the side-0 output is computed in the GEMM's operand producer and never written. K = H;
- *   base [2, 2, K] fp32; G divides 128, M % G == 0, group_size in {8, 16, 32, 64}.
+ *   base [2, 2, K] fp32; d0 16-byte aligned; G divides 128, M % G == 0, group_size 16.
  * dflash2_proj_conv_out: out = residual + Conv_1(a . W^T) (residual may be NULL), Conv_1 with the
  *   side-1 deltas coef1 [M, 2, N/gs] (bf16) and base[1] over the N = H output channels, computed in
  *   the GEMM's epilogue (fp32 add, one rounding). G divides 32, M % G == 0, group_size in {8, 16, 32},
@@ -300,8 +301,9 @@ DFLASH2_API int dflash2_score_edges_ragged(const int32_t* cand, const float* una
  * Weights: wbits = 16: w is bf16 [N, K] (out, in). wbits = 4: affine 4-bit weights in groups of 64
  * along K (dflash2.ts quantizedWeight: quantize(w, 64, bits), mode "affine"): w is [N, K/8] uint32,
  * value k of row n in bits 4 (k % 8) .. 4 (k % 8) + 3 of word k / 8 (an unsigned q in [0, 15]);
- * w_scales and w_biases are bf16 [N, K/64]; W[n, k] = w_scales[n, k/64] * q + w_biases[n, k/64],
- * rounded once to bf16 before the MMA. K % 64 == 0, N % 8 == 0, M >= 1; a, w, out, residual and base
+ * w_scales and w_biases are bf16 [K/64, N] (group-major, so one group's values for a tile of rows
+ * are contiguous); W[n, k] = w_scales[k/64, n] * q + w_biases[k/64, n], rounded once to bf16
+ * before the MMA. K % 64 == 0, N % 8 == 0, M >= 1; a, w, w_scales, w_biases, out, residual and base
  * 16-byte aligned.
  * ---------------------------------------------------------------------------------- */
 DFLASH2_API int dflash2_conv_coefficients(const void* x, const void* norm_w, float eps, const void* w_kp, int B, int G,

@@ -26,6 +26,11 @@ def _u32(packed):
     return torch.from_numpy(packed.view(np.int32)).cuda()
 
 
+def _gm(t):
+    """Scales / biases [N, K/64] -> the library's group-major [K/64, N]."""
+    return _dev(np.ascontiguousarray(t.T))
+
+
 def _bound(a64, W64):
     """fp32 accumulation over K of exact bf16 products, then one bf16 rounding of the output."""
     K = a64.shape[-1]
@@ -42,7 +47,8 @@ def _conv_case(seed, B, G, H, gs):
     return n, d, base
 
 
-@pytest.mark.parametrize("M,K,N", [(16, 256, 256), (300, 512, 264), (1024, 5120, 512), (129, 128, 1000)])
+@pytest.mark.parametrize("M,K,N", [(16, 256, 256), (300, 512, 264), (1024, 5120, 512), (129, 128, 1000),
+                                   (2048, 256, 4096)])
 def test_proj_bf16(torch, M, K, N):
     import dflash2_block_drafter_gb300 as d
     a = I.normal(M, "a", (M, K), 1.0)
@@ -55,7 +61,7 @@ def test_proj_bf16(torch, M, K, N):
     assert np.all(np.abs(got - ref) <= _bound(I.to_f64(a), I.to_f64(W))), "outside the fp32-accumulation bound"
 
 
-@pytest.mark.parametrize("M,K,N", [(48, 256, 128), (272, 5120, 520)])
+@pytest.mark.parametrize("M,K,N", [(48, 256, 128), (272, 5120, 520), (1024, 512, 5120)])
 def test_proj_w4_exact_codes_equal_the_bf16_weight(torch, M, K, N):
     """4-bit weights whose scale * q + bias are bf16 values: the dequantised operand is exact, so the
     W4 GEMM equals the bf16 GEMM on that weight bit for bit (same tiles, same accumulation order)."""
@@ -65,7 +71,7 @@ def test_proj_w4_exact_codes_equal_the_bf16_weight(torch, M, K, N):
     W_bf16 = I.round_to_bf16_bits(W.astype(np.float32))
     assert np.array_equal(I.to_f64(W_bf16), W)       # exactly representable
     a = _dev(I.normal(M, "a", (M, K), 1.0))
-    y4 = d.dflash2_proj(a, _u32(q.packed), w_scales=_dev(q.scales), w_biases=_dev(q.biases))
+    y4 = d.dflash2_proj(a, _u32(q.packed), w_scales=_gm(q.scales), w_biases=_gm(q.biases))
     y16 = d.dflash2_proj(a, _dev(W_bf16))
     assert d.dflash2_poll_error() == 0
     assert torch.equal(y4, y16)
@@ -76,7 +82,7 @@ def test_proj_w4_parity(torch):
     M, K, N = 200, 1024, 384
     q = I.affine4_weight(7, "w4", N, K)
     a = I.normal(7, "a", (M, K), 1.0)
-    y = d.dflash2_proj(_dev(a), _u32(q.packed), w_scales=_dev(q.scales), w_biases=_dev(q.biases))
+    y = d.dflash2_proj(_dev(a), _u32(q.packed), w_scales=_gm(q.scales), w_biases=_gm(q.biases))
     assert d.dflash2_poll_error() == 0
     W = O.affine_dequantize(q.q, I.to_f64(q.scales), I.to_f64(q.biases))
     ref = O.projection(I.to_f64(a), W)
@@ -86,12 +92,13 @@ def test_proj_w4_parity(torch):
     assert np.all(np.abs(got - ref) <= _bound(I.to_f64(a), W) + 2.0 ** -9 * np.abs(I.to_f64(a)) @ np.abs(W).T)
 
 
-@pytest.mark.parametrize("B,G,H,gs,N", [(2, 16, 256, 16, 256), (9, 16, 5120, 16, 512), (5, 8, 512, 8, 136)])
+@pytest.mark.parametrize("B,G,H,gs,N", [(2, 16, 256, 16, 256), (9, 16, 5120, 16, 512), (5, 8, 512, 16, 136),
+                                        (64, 16, 1024, 16, 4864)])
 def test_proj_conv_in(torch, B, G, H, gs, N):
     import dflash2_block_drafter_gb300 as d
     n, D, base = _conv_case(B * G, B, G, H, gs)
     W = I.normal(B, "W", (N, H), H ** -0.5)
-    d0 = np.ascontiguousarray(D[:, 0])                   # [M, 2, groups] side 0's deltas
+    d0 = np.ascontiguousarray(D[:, 0].transpose(1, 2, 0))  # side 0's deltas [tap, group, M]
     y = d.dflash2_proj_conv_in(_dev(n), _dev(d0), _dev(base), G, gs, _dev(W))
     assert d.dflash2_poll_error() == 0
     ref = O.sublayer_in(I.to_f64(n).reshape(B, G, H), D.reshape(B, G, 2, 2, -1)[:, :, 0].astype(np.float64),
@@ -106,7 +113,7 @@ def test_proj_conv_in(torch, B, G, H, gs, N):
 
 
 @pytest.mark.parametrize("B,G,K,H,gs,res", [(2, 16, 256, 256, 16, True), (9, 16, 512, 5120, 16, True),
-                                            (12, 8, 128, 96, 8, False)])
+                                            (12, 8, 128, 96, 8, False), (64, 16, 256, 5120, 16, True)])
 def test_proj_conv_out(torch, B, G, K, H, gs, res):
     import dflash2_block_drafter_gb300 as d
     M = B * G
@@ -183,12 +190,12 @@ def test_proj_w4_with_both_conv_fusions(torch):
     n, D, base = _conv_case(5, B, G, H, gs)
     q_in = I.affine4_weight(5, "w_in", N, H)
     q_out = I.affine4_weight(5, "w_out", H, N)
-    d0 = np.ascontiguousarray(D[:, 0])
+    d0 = np.ascontiguousarray(D[:, 0].transpose(1, 2, 0))
     d1 = I.round_to_bf16_bits(np.ascontiguousarray(D[:, 1]))
-    u = d.dflash2_proj_conv_in(_dev(n), _dev(d0), _dev(base), G, gs, _u32(q_in.packed), w_scales=_dev(q_in.scales),
-                               w_biases=_dev(q_in.biases))
-    out = d.dflash2_proj_conv_out(u, _u32(q_out.packed), _dev(d1), _dev(base), G, gs, w_scales=_dev(q_out.scales),
-                                  w_biases=_dev(q_out.biases))
+    u = d.dflash2_proj_conv_in(_dev(n), _dev(d0), _dev(base), G, gs, _u32(q_in.packed), w_scales=_gm(q_in.scales),
+                               w_biases=_gm(q_in.biases))
+    out = d.dflash2_proj_conv_out(u, _u32(q_out.packed), _dev(d1), _dev(base), G, gs, w_scales=_gm(q_out.scales),
+                                  w_biases=_gm(q_out.biases))
     assert d.dflash2_poll_error() == 0
     W_in = O.affine_dequantize(q_in.q, I.to_f64(q_in.scales), I.to_f64(q_in.biases))
     W_out = O.affine_dequantize(q_out.q, I.to_f64(q_out.scales), I.to_f64(q_out.biases))
