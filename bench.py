@@ -342,26 +342,29 @@ def proj_sweep(d, gen, dev, time_call, pk, G=16, H=5120, gs=16, N=5120):
         u = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
         out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+        pw = torch.empty(max(256, d.dflash2_proj_workspace_bytes(M, N, H), d.dflash2_proj_workspace_bytes(M, H, N)),
+                         dtype=torch.uint8, device=dev)
 
         def in_unfused():
             d.dflash2_conv_prepare(n, None, 1e-6, w_kp, base, gs, out=a, coef1=coef1, workspace=ws)
-            d.dflash2_proj(a.view(M, H), w_in, out=u)
+            d.dflash2_proj(a.view(M, H), w_in, out=u, workspace=pw)
 
         def in_fused():
             d.dflash2_conv_coefficients(n, None, 1e-6, w_kp, gs, d0=d0, coef1=c1, workspace=ws)
-            d.dflash2_proj_conv_in(n.view(M, H), d0, base, G, gs, w_in, out=u)
+            d.dflash2_proj_conv_in(n.view(M, H), d0, base, G, gs, w_in, out=u, workspace=pw)
 
         def out_unfused():
-            d.dflash2_proj(u, w_out, out=y)
+            d.dflash2_proj(u, w_out, out=y, workspace=pw)
             d.dflash2_conv_finish(y.view(B, G, H), coef1, base, gs, residual=x.view(B, G, H), out=out.view(B, G, H))
 
         def out_fused():
-            d.dflash2_proj_conv_out(u, w_out, c1, base, G, gs, residual=x, out=out)
+            d.dflash2_proj_conv_out(u, w_out, c1, base, G, gs, residual=x, out=out, workspace=pw)
 
         t = {name: time_call(fn) for name, fn in (("in_unfused", in_unfused), ("in_fused", in_fused),
                                                   ("out_unfused", out_unfused), ("out_fused", out_fused))}
-        t["proj_bf16"] = time_call(lambda: d.dflash2_proj(n.view(M, H), w_in, out=u))
-        t["proj_w4"] = time_call(lambda: d.dflash2_proj(n.view(M, H), q_in, w_scales=s_in, w_biases=b_in, out=u))
+        t["proj_bf16"] = time_call(lambda: d.dflash2_proj(n.view(M, H), w_in, out=u, workspace=pw))
+        t["proj_w4"] = time_call(lambda: d.dflash2_proj(n.view(M, H), q_in, w_scales=s_in, w_biases=b_in, out=u,
+                                                        workspace=pw))
         e = 2.0  # bf16 bytes
         # algorithmic bytes of each sequence (every tensor read or written once per call)
         act_h, act_n = M * H * e, M * N * e

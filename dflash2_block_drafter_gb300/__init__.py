@@ -24,6 +24,7 @@ __all__ = [
     "dflash2_select_path", "dflash2_selftest_bounded_wait", "dflash2_head_topk_noalloc", "dflash2_head_topk_vocab", "dflash2_score_edges_depths", "dflash2_select_path_depths",
     "dflash2_ragged_offsets", "dflash2_conv_finish_ragged", "dflash2_score_edges_ragged",
     "dflash2_conv_coefficients", "dflash2_proj", "dflash2_proj_conv_in", "dflash2_proj_conv_out",
+    "dflash2_proj_workspace_bytes",
     "DTYPE_CODES",
 ]
 
@@ -63,9 +64,11 @@ _SIGNATURES = {
     "dflash2_score_edges_ragged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp,
                                         _vp]),
     "dflash2_conv_coefficients": (_i, [_vp, _vp, _f, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "dflash2_proj": (_i, [_vp, _i, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
-    "dflash2_proj_conv_in": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
-    "dflash2_proj_conv_out": (_i, [_vp, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _vp, _i, _vp, _vp]),
+    "dflash2_proj_workspace_bytes": (_sz, [_i, _i, _i]),
+    "dflash2_proj": (_i, [_vp, _i, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "dflash2_proj_conv_in": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "dflash2_proj_conv_out": (_i, [_vp, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _vp, _i, _vp, _vp, _sz,
+                                   _vp]),
 }
 
 
@@ -447,6 +450,23 @@ def dflash2_conv_coefficients(x, norm_w, eps, w_kp, group_size, n_out=None, d0=N
     return (n_out if norm_w is not None else x.view(B * G, H)), d0, coef1
 
 
+def _proj_ws(M, N, K, dev, workspace):
+    """(pointer, bytes) of the projection workspace (allocated here when not given; NULL, 0 when the
+    shape needs none)."""
+    need = library().dflash2_proj_workspace_bytes(M, N, K)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace.numel() < need:
+        raise ValueError(f"workspace holds {workspace.numel()} bytes, fewer than the {need} needed")
+    return _dev(workspace, "workspace"), workspace.numel()
+
+
+def dflash2_proj_workspace_bytes(M, N, K) -> int:
+    return library().dflash2_proj_workspace_bytes(M, N, K)
+
+
 def _proj_out(out, M, N, dev):
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if out is None else out
     if out.numel() < M * N:
@@ -454,17 +474,19 @@ def _proj_out(out, M, N, dev):
     return out
 
 
-def dflash2_proj(a, w, w_scales=None, w_biases=None, out=None, stream=None):
+def dflash2_proj(a, w, w_scales=None, w_biases=None, out=None, workspace=None, stream=None):
     """out [M, N] = a [M, K] . W^T (bf16; W bf16 [N, K] or affine 4-bit with scales / biases)."""
     M, K = a.shape
     wp, wbits, N = _proj_weight(w, w_scales, w_biases, K)
     out = _proj_out(out, M, N, a.device)
+    ws = _proj_ws(M, N, K, a.device, workspace)
     _check(library().dflash2_proj(_dev(a, "a", torch.bfloat16), M, K, *wp, wbits, N, BF16,
-                                  _dev(out, "out", torch.bfloat16), _stream(stream)))
+                                  _dev(out, "out", torch.bfloat16), *ws, _stream(stream)))
     return out
 
 
-def dflash2_proj_conv_in(n, d0, base, G, group_size, w, w_scales=None, w_biases=None, out=None, stream=None):
+def dflash2_proj_conv_in(n, d0, base, G, group_size, w, w_scales=None, w_biases=None, out=None, workspace=None,
+                         stream=None):
     """out = Conv_0(n) . W^T with the conv's side 0 computed inside the GEMM (n [M, K = H]; d0
     [2, K / 16, M] fp32 as dflash2_conv_coefficients returns it)."""
     M, K = n.shape
@@ -472,14 +494,15 @@ def dflash2_proj_conv_in(n, d0, base, G, group_size, w, w_scales=None, w_biases=
     if d0.numel() < M * 2 * (K // group_size) or base.numel() < 4 * K:
         raise ValueError("d0 must hold [M, 2, K / group_size] and base [2, 2, K]")
     out = _proj_out(out, M, N, n.device)
+    ws = _proj_ws(M, N, K, n.device, workspace)
     _check(library().dflash2_proj_conv_in(
         _dev(n, "n", torch.bfloat16), _dev(d0, "d0", torch.float32), _dev(base, "base", torch.float32), G, group_size,
-        M, K, *wp, wbits, N, BF16, _dev(out, "out", torch.bfloat16), _stream(stream)))
+        M, K, *wp, wbits, N, BF16, _dev(out, "out", torch.bfloat16), *ws, _stream(stream)))
     return out
 
 
 def dflash2_proj_conv_out(a, w, coef1, base, G, group_size, residual=None, w_scales=None, w_biases=None, out=None,
-                          stream=None):
+                          workspace=None, stream=None):
     """out = residual + Conv_1(a . W^T) with the conv's side 1 (and the residual add) in the GEMM's epilogue."""
     M, K = a.shape
     wp, wbits, N = _proj_weight(w, w_scales, w_biases, K)
@@ -488,8 +511,9 @@ def dflash2_proj_conv_out(a, w, coef1, base, G, group_size, residual=None, w_sca
     if residual is not None and residual.numel() < M * N:
         raise ValueError("residual must hold [M, N]")
     out = _proj_out(out, M, N, a.device)
+    ws = _proj_ws(M, N, K, a.device, workspace)
     _check(library().dflash2_proj_conv_out(
         _dev(a, "a", torch.bfloat16), M, K, *wp, wbits, N, _dev(coef1, "coef1", torch.bfloat16),
         _dev(base, "base", torch.float32), G, group_size, _dev(residual, "residual", torch.bfloat16, True), BF16,
-        _dev(out, "out", torch.bfloat16), _stream(stream)))
+        _dev(out, "out", torch.bfloat16), *ws, _stream(stream)))
     return out

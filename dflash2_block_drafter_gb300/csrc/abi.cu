@@ -249,11 +249,31 @@ static int check_proj(const void* a, int M, int K, const void* w, const void* w_
   return DFLASH2_OK;
 }
 
+size_t dflash2_proj_workspace_bytes(int M, int N, int K) {
+  if (M < 1 || N < 8 || K < 64) return 0;
+  return proj_workspace(M, N, K, sm_count());
+}
+
+static int proj_ws(int M, int N, int K, void* workspace, size_t workspace_bytes, float** part) {
+  const size_t need = proj_workspace(M, N, K, sm_count());
+  *part = nullptr;
+  if (need == 0) return DFLASH2_OK;
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(DFLASH2_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu bytes needed", workspace_bytes,
+                need);
+  REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0, "workspace must be 256-byte aligned");
+  *part = static_cast<float*>(workspace);
+  return DFLASH2_OK;
+}
+
 int dflash2_proj(const void* a, int M, int K, const void* w, const void* w_scales, const void* w_biases, int wbits,
-                 int N, int dtype, void* out, void* stream) {
-  const int rc = check_proj(a, M, K, w, w_scales, w_biases, wbits, N, dtype, out);
+                 int N, int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_proj(a, M, K, w, w_scales, w_biases, wbits, N, dtype, out);
   if (rc != DFLASH2_OK) return rc;
+  float* part = nullptr;
+  if ((rc = proj_ws(M, N, K, workspace, workspace_bytes, &part)) != DFLASH2_OK) return rc;
   ProjSpec p{};
+  p.part = part;
   p.a = a; p.w = w; p.scales = w_scales; p.qbias = w_biases; p.wbits = wbits;
   p.M = M; p.N = N; p.K = K; p.out = out;
   return launch_proj(p, static_cast<cudaStream_t>(stream));
@@ -261,16 +281,19 @@ int dflash2_proj(const void* a, int M, int K, const void* w, const void* w_scale
 
 int dflash2_proj_conv_in(const void* n, const float* d0, const float* base, int G, int group_size, int M, int K,
                          const void* w, const void* w_scales, const void* w_biases, int wbits, int N, int dtype,
-                         void* out, void* stream) {
-  const int rc = check_proj(n, M, K, w, w_scales, w_biases, wbits, N, dtype, out);
+                         void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_proj(n, M, K, w, w_scales, w_biases, wbits, N, dtype, out);
   if (rc != DFLASH2_OK) return rc;
+  float* part = nullptr;
   REQUIRE(d0 && base, "d0 and base are required");
   REQUIRE(G >= 2 && G <= 64 && 128 % G == 0, "G=%d must divide 128 (blocks must not straddle a 128-row tile)", G);
   REQUIRE(M % G == 0, "M=%d must be a whole number of %d-row blocks", M, G);
   REQUIRE(group_size == 16, "group_size=%d: the fused side 0 is built for groups of 16 channels", group_size);
   REQUIRE(M % 4 == 0, "M=%d must be a multiple of 4 (rows of the side-0 deltas are loaded in 16-byte units)", M);
   REQUIRE(aligned16(base) && aligned16(d0), "base and d0 must be 16-byte aligned");
+  if ((rc = proj_ws(M, N, K, workspace, workspace_bytes, &part)) != DFLASH2_OK) return rc;
   ProjSpec p{};
+  p.part = part;
   p.a = n; p.w = w; p.scales = w_scales; p.qbias = w_biases; p.wbits = wbits;
   p.M = M; p.N = N; p.K = K; p.out = out;
   p.d0 = d0; p.base = base; p.G = G; p.gs = group_size; p.groups = K / group_size;
@@ -279,16 +302,20 @@ int dflash2_proj_conv_in(const void* n, const float* d0, const float* base, int 
 
 int dflash2_proj_conv_out(const void* a, int M, int K, const void* w, const void* w_scales, const void* w_biases,
                           int wbits, int N, const void* coef1, const float* base, int G, int group_size,
-                          const void* residual, int dtype, void* out, void* stream) {
-  const int rc = check_proj(a, M, K, w, w_scales, w_biases, wbits, N, dtype, out);
+                          const void* residual, int dtype, void* out, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  int rc = check_proj(a, M, K, w, w_scales, w_biases, wbits, N, dtype, out);
   if (rc != DFLASH2_OK) return rc;
+  float* part = nullptr;
   REQUIRE(coef1 && base, "coef1 and base are required");
   REQUIRE(G >= 2 && G <= 32 && 32 % G == 0, "G=%d must divide 32 (a block's rows must share a warp)", G);
   REQUIRE(M % G == 0, "M=%d must be a whole number of %d-row blocks", M, G);
   REQUIRE(group_size == 8 || group_size == 16 || group_size == 32, "group_size=%d must be 8, 16 or 32", group_size);
   REQUIRE(N % group_size == 0 && N % 32 == 0, "N=%d must be a multiple of 32 and of group_size", N);
   REQUIRE(aligned16(base) && (!residual || aligned16(residual)), "base and residual must be 16-byte aligned");
+  if ((rc = proj_ws(M, N, K, workspace, workspace_bytes, &part)) != DFLASH2_OK) return rc;
   ProjSpec p{};
+  p.part = part;
   p.a = a; p.w = w; p.scales = w_scales; p.qbias = w_biases; p.wbits = wbits;
   p.M = M; p.N = N; p.K = K; p.out = out;
   p.coef1 = coef1; p.base = base; p.residual = residual; p.G = G; p.gs = group_size; p.groups = N / group_size;

@@ -150,7 +150,14 @@ struct ProjSpec {
   const void* coef1;
   const void* residual;
   void* out;
+  float* part;  // split-K partial sums (proj_workspace bytes), or null when the plan does not split
 };
+struct ProjPlan {
+  int nt;        // columns per tile (64 or 256)
+  int k_splits;  // K ranges summed by a reduce pass (1: none)
+};
+ProjPlan proj_plan(int M, int N, int K, int sms);
+size_t proj_workspace(int M, int N, int K, int sms);
 int launch_proj(const ProjSpec& p, cudaStream_t st);
 // D from kernel_projection's split-K partials: d0 = side 0's deltas (fp32), coef1 = side 1's (dtype).
 int launch_conv_coefficients(const float* part, int k_splits, int M, int groups, int dtype, float* d0, void* coef1,

@@ -79,6 +79,8 @@ struct PCfg {
 
 struct ProjArgs {
   int M, N, K;
+  int k_splits;                // > 1: fp32 partial sums of K ranges to `part`, summed by proj_reduce_kernel
+  float* part;                 // [k_splits][M][N]
   int a_rows;                  // rows of the A box (up to 128: fewer when M is small)
   int tiles_m, tiles_n;
   int G, gs, groups;           // conv shape (G rows per block, group size, channels / group size)
@@ -161,6 +163,7 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int k_stages = a.K / kPK;
   const int n_tiles = a.tiles_m * a.tiles_n;
+  const int n_items = n_tiles * a.k_splits;  // work item i: tile i % n_tiles, K range i / n_tiles
   const int gpc = AM ? kPK / 16 : 1;  // groups per stage (conv side 0 over K, group size 16)
 
   if (threadIdx.x == 0) {
@@ -208,10 +211,11 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+        const int t = it % n_tiles, ks = it / n_tiles;
         const int m0 = (t % a.tiles_m) * kPM;
         const int n0 = (t / a.tiles_m) * NT;
-        for (int kb = 0; kb < k_stages; ++kb) {
+        for (int kb = k_stages * ks / a.k_splits; kb < k_stages * (ks + 1) / a.k_splits; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
@@ -262,7 +266,9 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
       uint32_t phase = 0;
       bool ok = true, any = false;
       const uint32_t idesc = make_idesc(false, kPM, NT);
-      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++tile_i) {
+      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++tile_i) {
+        const int ks = it / n_tiles;
+        const int kb0 = k_stages * ks / a.k_splits, kb1 = k_stages * (ks + 1) / a.k_splits;
         const int ab = tile_i & 1;
         const uint32_t acc_par = static_cast<uint32_t>(tile_i >> 1) & 1u;
         if (!mbar_wait_bounded(smem_u32(&acc_empty[ab]), acc_par ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
           break;
         }
         tc_fence_after();
-        for (int kb = 0; kb < k_stages; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs) ||
               (C::kProdWarps > 0 && !mbar_wait_bounded(smem_u32(&ready[stage]), phase, abort_flag, kWaitLimitNs))) {
             ok = false;
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k)  // 16-element (32-byte) steps along the swizzled row
             mma_f16(tmem_base + static_cast<uint32_t>(ab * NT), adesc + static_cast<uint64_t>(2 * k),
-                    bdesc + static_cast<uint64_t>(2 * k), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    bdesc + static_cast<uint64_t>(2 * k), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           mma_commit(smem_u32(&empty[stage]));
           any = true;
           if (++stage == C::kStages) {
@@ -307,7 +313,8 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lanes 32q .. 32q + 31
     int tile_i = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_i) {
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++tile_i) {
+      const int t = it % n_tiles, ks = it / n_tiles;
       const int m0 = (t % a.tiles_m) * kPM;
       const int n0 = (t / a.tiles_m) * NT;
       const int row = m0 + q * 32 + lane;
@@ -336,6 +343,17 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
         float y[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(r[j]);
+        if (a.k_splits > 1) {
+          // a K range's partial sums; the reduce pass adds them and applies the epilogue
+          if (valid) {
+            float* dst = a.part + (static_cast<size_t>(ks) * a.M + row) * a.N + col0;
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              if (col0 + 4 * v < a.N)
+                *reinterpret_cast<float4*>(dst + 4 * v) = make_float4(y[4 * v], y[4 * v + 1], y[4 * v + 2], y[4 * v + 3]);
+          }
+          continue;
+        }
         if (EM) {
           // x = residual + (b10 + d10) y[m] + (b11 + d11) y[m - 1]; y[m - 1] is lane - 1's value
           // (lane 0's row 32w starts a block, as G divides 32)
@@ -402,11 +420,12 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int t = it % n_tiles, ks = it / n_tiles;
       const int m0 = (t % a.tiles_m) * kPM;
       const int row_first = m0 + r_first;
       const int t_first = row_first % a.G;
-      for (int kb = 0; kb < k_stages; ++kb) {
+      for (int kb = k_stages * ks / a.k_splits; kb < k_stages * (ks + 1) / a.k_splits; ++kb) {
         if (!mbar_wait_bounded_suspend(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs, 200)) {
           ok = false;
           break;
@@ -485,8 +504,9 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     uint32_t phase = 0;
     bool ok = true;
     const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
-    for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
-      for (int kb = 0; kb < k_stages; ++kb) {
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int t = it % n_tiles, ks = it / n_tiles;
+      for (int kb = k_stages * ks / a.k_splits; kb < k_stages * (ks + 1) / a.k_splits; ++kb) {
         if (!mbar_wait_bounded_suspend(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs, 200)) {
           ok = false;
           break;
@@ -535,6 +555,53 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
   }
 }
 
+// Adds the K ranges' partial sums of a split projection and applies its epilogue: out = y, or
+// (EM) out = residual + (b10 + d10) y[m] + (b11 + d11) y[m - 1] with y[m - 1] = 0 at a block start.
+// One thread per row and 8 columns (one group: gs >= 8).
+template <int EM>
+__global__ void __launch_bounds__(256) proj_reduce_kernel(const ProjArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int n8 = a.N / 8;
+  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<size_t>(a.M) * n8) return;
+  const int m = static_cast<int>(idx / n8);
+  const int c8 = static_cast<int>(idx % n8) * 8;
+  const size_t plane = static_cast<size_t>(a.M) * a.N;
+  float y[8] = {}, yp[8] = {};
+  const bool prev = EM && (m % a.G) != 0;
+  for (int s = 0; s < a.k_splits; ++s) {
+    const float* p = a.part + s * plane + static_cast<size_t>(m) * a.N + c8;
+    const float4 u0 = *reinterpret_cast<const float4*>(p);
+    const float4 u1 = *reinterpret_cast<const float4*>(p + 4);
+    y[0] += u0.x; y[1] += u0.y; y[2] += u0.z; y[3] += u0.w;
+    y[4] += u1.x; y[5] += u1.y; y[6] += u1.z; y[7] += u1.w;
+    if (prev) {
+      const float4 v0 = *reinterpret_cast<const float4*>(p - a.N);
+      const float4 v1 = *reinterpret_cast<const float4*>(p - a.N + 4);
+      yp[0] += v0.x; yp[1] += v0.y; yp[2] += v0.z; yp[3] += v0.w;
+      yp[4] += v1.x; yp[5] += v1.y; yp[6] += v1.z; yp[7] += v1.w;
+    }
+  }
+  float o[8];
+  if (EM) {
+    const float d0 = __bfloat162float(a.coef1[(static_cast<size_t>(m) * 2 + 0) * a.groups + c8 / a.gs]);
+    const float d1 = __bfloat162float(a.coef1[(static_cast<size_t>(m) * 2 + 1) * a.groups + c8 / a.gs]);
+    float res[8] = {};
+    if (a.residual != nullptr) bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.residual + static_cast<size_t>(m) * a.N + c8), res);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float b0 = a.base[2 * static_cast<size_t>(a.N) + c8 + e];
+      const float b1 = a.base[3 * static_cast<size_t>(a.N) + c8 + e];
+      o[e] = res[e] + ((b0 + d0) * y[e] + (b1 + d1) * yp[e]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = y[e];
+  }
+  *reinterpret_cast<uint4*>(a.out + static_cast<size_t>(m) * a.N + c8) = f32x8_to_bf16(o);
+}
+
 // Sums the split-K partial sums of kernel_projection into the side-0 deltas (fp32, [tap][group][row],
 // the layout the fused input projection loads) and the side-1 deltas (activation dtype,
 // [row][tap][group], as prepare stores them): D[m, side, tap, g] = sum_s part[s][m][(side*2+tap)*groups + g].
@@ -568,7 +635,7 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 template <int AM, int BM, int EM, int NT>
-static int launch_proj_t(const ProjSpec& p, cudaStream_t st) {
+static int launch_proj_t(const ProjSpec& p, int k_splits, cudaStream_t st) {
   using C = PCfg<AM, BM, EM, NT>;
   static_assert(C::kStages >= 2, "at least two pipeline stages");
   ProjMaps maps;
@@ -610,6 +677,8 @@ static int launch_proj_t(const ProjSpec& p, cudaStream_t st) {
   args.M = p.M;
   args.N = p.N;
   args.K = p.K;
+  args.k_splits = k_splits;
+  args.part = p.part;
   args.a_rows = a_rows;
   args.tiles_m = (p.M + kPM - 1) / kPM;
   args.tiles_n = (p.N + NT - 1) / NT;
@@ -621,23 +690,46 @@ static int launch_proj_t(const ProjSpec& p, cudaStream_t st) {
   args.residual = static_cast<const __nv_bfloat16*>(p.residual);
   args.out = static_cast<__nv_bfloat16*>(p.out);
   args.err = device_error_word();
-  const int tiles = args.tiles_m * args.tiles_n;
-  const int grid = std::min(tiles, sm_count());
+  const int items = args.tiles_m * args.tiles_n * k_splits;
+  const int grid = std::min(items, sm_count());
   static unsigned done = 0;
   auto kern = proj_kernel<AM, BM, EM, NT>;
   if (!ensure_smem_attr(kern, C::kSmem, &done))
     return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed (projection)");
-  const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, st, nullptr, 0, maps, args);
-  return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "projection launch failed: %s", cudaGetErrorString(e));
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, st, nullptr, 0, maps, args);
+  if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "projection launch failed: %s", cudaGetErrorString(e));
+  if (k_splits > 1) {
+    const size_t n = static_cast<size_t>(p.M) * (p.N / 8);
+    e = launch_pdl(proj_reduce_kernel<EM>, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, st, nullptr, 0,
+                   args);
+    if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "projection reduce launch failed: %s", cudaGetErrorString(e));
+  }
+  return DFLASH2_OK;
 }
 
-// 256-column tiles, or 64-column ones when the 256-column tiles would leave more than half the
-// SMs without a tile (few rows: the weight stream then spreads over four times as many CTAs).
+// Tiles and K splits of a projection. With enough rows every SM gets 256-column tiles. With few
+// (the weight-streaming case) the K range is split so that about every SM streams a share of the
+// weights through 256-column MMAs, the partial sums going through a workspace and a reduce pass;
+// when K is too short to split, 64-column tiles spread the columns instead.
+ProjPlan proj_plan(int M, int N, int K, int sms) {
+  const long long tiles256 = static_cast<long long>((M + kPM - 1) / kPM) * ((N + 255) / 256);
+  const int k_stages = K / kPK;
+  if (2 * tiles256 >= sms) return ProjPlan{256, 1};
+  const int ks = static_cast<int>(std::min<long long>(sms / std::max<long long>(tiles256, 1), k_stages / 4));
+  if (ks >= 2) return ProjPlan{256, ks};
+  return ProjPlan{64, 1};
+}
+
+size_t proj_workspace(int M, int N, int K, int sms) {
+  const ProjPlan pl = proj_plan(M, N, K, sms);
+  return pl.k_splits > 1 ? static_cast<size_t>(pl.k_splits) * M * N * sizeof(float) : 0;
+}
+
 template <int AM, int BM, int EM>
 static int launch_proj_nt(const ProjSpec& p, cudaStream_t st) {
-  const long long tiles256 = static_cast<long long>((p.M + kPM - 1) / kPM) * ((p.N + 255) / 256);
-  if (2 * tiles256 < sm_count()) return launch_proj_t<AM, BM, EM, 64>(p, st);
-  return launch_proj_t<AM, BM, EM, 256>(p, st);
+  const ProjPlan pl = proj_plan(p.M, p.N, p.K, sm_count());
+  if (pl.nt == 64) return launch_proj_t<AM, BM, EM, 64>(p, 1, st);
+  return launch_proj_t<AM, BM, EM, 256>(p, pl.k_splits, st);
 }
 
 int launch_proj(const ProjSpec& p, cudaStream_t st) {

@@ -298,6 +298,10 @@ DFLASH2_API int dflash2_score_edges_ragged(const int32_t* cand, const float* una
  *   the GEMM's epilogue (fp32 add, one rounding). G divides 32, M % G == 0, group_size in {8, 16, 32},
  *   N % 32 == 0. out may not alias residual.
  *
+ * Workspace: at least dflash2_proj_workspace_bytes(M, N, K) bytes, 256-byte aligned (0 bytes, and
+ * workspace may be NULL, when the shape does not split K: with few rows the K range is split over
+ * the SMs and the partial sums go through the workspace to a reduce pass that applies the epilogue).
+ *
  * Weights: wbits = 16: w is bf16 [N, K] (out, in). wbits = 4: affine 4-bit weights in groups of 64
  * along K (dflash2.ts quantizedWeight: quantize(w, 64, bits), mode "affine"): w is [N, K/8] uint32,
  * value k of row n in bits 4 (k % 8) .. 4 (k % 8) + 3 of word k / 8 (an unsigned q in [0, 15]);
@@ -309,14 +313,17 @@ DFLASH2_API int dflash2_score_edges_ragged(const int32_t* cand, const float* una
 DFLASH2_API int dflash2_conv_coefficients(const void* x, const void* norm_w, float eps, const void* w_kp, int B, int G,
                                           int H, int group_size, int taps, int dtype, void* n_out, float* d0,
                                           void* coef1, void* workspace, size_t workspace_bytes, void* stream);
+DFLASH2_API size_t dflash2_proj_workspace_bytes(int M, int N, int K);
 DFLASH2_API int dflash2_proj(const void* a, int M, int K, const void* w, const void* w_scales, const void* w_biases,
-                             int wbits, int N, int dtype, void* out, void* stream);
+                             int wbits, int N, int dtype, void* out, void* workspace, size_t workspace_bytes,
+                             void* stream);
 DFLASH2_API int dflash2_proj_conv_in(const void* n, const float* d0, const float* base, int G, int group_size, int M,
                                      int K, const void* w, const void* w_scales, const void* w_biases, int wbits, int N,
-                                     int dtype, void* out, void* stream);
+                                     int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream);
 DFLASH2_API int dflash2_proj_conv_out(const void* a, int M, int K, const void* w, const void* w_scales,
                                       const void* w_biases, int wbits, int N, const void* coef1, const float* base,
-                                      int G, int group_size, const void* residual, int dtype, void* out, void* stream);
+                                      int G, int group_size, const void* residual, int dtype, void* out,
+                                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* Self-test of the bounded-wait machinery: launches one block that waits on an mbarrier that
  * nothing completes, with a limit of `limit_us` microseconds (1..1000000). The wait gives up,
