@@ -785,7 +785,12 @@ def kernel_source_sha(name):
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture with
 # caches flushed before the launch) of the head kernel and its top-K merge, by workload, with the
 # hash of the kernel source it was taken on. A capture of a different source is not reported.
-HEAD_TRAFFIC = {}
+HEAD_TRAFFIC = {
+    # tc_pair_kernel<bf16, TOPK> over 960 rows + topk_merge_kernel, mean of two launches of the
+    # full-tail-B64 bench (dram__bytes_read.sum + dram__bytes_write.sum, one-pass metrics)
+    "full-tail-B64": {"bytes": 3.3432591e9 + 1.747840e6 + 2.347776e6, "date": "2026-12-03",
+                      "gemm_sha": "342139484c8922de"},
+}
 
 
 def head_traffic(wl_name):
