@@ -45,19 +45,6 @@ constexpr int kTopL = 16;                          // list length kept per row
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms
 constexpr int kSmemLimit = 232448;
 
-// How far (k-blocks of 64 columns of K) a head pair may run ahead of the slowest pair streaming the
-// same column range: 64 k-blocks of a 256-column tile are 2 MB of weights, well inside the ~7 MB of
-// L2 a column range has when 19 ranges share it.
-#ifndef DFL_PACE_SLACK
-#define DFL_PACE_SLACK 64
-#endif
-constexpr int kPaceSlack = DFL_PACE_SLACK;
-// The leader publishes its count every kPaceEvery k-blocks (a power of two).
-#ifndef DFL_PACE_EVERY
-#define DFL_PACE_EVERY 16
-#endif
-constexpr int kPaceEvery = DFL_PACE_EVERY;
-
 template <int MT>
 struct Cfg {
   static constexpr int kStageBytes = MT * kATile + kBTile;
@@ -92,8 +79,6 @@ struct GemmArgs {
   int* list_idx;
   float* z;               // TOPK: [M][n_extra] or null
   float* logits;          // TOPK: [M][n_main] or null
-  int* progress;          // TOPK pairs: k-blocks issued per (column range, row group), or null
-  int pace_slack;         // how far (k-blocks) a pair may run ahead of the slowest of its range
   int* err;
 };
 
@@ -564,8 +549,7 @@ template <int MODE>
 struct PairCfg {
   static constexpr int kStageBytes = kATile + 2 * kBChunkBytes;
   static constexpr int kEpiWarps = 4;
-  static constexpr int kPacer = MODE == 1 ? 1 : 0;  // TOPK: a warp that paces the row groups
-  static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kPacer;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kAccBufs = 2;
   static constexpr int kTmemCols = 512;
   static constexpr int kBarBytes = 256;
@@ -584,9 +568,8 @@ static_assert(PairCfg<0>::kEpiWarps * PairCfg<0>::kOutPerWarp * PairCfg<0>::kOut
                   PairCfg<0>::kStages * PairCfg<0>::kStageBytes,
               "STORE staging tiles fit in the stage ring");
 static_assert(PairCfg<0>::kStages >= 2 && PairCfg<0>::kSmem <= kSmemLimit, "shared memory budget (pair, store)");
-// barriers, then the TMEM slot, the abort flag and the two pacing words
-static_assert((2 * PairCfg<1>::kStages + 2 * PairCfg<1>::kAccBufs + 1) * 8 + 16 <= PairCfg<1>::kBarBytes, "barriers");
-static_assert((2 * PairCfg<0>::kStages + 2 * PairCfg<0>::kAccBufs + 1) * 8 + 16 <= PairCfg<0>::kBarBytes, "barriers");
+static_assert((2 * PairCfg<1>::kStages + 2 * PairCfg<1>::kAccBufs + 1) * 8 + 8 <= PairCfg<1>::kBarBytes, "barriers");
+static_assert((2 * PairCfg<0>::kStages + 2 * PairCfg<0>::kAccBufs + 1) * 8 + 8 <= PairCfg<0>::kBarBytes, "barriers");
 
 // Next tile of the unit range [u, u_end): up to 2 units, never straddling the operand boundary.
 __device__ __forceinline__ bool next_unit_tile(int& u, int u_end, int main_units, int& u0, int& nu) {
@@ -623,8 +606,6 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
   uint64_t* drain = acc_empty + C::kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* pace_limit = abort_flag + 1;  // k-blocks the leader's producer may have issued
-  volatile int* pace_done = abort_flag + 2;   // the producer has issued everything
   float* sbias_all = reinterpret_cast<float*>(bar_area + C::kBarBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -653,8 +634,6 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
-    *pace_limit = INT_MAX;
-    *pace_done = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -706,14 +685,6 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      // Pacing (TOPK, leader): the pairs of the row groups that share this column range stream the
-      // same weight tiles; kept within pace_slack k-blocks of each other, each tile comes from DRAM
-      // once and is an L2 hit for the others. The leader publishes its count every kPaceEvery
-      // k-blocks and waits while it is more than pace_slack ahead of the slowest (the pacer warp's
-      // limit).
-      int* my_progress = (MODE == 1 && rank == 0 && a.progress != nullptr && a.m_groups > 1)
-                             ? a.progress + ns * a.m_groups + mg
-                             : nullptr;
       int u = u_begin, u0 = 0, nu = 0;
       while (ok && next_unit_tile(u, u_end, a.main_units, u0, nu)) {
         const bool extra = u0 >= a.main_units;
@@ -724,19 +695,6 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
         for (int kb = kb0; kb < kb1; ++kb) {
           // the first tile's first w_pre stages: fresh barriers, byte count and weights already set
           const bool pre = issued < w_pre;
-          if (my_progress != nullptr) {
-            if ((issued & (kPaceEvery - 1)) == 0) st_relaxed_gpu(my_progress, issued);
-            if (issued > *pace_limit) {
-              const uint64_t t0 = globaltimer_ns();
-              while (issued > *pace_limit && *abort_flag == 0) {
-                __nanosleep(64);
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {  // never block on pacing: stop it
-                  my_progress = nullptr;
-                  break;
-                }
-              }
-            }
-          }
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
@@ -757,10 +715,6 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
             phase ^= 1u;
           }
         }
-      }
-      if (MODE == 1 && rank == 0 && a.progress != nullptr && a.m_groups > 1) {
-        st_relaxed_gpu(a.progress + ns * a.m_groups + mg, INT_MAX / 2);  // finished: paces nobody
-        *pace_done = 1;
       }
       // Every stage released: all of the leader's commits towards this CTA have landed.
       for (int i = 0; ok && i < C::kStages; ++i) {
@@ -850,26 +804,6 @@ __global__ void __launch_bounds__(PairCfg<MODE>::kThreads, 1)
           mbar_wait_bounded(smem_u32(drain), 0, nullptr, kDrainLimitNs);
         }
       }
-    }
-    __syncwarp();
-  } else if (C::kPacer && warp == 2 + C::kEpiWarps) {
-    // ------------------------------------------------------------------ pacer (TOPK leader)
-    // Polls the progress of the row groups sharing this column range and publishes, in shared
-    // memory, how far the producer may run: the slowest count plus pace_slack. Counts outside
-    // [0, total] (another launch's leftovers, never written) are ignored. Bounded in time.
-    if (lane == 0 && rank == 0 && a.progress != nullptr && a.m_groups > 1) {
-      const int* base = a.progress + ns * a.m_groups;
-      const uint64_t t0 = globaltimer_ns();
-      while (*pace_done == 0 && *abort_flag == 0 && globaltimer_ns() - t0 < kWaitLimitNs) {
-        int lo = INT_MAX;
-        for (int g = 0; g < a.m_groups; ++g) {
-          const int v = ld_relaxed_gpu(base + g);
-          if (v >= 0 && v < lo) lo = v;
-        }
-        *pace_limit = lo >= INT_MAX / 2 ? INT_MAX : lo + a.pace_slack;
-        __nanosleep(256);
-      }
-      *pace_limit = INT_MAX;
     }
     __syncwarp();
   } else {
@@ -1276,8 +1210,6 @@ bool make_tmap_sw128(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t co
   return r == CUDA_SUCCESS;
 }
 
-
-
 // Largest M-tile count per CTA the head uses (2: one weight tile feeds 256 rows, single-buffered
 // accumulator; 1: 128 rows, double-buffered accumulator).
 #ifndef DFL_HEAD_MAX_MT
@@ -1314,9 +1246,7 @@ size_t head_workspace(int M, int V, int K, int R, int sms) {
   (void)K;
   const GemmPlan p = head_plan(M, 0, V, R, sms);
   const size_t lists = static_cast<size_t>(p.n_splits) * M * kTopL;
-  const size_t list_bytes = (lists * (sizeof(float) + sizeof(int)) + 255) & ~static_cast<size_t>(255);
-  // the pair head's progress counters, one per (column range, row group)
-  return list_bytes + (p.pair ? static_cast<size_t>(p.n_splits) * p.m_groups * sizeof(int) : 0) + 256;
+  return lists * (sizeof(float) + sizeof(int)) + 256;
 }
 
 int gemm_pair_capacity() { return pair_capacity(); }
@@ -1371,11 +1301,6 @@ int launch_head_topk(const GemmProblem& p, const GemmPlan& plan, const float* bi
   const size_t lists = static_cast<size_t>(plan.n_splits) * p.M * kTopL;
   a.list_val = static_cast<float*>(workspace);
   a.list_idx = reinterpret_cast<int*>(a.list_val + lists);
-  if (plan.pair && plan.m_groups > 1) {
-    const size_t list_bytes = (lists * (sizeof(float) + sizeof(int)) + 255) & ~static_cast<size_t>(255);
-    a.progress = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + list_bytes);
-    a.pace_slack = kPaceSlack;
-  }
   a.bias = bias;
   a.z = z;
   a.logits = logits;

@@ -94,16 +94,6 @@ __device__ __forceinline__ bool mbar_wait_bounded_suspend(uint32_t bar, uint32_t
   }
 }
 
-// Relaxed gpu-scope global store / load of a counter that other CTAs poll.
-__device__ __forceinline__ void st_relaxed_gpu(int* p, int v) {
-  asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
-  int v;
-  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
