@@ -154,6 +154,7 @@ int dflash2_conv_prepare(const void* x, const void* norm_w, float eps, const voi
     if (rc != DFLASH2_OK) return rc;
     n = ws;
   }
+  if (kp_small_eligible(s, sms)) return launch_kp_small(s, n, w_kp, base, out, coef1, d_full, st);
   float* part = reinterpret_cast<float*>(ws + n_bytes);
   const GemmProblem gp{n, w_kp, nullptr, s.rows(), H, 4 * s.groups, 0, dtype};
   rc = launch_gemm_store(gp, plan, part, st);
@@ -227,6 +228,7 @@ int dflash2_conv_coefficients(const void* x, const void* norm_w, float eps, cons
     if (rc != DFLASH2_OK) return rc;
     n = n_out;
   }
+  if (kp_small_eligible(s, sms)) return launch_kp_small(s, n, w_kp, nullptr, nullptr, coef1, nullptr, st, d0);
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + n_bytes);
   const GemmProblem gp{n, w_kp, nullptr, s.rows(), H, 4 * s.groups, 0, dtype};
   rc = launch_gemm_store(gp, plan, part, st);

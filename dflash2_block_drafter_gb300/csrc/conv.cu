@@ -663,6 +663,81 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
   }
 }
 
+// finish (+ the next RMSNorm) for a few rows: one CTA per row, thread i owning channels
+// 8i .. 8i + 7, so that a small batch spreads over as many SMs as it has rows instead of the few
+// clusters of the strip-resident kernel. Same arithmetic as that kernel:
+//   x = residual + (base[1][0] + D10) y[t] + (base[1][1] + D11) y[t - 1]   (rounded to T)
+//   n = (x * rsqrt(mean(x^2) + eps)) * w   for rows t >= next_row0 (next_w given)
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads)
+    conv_finish_rows_kernel(const T* __restrict__ y, const T* __restrict__ coef1, const float* __restrict__ base,
+                            const T* __restrict__ residual, T* __restrict__ out, const T* __restrict__ next_w,
+                            float eps, T* __restrict__ next_n, int G, int H, int gs, int groups, int next_row0,
+                            const int32_t* __restrict__ row_off, int m_out, int* err) {
+  __shared__ float warp_ss[32];
+  __shared__ float row_r;
+  pdl_trigger();
+  pdl_wait();
+  const int o = blockIdx.x;  // row b * G + t
+  const int b = o / G;
+  const int t = o - b * G;
+  const int c = threadIdx.x * 8;
+  const bool active = c < H;
+  float xr[8];
+  float ss = 0.f;
+  if (active) {
+    float cur[8], prev[8], res[8], b0[8], b1[8];
+    load8(y + static_cast<size_t>(o) * H + c, cur);
+    if (t > 0) {
+      load8(y + static_cast<size_t>(o - 1) * H + c, prev);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) prev[i] = 0.f;
+    }
+    if (residual != nullptr) {
+      load8(residual + static_cast<size_t>(o) * H + c, res);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) res[i] = 0.f;
+    }
+    load8(base + 2 * static_cast<size_t>(H) + c, b0);  // base[1][0]
+    load8(base + 3 * static_cast<size_t>(H) + c, b1);  // base[1][1]
+    const int g = c / gs;
+    const float d0 = load1(coef1 + (static_cast<size_t>(o) * 2 + 0) * groups + g);
+    const float d1 = load1(coef1 + (static_cast<size_t>(o) * 2 + 1) * groups + g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float x = fmaf(b0[i] + d0, cur[i], (b1[i] + d1) * prev[i]) + res[i];
+      xr[i] = round_as<T>(x);
+      ss = fmaf(xr[i], xr[i], ss);
+    }
+    store8(out + static_cast<size_t>(o) * H + c, xr);
+  }
+  if (next_n == nullptr) return;
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, s);
+  if ((threadIdx.x & 31) == 0) warp_ss[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? warp_ss[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) v += __shfl_xor_sync(0xffffffffu, v, s);
+    if (threadIdx.x == 0) row_r = rsqrtf(v / static_cast<float>(H) + eps);
+  }
+  __syncthreads();
+  if (!active || t < next_row0) return;
+  const int rows_out = G - next_row0;
+  const int i = t - next_row0;
+  const RowSpan span = out_rows(row_off, b, rows_out, m_out, (threadIdx.x == 0 && i == 0) ? err : nullptr);
+  if (i >= span.n) return;
+  const float r = row_r;
+  float w8[8], v[8];
+  load8(next_w + c, w8);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = (xr[j] * r) * w8[j];
+  store8(next_n + (span.first + i) * H + c, v);
+}
+
 // D of one row and group (and of the next group when `two`) summed over KS split-K partial tiles
 // in split order; pa points at split 0's (side, tap) 0 tile, pstride floats apart.
 template <int KS>
@@ -1164,9 +1239,36 @@ static int launch_finish_norm(const ConvShape& s, int csize, const void* y, cons
 #define DFL_FINISH_NORM 1
 #endif
 
+// The row-per-CTA finish takes batches of at most this many rows (a CTA per row, all resident at once).
+#ifndef DFL_FINISH_ROWS_MAX
+#define DFL_FINISH_ROWS_MAX 256
+#endif
+static bool finish_rows_eligible(const ConvShape& s) {
+  return s.rows() <= DFL_FINISH_ROWS_MAX && s.H % 8 == 0 && s.H / 8 <= kNormThreads && s.gs % 8 == 0;
+}
+
+template <typename T>
+static int launch_finish_rows(const ConvShape& s, const void* y, const void* coef1, const float* base,
+                              const void* residual, void* out, const void* next_w, float eps, void* next_n,
+                              int next_row0, cudaStream_t st, const int32_t* row_off, int m_out) {
+  const int threads = ((s.H / 8 + 31) / 32) * 32;
+  const cudaError_t e = launch_pdl(conv_finish_rows_kernel<T>, dim3(s.rows()), dim3(threads), 0, st, nullptr, 0,
+                                   static_cast<const T*>(y), static_cast<const T*>(coef1), base,
+                                   static_cast<const T*>(residual), static_cast<T*>(out),
+                                   static_cast<const T*>(next_w), eps, static_cast<T*>(next_n), s.G, s.H, s.gs,
+                                   s.groups, next_row0, row_off, m_out, device_error_word());
+  return e == cudaSuccess ? DFLASH2_OK : fail(DFLASH2_ERR_CUDA, "finish rows launch failed: %s", cudaGetErrorString(e));
+}
+
 int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, const float* base, const void* residual,
                       void* out, const void* next_w, float eps, void* next_n, int next_row0, cudaStream_t st,
                       const int32_t* row_off, int m_out) {
+  if (finish_rows_eligible(s))
+    return s.dtype == DFLASH2_F32
+               ? launch_finish_rows<float>(s, y, coef1, base, residual, out, next_w, eps, next_n, next_row0, st,
+                                           row_off, m_out)
+               : launch_finish_rows<__nv_bfloat16>(s, y, coef1, base, residual, out, next_w, eps, next_n, next_row0,
+                                                   st, row_off, m_out);
   const int csize = (DFL_FINISH_NORM && next_n != nullptr) ? finish_norm_cluster(s) : 0;
   if (csize > 0)
     return s.dtype == DFLASH2_F32
@@ -1202,12 +1304,12 @@ int launch_conv_side1(const ConvShape& s, const void* y, const void* coef1, cons
 }
 
 int conv_prepare_kernels(const ConvShape& s, bool with_norm) {
-  (void)s;
-  return (with_norm ? 1 : 0) + 2;  // [RMSNorm] + kernel_projection + side-0 pass
+  // [RMSNorm] + kernel_projection + side-0 pass, or the two in one kernel for a few rows
+  return (with_norm ? 1 : 0) + (kp_small_eligible(s, sm_count()) ? 1 : 2);
 }
 
 int conv_finish_kernels(const ConvShape& s, bool with_next_norm) {
-  if (!with_next_norm) return 1;
+  if (!with_next_norm || finish_rows_eligible(s)) return 1;
   return (DFL_FINISH_NORM && finish_norm_cluster(s) > 0) ? 1 : 2;
 }
 

@@ -1210,6 +1210,21 @@ bool make_tmap_sw128(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t co
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_sw128_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t planes,
+                        uint64_t plane_stride_bytes, uint32_t box_rows, uint32_t box_planes) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(plane_stride_bytes)};
+  cuuint32_t box[3] = {64, box_rows, box_planes};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Largest M-tile count per CTA the head uses (2: one weight tile feeds 256 rows, single-buffered
 // accumulator; 1: 128 rows, double-buffered accumulator).
 #ifndef DFL_HEAD_MAX_MT

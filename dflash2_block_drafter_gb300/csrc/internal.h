@@ -83,6 +83,11 @@ size_t conv_prepare_workspace(const ConvShape& s, int sms);
 int launch_rmsnorm(const void* x, const void* w, float eps, void* n, int rows, int H, int dtype, cudaStream_t st);
 int launch_conv_side0(const ConvShape& s, const void* n, const float* part, int k_splits, const float* base,
                       void* out, void* coef1, float* d_full, cudaStream_t st);
+// kernel_projection and the side-0 pass in one kernel for at most 128 bf16 rows (kp_small.cu);
+// with out = null and d0 given, the coefficients only (d0 [2][groups][M] fp32, coef1).
+bool kp_small_eligible(const ConvShape& s, int sms);
+int launch_kp_small(const ConvShape& s, const void* n, const void* w_kp, const float* base, void* out, void* coef1,
+                    float* d_full, cudaStream_t st, float* d0 = nullptr);
 // Kernels one prepare call launches (the optional first RMSNorm, kernel_projection, the side-0
 // pass) and one finish call (the fused finish + next norm, or the side-1 pass and the norm).
 int conv_prepare_kernels(const ConvShape& s, bool with_norm);
@@ -129,6 +134,10 @@ int launch_wait_selftest(int limit_us, cudaStream_t st);
 // bf16 row-major [rows, cols] operand for tcgen05: box of 64 elements (128 bytes) x box_rows rows,
 // 128-byte swizzle (defined in gemm.cu).
 bool make_tmap_sw128(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// The same over `planes` planes of [rows, cols] (plane_stride_bytes apart): box of 64 elements x
+// box_rows rows x box_planes planes, landing as box_planes consecutive [box_rows][128 B] tiles.
+bool make_tmap_sw128_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t planes,
+                        uint64_t plane_stride_bytes, uint32_t box_rows, uint32_t box_planes);
 
 // ---------------------------------------------------------------- sublayer projections (proj.cu)
 // out[M, N] = A[M, K] W[N, K]^T (bf16 in and out, fp32 accumulation), with optional fusions:

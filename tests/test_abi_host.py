@@ -161,10 +161,18 @@ def test_launch_count_queries(lib):
     # finish with the next norm is one fused kernel where its tiles fit
     assert lib.dflash2_conv_finish_launches(64, 16, 5120, 16, bf16, 1) == 1
     assert lib.dflash2_conv_finish_launches(64, 16, 5120, 16, bf16, 0) == 1
-    # H not a multiple of 256 channels: a side-1 pass and a separate norm
-    assert lib.dflash2_conv_finish_launches(5, 7, 320, 16, bf16, 1) == 2
-    # G above 32 rows per block: not fused either
+    # up to 128 bf16 rows: kernel_projection and the side-0 pass in one kernel
+    assert lib.dflash2_conv_prepare_launches(1, 16, 5120, 16, bf16, 0) == 1
+    assert lib.dflash2_conv_prepare_launches(8, 16, 5120, 16, bf16, 1) == 2
+    assert lib.dflash2_conv_prepare_launches(9, 16, 5120, 16, bf16, 0) == 2
+    assert lib.dflash2_conv_prepare_launches(1, 16, 5120, 16, f32, 0) == 2
+    # up to 256 rows: finish and the next norm in one row-per-CTA kernel, whatever H and G
+    assert lib.dflash2_conv_finish_launches(5, 7, 320, 16, bf16, 1) == 1
+    assert lib.dflash2_conv_finish_launches(16, 16, 5120, 16, bf16, 1) == 1
+    # above that, H not a multiple of 256 channels or G above 32 rows per block: a side-1 pass and
+    # a separate norm
     assert lib.dflash2_conv_finish_launches(5, 64, 256, 16, f32, 1) == 2
+    assert lib.dflash2_conv_finish_launches(64, 7, 320, 16, bf16, 1) == 2
     assert lib.dflash2_conv_prepare_launches(1, 16, 5000, 16, bf16, 0) == -1  # H % 64: rejected
     assert lib.dflash2_conv_finish_launches(1, 65, 5120, 16, bf16, 1) == -1   # G > 64: rejected
 
