@@ -17,7 +17,7 @@ INCLUDE = os.path.join(REPO_DIR, "include")
 BUILD_DIR = os.path.join(REPO_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libdflash2.so")
 
-SOURCES = ["abi.cu", "conv.cu", "gemm.cu", "selector.cu", "noalloc.cu", "proj.cu", "kp_small.cu"]
+SOURCES = ["abi.cu", "conv.cu", "gemm.cu", "selector.cu", "noalloc.cu", "proj.cu", "kp_small.cu", "proj_small.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                 "--expt-relaxed-constexpr", "-I", INCLUDE]

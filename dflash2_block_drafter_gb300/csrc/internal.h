@@ -166,6 +166,10 @@ struct ProjPlan {
   int k_splits;  // K ranges summed by a reduce pass (1: none)
 };
 ProjPlan proj_plan(int M, int N, int K, int sms);
+// At most 128 rows: the weight rows on the MMA's 128-row side, K split over a cluster and reduced in
+// shared memory, no workspace (proj_small.cu).
+bool proj_small_eligible(int M, int N, int K);
+int launch_proj_small(const ProjSpec& p, cudaStream_t st);
 size_t proj_workspace(int M, int N, int K, int sms);
 int launch_proj(const ProjSpec& p, cudaStream_t st);
 // D from kernel_projection's split-K partials: d0 = side 0's deltas (fp32), coef1 = side 1's (dtype).

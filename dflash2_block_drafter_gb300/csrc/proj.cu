@@ -721,6 +721,7 @@ ProjPlan proj_plan(int M, int N, int K, int sms) {
 }
 
 size_t proj_workspace(int M, int N, int K, int sms) {
+  if (proj_small_eligible(M, N, K)) return 0;  // the small-row kernel reduces in shared memory
   const ProjPlan pl = proj_plan(M, N, K, sms);
   return pl.k_splits > 1 ? static_cast<size_t>(pl.k_splits) * M * N * sizeof(float) : 0;
 }
@@ -733,6 +734,7 @@ static int launch_proj_nt(const ProjSpec& p, cudaStream_t st) {
 }
 
 int launch_proj(const ProjSpec& p, cudaStream_t st) {
+  if (proj_small_eligible(p.M, p.N, p.K)) return launch_proj_small(p, st);
   const bool am = p.d0 != nullptr, bm = p.wbits == 4, em = p.coef1 != nullptr;
   if (am && bm && em) return launch_proj_nt<1, 1, 1>(p, st);
   if (am && bm) return launch_proj_nt<1, 1, 0>(p, st);
