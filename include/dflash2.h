@@ -112,8 +112,9 @@ DFLASH2_API int dflash2_poll_error(void* stream);
  * ---------------------------------------------------------------------------------- */
 DFLASH2_API size_t dflash2_conv_prepare_workspace_bytes(int B, int G, int H, int group_size, int dtype);
 /* Number of kernels one dflash2_conv_prepare call launches for this shape (with_norm: norm_w
- * given) and one dflash2_conv_finish call (with_next_norm: next_norm_w given): with the next
- * norm, finish is a single fused kernel where its tiles fit, else a side-1 pass and a norm pass.
+ * given; kernel_projection and the side-0 pass are one kernel up to 128 bf16 rows, two above) and
+ * one dflash2_conv_finish call (with_next_norm: next_norm_w given): with the next norm, finish is a
+ * single fused kernel up to 256 rows or where its tiles fit, else a side-1 pass and a norm pass.
  * -1 for a shape the calls reject. Host-only; launches nothing. */
 DFLASH2_API int dflash2_conv_prepare_launches(int B, int G, int H, int group_size, int dtype, int with_norm);
 DFLASH2_API int dflash2_conv_finish_launches(int B, int G, int H, int group_size, int dtype, int with_next_norm);
@@ -299,8 +300,10 @@ DFLASH2_API int dflash2_score_edges_ragged(const int32_t* cand, const float* una
  *   N % 32 == 0. out may not alias residual.
  *
  * Workspace: at least dflash2_proj_workspace_bytes(M, N, K) bytes, 256-byte aligned (0 bytes, and
- * workspace may be NULL, when the shape does not split K: with few rows the K range is split over
- * the SMs and the partial sums go through the workspace to a reduce pass that applies the epilogue).
+ * workspace may be NULL, when the shape needs none: up to 128 rows the K range is split over the
+ * CTAs of a thread-block cluster and reduced in shared memory; above, a shape whose tiles do not
+ * fill the SMs splits K over them and the partial sums go through the workspace to a reduce pass
+ * that applies the epilogue).
  *
  * Weights: wbits = 16: w is bf16 [N, K] (out, in). wbits = 4: affine 4-bit weights in groups of 64
  * along K (dflash2.ts quantizedWeight: quantize(w, 64, bits), mode "affine"): w is [N, K/8] uint32,
