@@ -606,30 +606,45 @@ def our_arm(args, wl_name):
               ([h_h] if h_h is not None else []) + ([h_anchors] if h_anchors is not None else []))
     d2h = h_out.numel() * h_out.element_size()
     e2e_ms = []
-    # the full tail with host inputs as one CUDA graph: the copies are graph nodes on a branch of
-    # their own, each site's finish waiting only for its own sublayer output
-    e2e_graph = run.capture(run.full_from_host, h_x0, h_ys, h_anchors, x0, ys, anchors, ragged=rag) \
-        if (full_tail and args.graph) else None
-    for i in range(args.warmup + args.steps):
+    if full_tail:
+        # A serving loop through the runner's public host-input pipeline: two device input sets
+        # alternate, batch i + 1's inputs are copied from pinned host memory while batch i
+        # computes, and every batch's path is copied back to the host after its pass. One timed
+        # region over the K steps; every step's copies are inside it (the first step's copies
+        # overlap nothing). The head's weight stream (2.54 GB a step) is larger than L2.
+        sets = [(x0, ys, anchors), (x0.clone(), [y.clone() for y in ys], anchors.clone())]  # both valid
+        if args.graph:
+            graphs = [run.capture(run.full_ragged, *sets[k], *rag) if rag is not None else run.capture(run.full, *sets[k])
+                      for k in range(2)]
+        else:
+            graphs = None
+        h_outs = [h_out, torch.empty_like(h_out).pin_memory()]
+        batch = (h_x0, h_ys, h_anchors)
+        run.pipeline_from_host([batch] * args.warmup, sets, [h_outs[i % 2] for i in range(args.warmup)], graphs,
+                               ragged=rag)
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        run.pipeline_from_host([batch] * args.steps, sets, [h_outs[i % 2] for i in range(args.steps)], graphs,
+                               ragged=rag)
+        e.record(stream)
+        e.synchronize()
+        e2e_ms.append(s.elapsed_time(e))
+    for i in range(0 if full_tail else args.warmup + args.steps):
         flush.zero_()
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record(stream)
-        if e2e_graph is not None:
-            e2e_graph.replay()
-        elif full_tail:
-            # inputs copied on a copy stream; each site waits only for its own sublayer output
-            run.full_from_host(h_x0, h_ys, h_anchors, x0, ys, anchors, ragged=rag)
-        else:
-            if h_x0 is not None:
-                x0.copy_(h_x0, non_blocking=True)
-            for yd, yh in zip(ys, h_ys):
-                yd.copy_(yh, non_blocking=True)
-            if h_h is not None:
-                h_in.copy_(h_h, non_blocking=True)
-            if h_anchors is not None:
-                anchors.copy_(h_anchors, non_blocking=True)
-            step()
+        if h_x0 is not None:
+            x0.copy_(h_x0, non_blocking=True)
+        for yd, yh in zip(ys, h_ys):
+            yd.copy_(yh, non_blocking=True)
+        if h_h is not None:
+            h_in.copy_(h_h, non_blocking=True)
+        if h_anchors is not None:
+            anchors.copy_(h_anchors, non_blocking=True)
+        step()
         h_out.copy_(out_dev, non_blocking=True)
         e.record(stream)
         e.synchronize()
@@ -788,8 +803,8 @@ def kernel_source_sha(name):
 HEAD_TRAFFIC = {
     # tc_pair_kernel<bf16, TOPK> over 960 rows + topk_merge_kernel, mean of two launches of the
     # full-tail-B64 bench (dram__bytes_read.sum + dram__bytes_write.sum, one-pass metrics)
-    "full-tail-B64": {"bytes": 3.3432591e9 + 1.747840e6 + 2.347776e6, "date": "2026-12-03",
-                      "gemm_sha": "342139484c8922de"},
+    "full-tail-B64": {"bytes": (2.947082496e9 + 3.107712256e9) / 2 + (3.199232e6 + 0.340992e6) / 2 + 2.347776e6,
+                      "date": "2026-12-03", "gemm_sha": "cc1ceec837c9c86c"},
 }
 
 

@@ -211,6 +211,59 @@ class TailRunner:
                 t.record_stream(cs)
         return path
 
+    def pipeline_from_host(self, batches, sets, out_host, graphs=None, ragged=None):
+        """Runs the tail over a sequence of batches in pinned host memory back to back, the way a
+        serving loop does. Two device input sets alternate: batch i + 1's inputs are copied on
+        the copy stream while batch i computes (a set is refilled only after the pass that read it
+        has finished), and every batch's path is copied into its pinned host buffer right after
+        its pass.
+
+        batches: list of (h_x0, h_ys, h_anchors) pinned host tensors; sets: two (x0, ys, anchors)
+        device buffer sets; out_host: one pinned [B, steps] int32 tensor per batch (a tensor may
+        appear several times); graphs: optional two captured passes, ``graphs[k]`` over
+        ``sets[k]`` (``capture(self.full, *sets[k])``); ragged = (row_offsets, m_rows) runs
+        ``full_ragged`` instead of ``full``. Everything is enqueued on the current stream and the
+        copy stream; the caller synchronizes."""
+        comp = torch.cuda.current_stream()
+        if getattr(self, "_copy_stream", None) is None:
+            self._copy_stream = torch.cuda.Stream(device=comp.device)
+        cs = self._copy_stream
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        freed = [None, None]  # after the last pass that read set k
+
+        def issue(i):
+            k = i % 2
+            if freed[k] is not None:
+                cs.wait_event(freed[k])
+            else:
+                cs.wait_stream(comp)
+            h_x0, h_ys, h_anchors = batches[i]
+            x0, ys, anchors = sets[k]
+            with torch.cuda.stream(cs):
+                x0.copy_(h_x0, non_blocking=True)
+                for dst, src in zip(ys, h_ys):
+                    dst.copy_(src, non_blocking=True)
+                anchors.copy_(h_anchors, non_blocking=True)
+                copied[k].record(cs)
+
+        if batches:
+            issue(0)
+        for i in range(len(batches)):
+            if i + 1 < len(batches):
+                issue(i + 1)
+            k = i % 2
+            comp.wait_event(copied[k])
+            if graphs is not None:
+                graphs[k].replay()
+            elif ragged is not None:
+                self.full_ragged(*sets[k], *ragged)
+            else:
+                self.full(*sets[k])
+            ev = torch.cuda.Event()
+            ev.record(comp)
+            freed[k] = ev
+            out_host[i].copy_(self.path, non_blocking=True)
+
     def capture(self, fn, *args, **kwargs) -> "torch.cuda.CUDAGraph":
         """Record one pass of ``fn`` (e.g. ``self.full``) into a CUDA graph over the runner's fixed
         buffers; ``graph.replay()`` then re-launches every kernel of the pass with one call.

@@ -152,3 +152,33 @@ def test_full_from_host_graph_replay(torch):
     assert torch.equal(run.path, want[0])
     assert torch.equal(run.S, want[1])
     assert torch.equal(run.h, want[2])
+
+
+def test_pipeline_from_host_matches_each_batch(torch):
+    """Three host batches through the two-set pipeline (the third refills the first set after the
+    first pass has read it): each batch's path equals the device-input pass on that batch, eager
+    and with a captured pass per set."""
+    from dflash2_block_drafter_gb300.tail import TailRunner, to_device
+    import dflash2_block_drafter_gb300 as d
+    wl = I.make_config(0, B=4)
+    run = TailRunner(wl)
+    base_x0 = to_device(wl.x0)
+    base_ys = [to_device(s.y) for s in wl.sites]
+    anchors = to_device(wl.anchors)
+    batches, want = [], []
+    for scale in (1.0, -1.0, 0.5):  # exact in bf16
+        x0 = (base_x0.float() * scale).to(base_x0.dtype)
+        ys = [(y.float() * scale).to(y.dtype) for y in base_ys]
+        run.full(x0, ys, anchors)
+        want.append(run.path.cpu().clone())
+        batches.append((x0.cpu().pin_memory(), [y.cpu().pin_memory() for y in ys], anchors.cpu().pin_memory()))
+    # both sets hold valid inputs before anything reads them (a capture runs its pass once)
+    sets = [(base_x0.clone(), [y.clone() for y in base_ys], anchors.clone()) for _ in range(2)]
+    for use_graphs in (False, True):
+        graphs = [run.capture(run.full, *sets[k]) for k in range(2)] if use_graphs else None
+        outs = [torch.full(tuple(run.path.shape), -7, dtype=torch.int32).pin_memory() for _ in batches]
+        run.pipeline_from_host(batches, sets, outs, graphs)
+        torch.cuda.synchronize()
+        assert d.dflash2_poll_error() == 0
+        for got, ref in zip(outs, want):
+            assert torch.equal(got, ref)
