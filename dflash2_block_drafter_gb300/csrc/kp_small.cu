@@ -49,6 +49,10 @@ constexpr int kKsMaxStages = 12;
 constexpr int kKsSmemLimit = 232448;
 constexpr int kKsBarBytes = 256;
 constexpr int kKsMinSmem = 64 * 1024;  // at most three CTAs per SM: their TMEM (<= 128 columns each) always fits
+constexpr int kKsHalfSmem = 112 * 1024;  // two CTAs per SM
+#ifndef DFL_KS_TWO_PER_SM
+#define DFL_KS_TWO_PER_SM 1
+#endif
 constexpr uint64_t kKsDrainNs = 100000000ull;  // 100 ms
 
 struct KsArgs {
@@ -441,6 +445,14 @@ bool ks_layout(const ConvShape& s, int tg, int ks, KsPlan* p) {
   const int nkb = (k_blocks + ks - 1) / ks;
   p->n_stages = std::min(std::min(nkb, kKsMaxStages), avail / p->stage_bytes);
   if (p->n_stages < 1) return false;
+  // Two CTAs per SM where a ring of at least four stages still fits in half of an SM: the next
+  // launch's clusters then start on the SMs this one holds and request their weights before the
+  // dependent-launch wait, instead of waiting for this launch's CTAs to leave.
+  const int avail_half = kKsHalfSmem - 1024 - kKsBarBytes - r_bytes - stg_bytes;
+  const int n_half = std::min(std::min(nkb, kKsMaxStages), std::max(0, avail_half) / p->stage_bytes);
+  if (DFL_KS_TWO_PER_SM && n_half >= std::min(nkb, 4) &&
+      round1024(std::max(n_half * p->stage_bytes, p_bytes)) <= avail_half)
+    p->n_stages = n_half;
   const int ring = round1024(std::max(p->n_stages * p->stage_bytes, p_bytes));
   if (ring > avail) return false;
   p->r_off = ring;
