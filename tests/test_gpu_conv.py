@@ -135,3 +135,28 @@ def test_conv_chain_b64_sampled_blocks(torch):
     ref, _ = O.conv_chain(I.to_f64(wl.x0)[blocks], oracle_sites(wl, blocks), wl.eps, wl.gs)
     assert_close_scaled(got[blocks], ref, what="chain B=64 (sampled)")
     assert np.all(np.isfinite(got))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("B,G,H,gs", [(1, 16, 5120, 16), (3, 7, 320, 16), (8, 16, 1024, 32), (9, 16, 512, 16)])
+def test_conv_coefficients_parity(torch, dtype, B, G, H, gs):
+    """Prepare without the side-0 output: side 0's deltas [tap][group][row] (fp32) and side 1's
+    [row][tap][group] against the oracle's kernel_projection of the normed rows, and the normed
+    rows themselves. Up to 128 bf16 rows this is the small-row kernel's coefficients-only mode,
+    else the split-K GEMM and its reduce pass."""
+    import dflash2_block_drafter_gb300 as d
+    wl = I.conv_case(300 + B * G + H, B, G, H, gs, dtype=dtype)
+    s = wl.sites[0]
+    x = _dev(torch, wl.x0)
+    w_kp, base, norm_w = _site_dev(torch, s)
+    n, d0, c1 = d.dflash2_conv_coefficients(x, norm_w, wl.eps, w_kp, gs)
+    assert d.dflash2_poll_error() == 0
+    os_ = oracle_sites(wl)[0]
+    _, _, rn = O.conv_prepare(I.to_f64(wl.x0), os_.norm_w, wl.eps, os_.w_kp, os_.base, gs)
+    rD = O.kernel_projection(rn, os_.w_kp).reshape(B * G, 2, 2, H // gs)
+    assert_close_scaled(dev_f64(n).reshape(B, G, H), rn, what="normed rows")
+    assert_close_scaled(dev_f64(d0), np.ascontiguousarray(rD[:, 0].transpose(1, 2, 0)), what="side-0 deltas")
+    assert_close_scaled(dev_f64(c1), rD[:, 1], what="side-1 deltas")
+    # the same deltas prepare computes, bit for bit (one kernel_projection per shape)
+    _, coef1 = d.dflash2_conv_prepare(x, norm_w, wl.eps, w_kp, base, gs)
+    assert torch.equal(coef1.reshape(-1), c1.reshape(-1))

@@ -206,3 +206,31 @@ def test_proj_w4_with_both_conv_fusions(torch):
     out_ref = O.sublayer_out(u.float().cpu().numpy().astype(np.float64).reshape(B, G, N), W_out,
                              I.to_f64(d1).reshape(B, G, 2, -1), base.astype(np.float64), gs)
     assert_close_scaled(out.float().cpu().numpy(), out_ref.reshape(M, H), what="W4 conv-out")
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 64, 8), (5, 320, 136), (128, 5120, 256), (16, 5120, 5120)])
+def test_proj_small_rows_bf16_and_w4(torch, M, K, N):
+    """The small-row kernel at its edges: one row (15 zero-filled MMA columns), a K of five
+    k-blocks (a partial 4-bit stage), a weight-row count that is not a multiple of the 128-row tile,
+    the full 128 rows, and the drafter's width. bf16 within the fp32-accumulation bound; 4-bit
+    against the dequantised weight; exact codes equal the bf16 weight bit for bit."""
+    import dflash2_block_drafter_gb300 as d
+    a = I.normal(M + K, "a", (M, K), 1.0)
+    W = I.normal(M + K, "W", (N, K), K ** -0.5)
+    y = d.dflash2_proj(_dev(a), _dev(W))
+    assert d.dflash2_poll_error() == 0
+    got = y.float().cpu().numpy().astype(np.float64)
+    ref = O.projection(I.to_f64(a), I.to_f64(W))
+    assert np.all(np.abs(got - ref) <= _bound(I.to_f64(a), I.to_f64(W))), "outside the fp32-accumulation bound"
+    q = I.affine4_weight(M + N, "w4", N, K)
+    y4 = d.dflash2_proj(_dev(a), _u32(q.packed), w_scales=_gm(q.scales), w_biases=_gm(q.biases))
+    assert d.dflash2_poll_error() == 0
+    W4 = O.affine_dequantize(q.q, I.to_f64(q.scales), I.to_f64(q.biases))
+    got4 = y4.float().cpu().numpy().astype(np.float64)
+    ref4 = O.projection(I.to_f64(a), W4)
+    assert np.all(np.abs(got4 - ref4) <= _bound(I.to_f64(a), W4) + 2.0 ** -9 * np.abs(I.to_f64(a)) @ np.abs(W4).T)
+    qe = I.affine4_weight(M + N + 1, "w4e", N, K, exact=True)
+    We = I.round_to_bf16_bits(O.affine_dequantize(qe.q, I.to_f64(qe.scales), I.to_f64(qe.biases)).astype(np.float32))
+    ye = d.dflash2_proj(_dev(a), _u32(qe.packed), w_scales=_gm(qe.scales), w_biases=_gm(qe.biases))
+    assert torch.equal(ye, d.dflash2_proj(_dev(a), _dev(We)))
+    assert d.dflash2_poll_error() == 0
