@@ -101,6 +101,19 @@ def test_ragged_tail_drafter_shape(torch):
     _check(run, wl, depths, [0, 5, 9, 63], "ragged tail B=64 drafter shape (blocks 0, 5, 9, 63)")
 
 
+def test_ragged_tail_small_batch(torch):
+    """B = 8 at the drafter's shape: the conv runs in the small-row kernels (prepare in one launch,
+    finish + the final norm one CTA per row, which writes the drafted rows packed)."""
+    wl = I.make_config(4, B=8)
+    depths = [15, 1, 0, 7, 3, 20, 11, 2]
+    run, dense_h, off, m = _run_both(wl, depths)
+    dr = _drafted(depths, wl.G)
+    assert m == sum(dr)
+    for b in range(wl.B):
+        assert torch.equal(run.h.view(-1, wl.H)[off[b]:off[b + 1]], dense_h[b, :dr[b]])
+    _check(run, wl, depths, [0, 2, 5], "ragged tail B=8 drafter shape (blocks 0, 2, 5)")
+
+
 def test_ragged_offsets_outside_their_rows_set_the_error_word(torch):
     """A block whose span holds no row, or reaches past m_rows, records DFLASH2_ERR_INVALID_ARG and is
     skipped (path -1); the other blocks are unaffected."""
