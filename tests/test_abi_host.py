@@ -220,3 +220,14 @@ def test_ragged_entry_points_reject_bad_arguments(lib):
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 15, 16, 64, 1000, 30, 1, None, FAKE, None) == -1  # f32 R=64
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 15, 16, 64, 1000, 30, 0, None, None, None) == -1  # no path
     assert b"path" in lib.dflash2_last_error_message() or b"NULL" in lib.dflash2_last_error_message()
+
+
+def test_projection_workspace_query(lib):
+    """Up to 128 rows the projections reduce their K splits in shared memory and need no
+    workspace; a few more rows than one 128-row tile split K through the workspace instead (the
+    query is host-only and needs no device)."""
+    lib.dflash2_proj_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.dflash2_proj_workspace_bytes(1, 5120, 5120) == 0
+    assert lib.dflash2_proj_workspace_bytes(128, 5120, 5120) == 0
+    assert lib.dflash2_proj_workspace_bytes(129, 5120, 5120) > 0
+    assert lib.dflash2_proj_workspace_bytes(1024, 5120, 5120) == 0  # enough tiles: no split
