@@ -110,6 +110,32 @@ def test_block_isolation_on_gpu(torch):
     assert not torch.equal(a1[3], a2[3])
 
 
+@pytest.mark.parametrize("B,G", [(64, 16), (60, 15), (17, 16)])
+def test_prepare_drafter_shape_every_row(torch, B, G):
+    """kernel_projection + side 0 at H=5120 over every row: 1024 rows (four pair row groups, K
+    split in two), 900 rows (a ragged last row group, blocks of 15 straddling the 256-row groups)
+    and 272 rows."""
+    import dflash2_block_drafter_gb300 as d
+    H, gs = 5120, 16
+    wl = I.conv_case(7 + B, B, G, H, gs)
+    s = wl.sites[0]
+    x = _dev(torch, wl.x0)
+    w_kp, base, norm_w = _site_dev(torch, s)
+    d_full = torch.empty((B, G, 2, 2, H // gs), dtype=torch.float32, device="cuda")
+    a, coef1 = d.dflash2_conv_prepare(x, norm_w, wl.eps, w_kp, base, gs, d_full=d_full)
+    assert d.dflash2_poll_error() == 0
+    os_ = oracle_sites(wl)[0]
+    ra, rd1, rn = O.conv_prepare(I.to_f64(wl.x0), os_.norm_w, wl.eps, os_.w_kp, os_.base, gs)
+    assert_close_scaled(dev_f64(d_full), O.kernel_projection(rn, os_.w_kp), what="D")
+    assert_close_scaled(dev_f64(a), ra, what="prepare out")
+    assert_close_scaled(dev_f64(coef1), rd1, what="coef1")
+    # the coefficients-only entry computes the same D in the same order
+    _, d0, c1b = d.dflash2_conv_coefficients(x, norm_w, wl.eps, w_kp, gs)
+    assert d.dflash2_poll_error() == 0
+    assert torch.equal(c1b.reshape(-1), coef1.reshape(-1))
+    assert torch.equal(d0.permute(2, 0, 1).reshape(B, G, 2, H // gs), d_full[:, :, 0])
+
+
 @pytest.mark.parametrize("B", [1, 8])
 def test_conv_chain_drafter_shape(torch, B):
     """The ten-site chain at H=5120, G=16, group 16, compared over every block."""
