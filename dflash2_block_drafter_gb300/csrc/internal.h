@@ -159,13 +159,14 @@ struct ProjSpec {
   const void* coef1;
   const void* residual;
   void* out;
-  float* part;  // split-K partial sums (proj_workspace bytes), or null when the plan does not split
+  float* part;  // split-K partial sums or stream-K slots (proj_workspace bytes), or null when the plan needs none
 };
 struct ProjPlan {
   int nt;        // columns per tile (64 or 256)
   int k_splits;  // K ranges summed by a reduce pass (1: none)
+  int ctas;      // > 0: stream-K over this many CTAs (equal shares of the tiles' k-blocks)
 };
-ProjPlan proj_plan(int M, int N, int K, int sms);
+ProjPlan proj_plan(int M, int N, int K, int sms, bool epilogue_conv);
 // At most 128 rows: the weight rows on the MMA's 128-row side, K split over a cluster and reduced in
 // shared memory, no workspace (proj_small.cu).
 bool proj_small_eligible(int M, int N, int K);

@@ -18,7 +18,14 @@
 //     dequantised to bf16 in shared memory by producer warps; the MMA stays kind::f16.
 //
 // One CTA per SM, persistent over 128 x 256 output tiles (M fastest, so neighbouring CTAs share
-// a weight tile in L2). K advances in 64-element stages: every operand row is one 128-byte
+// a weight tile in L2). With at least half as many tiles as SMs the work is split stream-K: CTA c
+// takes the k-blocks [c T / C, (c + 1) T / C) of the T = tiles x K/64 k-blocks in tile-major order, so
+// every CTA issues the same number of MMAs whatever the tile count. The CTA that holds a tile's
+// first k-block owns the tile: the later CTAs that hold the rest of its K range (always their first
+// piece, which they compute first) write their fp32 partial tile to a workspace slot and raise one
+// flag per 32-row quarter; the owner's epilogue warp of that quarter waits for the flags (bounded),
+// adds the partials in K order and applies the epilogue. Without stream-K (few tiles) K is split
+// into equal ranges summed by a reduce pass. K advances in 64-element stages: every operand row is one 128-byte
 // swizzled row, as TMA writes it, and the producer warps write their tiles in the same layout
 // (16-byte chunk c of row r at chunk position c ^ (r & 7) of the row, 1024-byte aligned tiles).
 // Warp roles: 0 TMA, 1 TMEM + MMA issue (one lane), 2-5 epilogue (TMEM lanes 32 (w % 4) ..),
@@ -80,7 +87,8 @@ struct PCfg {
 struct ProjArgs {
   int M, N, K;
   int k_splits;                // > 1: fp32 partial sums of K ranges to `part`, summed by proj_reduce_kernel
-  float* part;                 // [k_splits][M][N]
+  int stream_k;                // 1: stream-K shares; `part` holds one [128][NT] fp32 slot per CTA
+  float* part;                 // [k_splits][M][N], or the stream-K slots
   int a_rows;                  // rows of the A box (up to 128: fewer when M is small)
   int tiles_m, tiles_n;
   int G, gs, groups;           // conv shape (G rows per block, group size, channels / group size)
@@ -94,6 +102,63 @@ struct ProjArgs {
 struct ProjMaps {
   CUtensorMap a, b, base, d0, scales, biases;
 };
+
+// Stream-K hand-off flags: [CTA][epilogue warp] = 1 once that CTA's partial rows 32 q .. 32 q + 31
+// of its first tile are in its slot. The owner resets each flag after reading, so every launch
+// starts (and ends) with all flags 0; a CTA also clears its own flags when it starts. Calls that
+// overlap on the GPU would share them: keep projections of one device on one stream.
+constexpr int kSkMaxCtas = 1024;
+__device__ int g_sk_flags[kSkMaxCtas][4];
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits (bounded) until a stream-K flag is raised; false on timeout or abort.
+__device__ __forceinline__ bool sk_wait(const int* flag, const volatile int* abort_flag) {
+  if (ld_acquire_gpu(flag) != 0) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(flag) != 0) return true;
+    if ((i & 15u) == 0u) {
+      if (*abort_flag != 0) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+// One piece of this CTA's work: tile t, k-blocks [kb0, kb1), split-K range ks.
+struct PSeg {
+  int t, kb0, kb1, ks;
+};
+// Piece `idx` (0, 1, ...) of this CTA: split-K items (tile it % n_tiles, K range it / n_tiles) or the
+// idx-th tile touched by the CTA's stream-K share; false past the last.
+__device__ __forceinline__ bool p_seg(const ProjArgs& a, int k_stages, int n_tiles, int idx, PSeg& g) {
+  if (!a.stream_k) {
+    const int it = static_cast<int>(blockIdx.x) + idx * static_cast<int>(gridDim.x);
+    if (it >= n_tiles * a.k_splits) return false;
+    g.t = it % n_tiles;
+    g.ks = it / n_tiles;
+    g.kb0 = k_stages * g.ks / a.k_splits;
+    g.kb1 = k_stages * (g.ks + 1) / a.k_splits;
+    return true;
+  }
+  const long long total = static_cast<long long>(n_tiles) * k_stages;
+  const long long s0 = total * blockIdx.x / gridDim.x, e0 = total * (blockIdx.x + 1) / gridDim.x;
+  const long long s = idx == 0 ? s0 : (s0 / k_stages + idx) * k_stages;
+  if (s >= e0) return false;
+  g.t = static_cast<int>(s / k_stages);
+  g.kb0 = static_cast<int>(s - static_cast<long long>(g.t) * k_stages);
+  g.kb1 = static_cast<int>(min(static_cast<long long>(k_stages), e0 - static_cast<long long>(g.t) * k_stages));
+  g.ks = 0;
+  return true;
+}
 
 __device__ __forceinline__ void p_abort(volatile int* abort_flag, int* err) {
   *abort_flag = 1;
@@ -163,7 +228,6 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int k_stages = a.K / kPK;
   const int n_tiles = a.tiles_m * a.tiles_n;
-  const int n_items = n_tiles * a.k_splits;  // work item i: tile i % n_tiles, K range i / n_tiles
   const int gpc = AM ? kPK / 16 : 1;  // groups per stage (conv side 0 over K, group size 16)
 
   if (threadIdx.x == 0) {
@@ -200,6 +264,7 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_trigger();
   pdl_wait();
+  if (a.stream_k && threadIdx.x < 4) g_sk_flags[blockIdx.x][threadIdx.x] = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -211,11 +276,11 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-        const int t = it % n_tiles, ks = it / n_tiles;
-        const int m0 = (t % a.tiles_m) * kPM;
-        const int n0 = (t / a.tiles_m) * NT;
-        for (int kb = k_stages * ks / a.k_splits; kb < k_stages * (ks + 1) / a.k_splits; ++kb) {
+      PSeg g;
+      for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, idx, g); ++idx) {
+        const int m0 = (g.t % a.tiles_m) * kPM;
+        const int n0 = (g.t / a.tiles_m) * NT;
+        for (int kb = g.kb0; kb < g.kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
@@ -266,9 +331,9 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
       uint32_t phase = 0;
       bool ok = true, any = false;
       const uint32_t idesc = make_idesc(false, kPM, NT);
-      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++tile_i) {
-        const int ks = it / n_tiles;
-        const int kb0 = k_stages * ks / a.k_splits, kb1 = k_stages * (ks + 1) / a.k_splits;
+      PSeg g;
+      for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, idx, g); ++idx, ++tile_i) {
+        const int kb0 = g.kb0, kb1 = g.kb1;
         const int ab = tile_i & 1;
         const uint32_t acc_par = static_cast<uint32_t>(tile_i >> 1) & 1u;
         if (!mbar_wait_bounded(smem_u32(&acc_empty[ab]), acc_par ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -313,8 +378,20 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lanes 32q .. 32q + 31
     int tile_i = 0;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++tile_i) {
-      const int t = it % n_tiles, ks = it / n_tiles;
+    PSeg g;
+    for (int idx = 0; p_seg(a, k_stages, n_tiles, idx, g); ++idx, ++tile_i) {
+      const int t = g.t, ks = g.ks;
+      // stream-K: a later piece of its tile (the partial goes to this CTA's slot), or the owner of a
+      // tile whose last k-blocks the CTAs [c_first, c_end) hold
+      // (the plan never gives the conv epilogue stream-K shares: that code is compiled out there)
+      const bool sk_part = !EM && a.stream_k && g.kb0 > 0;
+      const int c_first = static_cast<int>(blockIdx.x) + 1;
+      int c_end = c_first;
+      if (!EM && a.stream_k && g.kb0 == 0 && g.kb1 < k_stages) {
+        const long long total = static_cast<long long>(n_tiles) * k_stages;
+        const long long tile_end = static_cast<long long>(t + 1) * k_stages;
+        while (c_end < static_cast<int>(gridDim.x) && total * c_end / gridDim.x < tile_end) ++c_end;
+      }
       const int m0 = (t % a.tiles_m) * kPM;
       const int n0 = (t / a.tiles_m) * NT;
       const int row = m0 + q * 32 + lane;
@@ -329,6 +406,19 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
         break;
       }
       tc_fence_after();
+      if (c_end > c_first) {
+        // the later pieces of this quarter's rows (lane 0 acquires; the warp barrier orders the
+        // other lanes' loads after it, and those loads bypass L1)
+        int got = 1;
+        if (lane == 0)
+          for (int c2 = c_first; got && c2 < c_end; ++c2) got = sk_wait(&g_sk_flags[c2][q], abort_flag) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        __syncwarp();
+        if (!got) {
+          if (lane == 0) p_abort(abort_flag, a.err);
+          break;
+        }
+      }
       for (int cc = 0; cc < NT / 32; ++cc) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ab * NT + cc * 32),
@@ -343,6 +433,25 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
         float y[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(r[j]);
+        if (sk_part) {
+          // this CTA's k-blocks of a tile another CTA owns: raw partial sums to its slot
+          float* dst = a.part + (static_cast<size_t>(blockIdx.x) * kPM + q * 32 + lane) * NT + cc * 32;
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<float4*>(dst + 4 * v) = make_float4(y[4 * v], y[4 * v + 1], y[4 * v + 2], y[4 * v + 3]);
+          continue;
+        }
+        for (int c2 = c_first; c2 < c_end; ++c2) {  // the later k-blocks' partial sums, in K order
+          const float* src = a.part + (static_cast<size_t>(c2) * kPM + q * 32 + lane) * NT + cc * 32;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const float4 u = __ldcg(reinterpret_cast<const float4*>(src + 4 * v));
+            y[4 * v] += u.x;
+            y[4 * v + 1] += u.y;
+            y[4 * v + 2] += u.z;
+            y[4 * v + 3] += u.w;
+          }
+        }
         if (a.k_splits > 1) {
           // a K range's partial sums; the reduce pass adds them and applies the epilogue
           if (valid) {
@@ -401,6 +510,13 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
+      if (sk_part) {
+        __threadfence();  // every lane's partial rows are visible before the flag
+        __syncwarp();
+        if (lane == 0) st_release_gpu(&g_sk_flags[blockIdx.x][q], 1);
+      }
+      if (c_end > c_first && lane == 0)
+        for (int c2 = c_first; c2 < c_end; ++c2) g_sk_flags[c2][q] = 0;  // read: ready for the next launch
     }
   } else if (AM && warp < 6 + C::kConvWarps) {
     // ------------------------------------------------------------------ conv side-0 producer
@@ -420,12 +536,12 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      const int t = it % n_tiles, ks = it / n_tiles;
-      const int m0 = (t % a.tiles_m) * kPM;
+    PSeg g;
+    for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, idx, g); ++idx) {
+      const int m0 = (g.t % a.tiles_m) * kPM;
       const int row_first = m0 + r_first;
       const int t_first = row_first % a.G;
-      for (int kb = k_stages * ks / a.k_splits; kb < k_stages * (ks + 1) / a.k_splits; ++kb) {
+      for (int kb = g.kb0; kb < g.kb1; ++kb) {
         if (!mbar_wait_bounded_suspend(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs, 200)) {
           ok = false;
           break;
@@ -504,9 +620,9 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     uint32_t phase = 0;
     bool ok = true;
     const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      const int t = it % n_tiles, ks = it / n_tiles;
-      for (int kb = k_stages * ks / a.k_splits; kb < k_stages * (ks + 1) / a.k_splits; ++kb) {
+    PSeg g;
+    for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, idx, g); ++idx) {
+      for (int kb = g.kb0; kb < g.kb1; ++kb) {
         if (!mbar_wait_bounded_suspend(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs, 200)) {
           ok = false;
           break;
@@ -635,7 +751,7 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 template <int AM, int BM, int EM, int NT>
-static int launch_proj_t(const ProjSpec& p, int k_splits, cudaStream_t st) {
+static int launch_proj_t(const ProjSpec& p, int k_splits, int sk_ctas, cudaStream_t st) {
   using C = PCfg<AM, BM, EM, NT>;
   static_assert(C::kStages >= 2, "at least two pipeline stages");
   ProjMaps maps;
@@ -678,6 +794,7 @@ static int launch_proj_t(const ProjSpec& p, int k_splits, cudaStream_t st) {
   args.N = p.N;
   args.K = p.K;
   args.k_splits = k_splits;
+  args.stream_k = sk_ctas > 0 ? 1 : 0;
   args.part = p.part;
   args.a_rows = a_rows;
   args.tiles_m = (p.M + kPM - 1) / kPM;
@@ -691,7 +808,7 @@ static int launch_proj_t(const ProjSpec& p, int k_splits, cudaStream_t st) {
   args.out = static_cast<__nv_bfloat16*>(p.out);
   args.err = device_error_word();
   const int items = args.tiles_m * args.tiles_n * k_splits;
-  const int grid = std::min(items, sm_count());
+  const int grid = sk_ctas > 0 ? sk_ctas : std::min(items, sm_count());
   static unsigned done = 0;
   auto kern = proj_kernel<AM, BM, EM, NT>;
   if (!ensure_smem_attr(kern, C::kSmem, &done))
@@ -711,26 +828,33 @@ static int launch_proj_t(const ProjSpec& p, int k_splits, cudaStream_t st) {
 // (the weight-streaming case) the K range is split so that about every SM streams a share of the
 // weights through 256-column MMAs, the partial sums going through a workspace and a reduce pass;
 // when K is too short to split, 64-column tiles spread the columns instead.
-ProjPlan proj_plan(int M, int N, int K, int sms) {
+ProjPlan proj_plan(int M, int N, int K, int sms, bool epilogue_conv) {
   const long long tiles256 = static_cast<long long>((M + kPM - 1) / kPM) * ((N + 255) / 256);
   const int k_stages = K / kPK;
-  if (2 * tiles256 >= sms) return ProjPlan{256, 1};
+  if (2 * tiles256 >= sms) {
+    // stream-K: every SM gets the same number of k-blocks. Not with side 1 + residual in the
+    // epilogue: every stream-K share ends in an owner epilogue that nothing overlaps, and the
+    // conv epilogue's loads made that variant slower (103 against 93 us at 1024 x 5120 x 5120).
+    if (epilogue_conv) return ProjPlan{256, 1, 0};
+    return ProjPlan{256, 1, static_cast<int>(std::min<long long>(std::min(sms, kSkMaxCtas), tiles256 * k_stages))};
+  }
   const int ks = static_cast<int>(std::min<long long>(sms / std::max<long long>(tiles256, 1), k_stages / 4));
-  if (ks >= 2) return ProjPlan{256, ks};
-  return ProjPlan{64, 1};
+  if (ks >= 2) return ProjPlan{256, ks, 0};
+  return ProjPlan{64, 1, 0};
 }
 
 size_t proj_workspace(int M, int N, int K, int sms) {
   if (proj_small_eligible(M, N, K)) return 0;  // the small-row kernel reduces in shared memory
-  const ProjPlan pl = proj_plan(M, N, K, sms);
+  const ProjPlan pl = proj_plan(M, N, K, sms, false);  // the largest workspace of the variants
+  if (pl.ctas > 0) return static_cast<size_t>(pl.ctas) * kPM * 256 * sizeof(float);  // one partial tile per CTA
   return pl.k_splits > 1 ? static_cast<size_t>(pl.k_splits) * M * N * sizeof(float) : 0;
 }
 
 template <int AM, int BM, int EM>
 static int launch_proj_nt(const ProjSpec& p, cudaStream_t st) {
-  const ProjPlan pl = proj_plan(p.M, p.N, p.K, sm_count());
-  if (pl.nt == 64) return launch_proj_t<AM, BM, EM, 64>(p, 1, st);
-  return launch_proj_t<AM, BM, EM, 256>(p, pl.k_splits, st);
+  const ProjPlan pl = proj_plan(p.M, p.N, p.K, sm_count(), EM != 0);
+  if (pl.nt == 64) return launch_proj_t<AM, BM, EM, 64>(p, 1, 0, st);
+  return launch_proj_t<AM, BM, EM, 256>(p, pl.k_splits, pl.ctas, st);
 }
 
 int launch_proj(const ProjSpec& p, cudaStream_t st) {

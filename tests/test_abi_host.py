@@ -224,10 +224,11 @@ def test_ragged_entry_points_reject_bad_arguments(lib):
 
 def test_projection_workspace_query(lib):
     """Up to 128 rows the projections reduce their K splits in shared memory and need no
-    workspace; a few more rows than one 128-row tile split K through the workspace instead (the
-    query is host-only and needs no device)."""
+    workspace; a few more rows than one 128-row tile split K through the workspace instead, and
+    with at least half as many 256-column tiles as SMs the stream-K shares need one 128 x 256 fp32
+    partial tile per CTA (the query is host-only and needs no device: 148 SMs are assumed)."""
     lib.dflash2_proj_workspace_bytes.restype = ctypes.c_size_t
     assert lib.dflash2_proj_workspace_bytes(1, 5120, 5120) == 0
     assert lib.dflash2_proj_workspace_bytes(128, 5120, 5120) == 0
-    assert lib.dflash2_proj_workspace_bytes(129, 5120, 5120) > 0
-    assert lib.dflash2_proj_workspace_bytes(1024, 5120, 5120) == 0  # enough tiles: no split
+    assert lib.dflash2_proj_workspace_bytes(129, 5120, 5120) == 3 * 129 * 5120 * 4  # 40 tiles: 3 K ranges
+    assert lib.dflash2_proj_workspace_bytes(1024, 5120, 5120) == 148 * 128 * 256 * 4

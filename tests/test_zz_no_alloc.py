@@ -57,3 +57,39 @@ def test_noalloc_rejects_sizes_beyond_its_array():
                                        None)
     assert rc == -1
     assert b"allocation-free" in lib.dflash2_last_error_message()
+
+
+def test_noalloc_replayed_from_a_cuda_graph():
+    """The documented use: one warm call, then the call captured in a CUDA graph with every output
+    preallocated, and the graph replayed after new inputs are copied into the captured buffers."""
+    torch = require_gpu()
+    import dflash2_block_drafter_gb300 as d
+    from dflash2_block_drafter_gb300.tail import to_device
+    first = I.selector_case(303, B=8, G=16, H=512, V=4000, K=16, R=64, bias=True)
+    second = I.selector_case(304, B=8, G=16, H=512, V=4000, K=16, R=64, bias=True)
+    H, K, R = first.H, first.K, first.R
+    h = to_device(first.h).reshape(-1, H).clone()
+    w = to_device(first.w_head).clone()
+    wp = to_device(first.w_proj).clone()
+    bias = to_device(first.bias).clone()
+    M = h.shape[0]
+    cand = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    unary = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    z = torch.empty((M, R), dtype=torch.float32, device="cuda")
+    d.dflash2_head_topk_noalloc(h, w, K, bias=bias, w_proj=wp, cand=cand, unary=unary, z=z)
+    torch.cuda.synchronize()
+    assert d.dflash2_poll_error() == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        d.dflash2_head_topk_noalloc(h, w, K, bias=bias, w_proj=wp, cand=cand, unary=unary, z=z)
+    h.copy_(to_device(second.h).reshape(-1, H))
+    w.copy_(to_device(second.w_head))
+    wp.copy_(to_device(second.w_proj))
+    bias.copy_(to_device(second.bias))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert d.dflash2_poll_error() == 0
+    rc, ru, rz, _ = d.dflash2_head_topk(h, w, K, bias=bias, w_proj=wp)
+    np.testing.assert_array_equal(cand.cpu().numpy(), rc.cpu().numpy())
+    assert_close_scaled(unary.cpu().numpy(), ru.cpu().numpy(), what="unary (graph replay)")
+    assert_close_scaled(z.cpu().numpy(), rz.cpu().numpy(), what="z (graph replay)")
