@@ -165,8 +165,9 @@ struct ProjPlan {
   int nt;        // columns per tile (64 or 256)
   int k_splits;  // K ranges summed by a reduce pass (1: none)
   int ctas;      // > 0: stream-K over this many CTAs (equal shares of the tiles' k-blocks)
+  int pair;      // 1: CTA pairs (cta_group::2) over 256-row tiles; the stream-K units are the pairs
 };
-ProjPlan proj_plan(int M, int N, int K, int sms, bool epilogue_conv);
+ProjPlan proj_plan(int M, int N, int K, int sms, bool epilogue_conv, bool producers);
 // At most 128 rows: the weight rows on the MMA's 128-row side, K split over a cluster and reduced in
 // shared memory, no workspace (proj_small.cu).
 bool proj_small_eligible(int M, int N, int K);

@@ -70,13 +70,18 @@ struct PLayout {
   static constexpr int kStageBytes = kAOp + kBOp + kARaw + kBRaw;
 };
 
-template <int AM, int BM, int EM, int NT>
+// P = 1: CTA pairs (cta_group::2) over 256 x NT tiles; each CTA of the pair stages its own 128 rows
+// of A and half of the tile's weight rows (kBRows), so a k-block brings it a third fewer bytes. Only
+// the plain projection (no producer warps, no conv epilogue) runs in pairs.
+template <int AM, int BM, int EM, int NT, int P>
 struct PCfg {
   static constexpr int kConvWarps = AM ? 8 : 0;
   static constexpr int kDeqWarps = BM ? 8 : 0;
   static constexpr int kProdWarps = kConvWarps + kDeqWarps;
   static constexpr int kThreads = 64 + 128 + 32 * kProdWarps;
-  static constexpr int kStageBytes = PLayout<AM, BM, NT>::kStageBytes;
+  static constexpr int kBRows = P ? NT / 2 : NT;  // weight rows this CTA stages per k-block
+  static constexpr int kTileM = P ? 2 * kPM : kPM;
+  static constexpr int kStageBytes = PLayout<AM, BM, kBRows>::kStageBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kFit = (kPSmemLimit - 1024 - kBarBytes) / kStageBytes;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
@@ -108,6 +113,10 @@ struct ProjMaps {
 // starts (and ends) with all flags 0; a CTA also clears its own flags when it starts. Calls that
 // overlap on the GPU would share them: keep projections of one device on one stream.
 constexpr int kSkMaxCtas = 1024;
+#ifndef DFL_PROJ_PAIR
+#define DFL_PROJ_PAIR 1
+#endif
+
 __device__ int g_sk_flags[kSkMaxCtas][4];
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
@@ -137,11 +146,13 @@ __device__ __forceinline__ bool sk_wait(const int* flag, const volatile int* abo
 struct PSeg {
   int t, kb0, kb1, ks;
 };
-// Piece `idx` (0, 1, ...) of this CTA: split-K items (tile it % n_tiles, K range it / n_tiles) or the
-// idx-th tile touched by the CTA's stream-K share; false past the last.
-__device__ __forceinline__ bool p_seg(const ProjArgs& a, int k_stages, int n_tiles, int idx, PSeg& g) {
+// Piece `idx` (0, 1, ...) of work unit `unit` (a CTA, or a CTA pair) of `units`: split-K items (tile
+// it % n_tiles, K range it / n_tiles) or the idx-th tile touched by the unit's stream-K share; false
+// past the last.
+__device__ __forceinline__ bool p_seg(const ProjArgs& a, int k_stages, int n_tiles, int unit, int units, int idx,
+                                      PSeg& g) {
   if (!a.stream_k) {
-    const int it = static_cast<int>(blockIdx.x) + idx * static_cast<int>(gridDim.x);
+    const int it = unit + idx * units;
     if (it >= n_tiles * a.k_splits) return false;
     g.t = it % n_tiles;
     g.ks = it / n_tiles;
@@ -150,7 +161,7 @@ __device__ __forceinline__ bool p_seg(const ProjArgs& a, int k_stages, int n_til
     return true;
   }
   const long long total = static_cast<long long>(n_tiles) * k_stages;
-  const long long s0 = total * blockIdx.x / gridDim.x, e0 = total * (blockIdx.x + 1) / gridDim.x;
+  const long long s0 = total * unit / units, e0 = total * (unit + 1) / units;
   const long long s = idx == 0 ? s0 : (s0 / k_stages + idx) * k_stages;
   if (s >= e0) return false;
   g.t = static_cast<int>(s / k_stages);
@@ -207,11 +218,11 @@ __device__ __forceinline__ void load_epi_chunk(EpiChunk& e, const ProjArgs& a, b
                                       : 0.f;
 }
 
-template <int AM, int BM, int EM, int NT>
-__global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
+template <int AM, int BM, int EM, int NT, int P>
+__global__ void __launch_bounds__(PCfg<AM, BM, EM, NT, P>::kThreads, 1)
     proj_kernel(const __grid_constant__ ProjMaps maps, const ProjArgs a) {
-  using C = PCfg<AM, BM, EM, NT>;
-  using L = PLayout<AM, BM, NT>;
+  using C = PCfg<AM, BM, EM, NT, P>;
+  using L = PLayout<AM, BM, C::kBRows>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* bar_area = smem + C::kStages * C::kStageBytes;
@@ -229,6 +240,14 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
   const int k_stages = a.K / kPK;
   const int n_tiles = a.tiles_m * a.tiles_n;
   const int gpc = AM ? kPK / 16 : 1;  // groups per stage (conv side 0 over K, group size 16)
+  // Pairs (the plain projection only): rank 0 (the leader) issues the MMAs for both CTAs, both CTAs'
+  // TMA loads complete on the leader's full barrier (cta_group::2 copies; the leader expects both
+  // halves' bytes), and the leader's acc_empty counts both CTAs' epilogue warps.
+  static_assert(!P || (C::kProdWarps == 0 && !EM), "CTA pairs only for the plain projection");
+  const uint32_t rank = P ? cluster_ctarank() : 0u;
+  constexpr bool kLeaderFull = P != 0;
+  const int unit = P ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = P ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -238,7 +257,7 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
-      mbar_init(smem_u32(&acc_empty[b]), 4);
+      mbar_init(smem_u32(&acc_empty[b]), P ? 8 : 4);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -255,11 +274,19 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
-    tmem_relinquish();
+    if (P) {
+      tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (P)
+    cluster_sync_all();  // both CTAs' barriers exist before the peer arrives on the leader's
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_trigger();
@@ -271,15 +298,16 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_a = policy_evict_last();   // activations: re-read by every column tile
       const uint64_t pol_w = policy_evict_normal(); // weights: shared by the CTAs of one column tile
-      const uint32_t bytes = static_cast<uint32_t>(a.a_rows * 128 + (BM ? NT * 32 + NT * 4 : NT * 128) +
+      constexpr int kB = C::kBRows;
+      const uint32_t bytes = static_cast<uint32_t>(a.a_rows * 128 + (BM ? kB * 32 + kB * 4 : kB * 128) +
                                                    (AM ? 2 * kPK * 4 + a.a_rows * 2 * gpc * 4 : 0));
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
       PSeg g;
-      for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, idx, g); ++idx) {
-        const int m0 = (g.t % a.tiles_m) * kPM;
-        const int n0 = (g.t / a.tiles_m) * NT;
+      for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, unit, units, idx, g); ++idx) {
+        const int m0 = (g.t % a.tiles_m) * C::kTileM + static_cast<int>(rank) * kPM;  // this CTA's rows
+        const int n0 = (g.t / a.tiles_m) * NT + static_cast<int>(rank) * C::kBRows;  // its weight rows
         for (int kb = g.kb0; kb < g.kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
@@ -287,6 +315,19 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
           }
           const uint32_t fb = smem_u32(&full[stage]);
           uint8_t* st = smem + stage * C::kStageBytes;
+          if (kLeaderFull) {
+            // both CTAs' operands complete on the leader's barrier, which counts both halves' bytes
+            const uint32_t fbl = mapa_shared(fb, 0);
+            if (rank == 0) mbar_arrive_expect_tx(fb, 2 * bytes);
+            tma_load_2d_pair(smem_u32(st), &maps.a, fbl, kb * kPK, m0, pol_a);
+            tma_load_2d_pair(smem_u32(st + kAOp), &maps.b, fbl, kb * kPK, n0, pol_w);
+            ++issued;
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(fb, bytes);
           tma_load_2d(smem_u32(st), &maps.a, fb, kb * kPK, m0, pol_a);
           if (AM) {
@@ -307,7 +348,13 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
           }
         }
       }
-      if (!ok) {
+      if (!ok && kLeaderFull && rank != 0) {
+        // this CTA's copies complete on the leader's barriers: give them a fixed bounded time
+        p_abort(abort_flag, a.err);
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
+        }
+      } else if (!ok) {
         p_abort(abort_flag, a.err);
         int s = stage;
         uint32_t ph = phase;
@@ -326,13 +373,13 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int stage = 0, tile_i = 0;
       uint32_t phase = 0;
       bool ok = true, any = false;
-      const uint32_t idesc = make_idesc(false, kPM, NT);
+      const uint32_t idesc = make_idesc(false, C::kTileM, NT);
       PSeg g;
-      for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, idx, g); ++idx, ++tile_i) {
+      for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, unit, units, idx, g); ++idx, ++tile_i) {
         const int kb0 = g.kb0, kb1 = g.kb1;
         const int ab = tile_i & 1;
         const uint32_t acc_par = static_cast<uint32_t>(tile_i >> 1) & 1u;
@@ -343,7 +390,8 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
         tc_fence_after();
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs) ||
-              (C::kProdWarps > 0 && !mbar_wait_bounded(smem_u32(&ready[stage]), phase, abort_flag, kWaitLimitNs))) {
+              (C::kProdWarps > 0 &&
+               !mbar_wait_bounded(smem_u32(&ready[stage]), phase, abort_flag, kWaitLimitNs))) {
             ok = false;
             break;
           }
@@ -352,10 +400,18 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
           const uint64_t adesc = desc_kmajor_swizzled<128>(sa);
           const uint64_t bdesc = desc_kmajor_swizzled<128>(sa + kAOp);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)  // 16-element (32-byte) steps along the swizzled row
-            mma_f16(tmem_base + static_cast<uint32_t>(ab * NT), adesc + static_cast<uint64_t>(2 * k),
-                    bdesc + static_cast<uint64_t>(2 * k), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&empty[stage]));
+          for (int k = 0; k < 4; ++k) {  // 16-element (32-byte) steps along the swizzled row
+            if (P)
+              mma_f16_pair(tmem_base + static_cast<uint32_t>(ab * NT), adesc + static_cast<uint64_t>(2 * k),
+                           bdesc + static_cast<uint64_t>(2 * k), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            else
+              mma_f16(tmem_base + static_cast<uint32_t>(ab * NT), adesc + static_cast<uint64_t>(2 * k),
+                      bdesc + static_cast<uint64_t>(2 * k), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          if (P)
+            mma_commit_pair(smem_u32(&empty[stage]), 0x3);  // frees the stage in both CTAs
+          else
+            mma_commit(smem_u32(&empty[stage]));
           any = true;
           if (++stage == C::kStages) {
             stage = 0;
@@ -363,12 +419,18 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(smem_u32(&acc_full[ab]));
+        if (P)
+          mma_commit_pair(smem_u32(&acc_full[ab]), 0x3);  // the accumulator is complete in both CTAs
+        else
+          mma_commit(smem_u32(&acc_full[ab]));
       }
       if (!ok) {
         p_abort(abort_flag, a.err);
         if (any) {
-          mma_commit(smem_u32(drain));
+          if (P)
+            mma_commit_pair(smem_u32(drain), 0x1);
+          else
+            mma_commit(smem_u32(drain));
           mbar_wait_bounded(smem_u32(drain), 0, nullptr, kPDrainNs);
         }
       }
@@ -379,20 +441,21 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     const int q = warp & 3;  // TMEM lanes 32q .. 32q + 31
     int tile_i = 0;
     PSeg g;
-    for (int idx = 0; p_seg(a, k_stages, n_tiles, idx, g); ++idx, ++tile_i) {
+    for (int idx = 0; p_seg(a, k_stages, n_tiles, unit, units, idx, g); ++idx, ++tile_i) {
       const int t = g.t, ks = g.ks;
       // stream-K: a later piece of its tile (the partial goes to this CTA's slot), or the owner of a
       // tile whose last k-blocks the CTAs [c_first, c_end) hold
       // (the plan never gives the conv epilogue stream-K shares: that code is compiled out there)
+      // (units: CTAs, or pairs whose CTAs of the same rank hand rows over)
       const bool sk_part = !EM && a.stream_k && g.kb0 > 0;
-      const int c_first = static_cast<int>(blockIdx.x) + 1;
+      const int c_first = unit + 1;
       int c_end = c_first;
       if (!EM && a.stream_k && g.kb0 == 0 && g.kb1 < k_stages) {
         const long long total = static_cast<long long>(n_tiles) * k_stages;
         const long long tile_end = static_cast<long long>(t + 1) * k_stages;
-        while (c_end < static_cast<int>(gridDim.x) && total * c_end / gridDim.x < tile_end) ++c_end;
+        while (c_end < units && total * c_end / units < tile_end) ++c_end;
       }
-      const int m0 = (t % a.tiles_m) * kPM;
+      const int m0 = (t % a.tiles_m) * C::kTileM + static_cast<int>(rank) * kPM;
       const int n0 = (t / a.tiles_m) * NT;
       const int row = m0 + q * 32 + lane;
       const bool valid = row < a.M;
@@ -411,7 +474,8 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
         // other lanes' loads after it, and those loads bypass L1)
         int got = 1;
         if (lane == 0)
-          for (int c2 = c_first; got && c2 < c_end; ++c2) got = sk_wait(&g_sk_flags[c2][q], abort_flag) ? 1 : 0;
+          for (int c2 = c_first; got && c2 < c_end; ++c2)
+            got = sk_wait(&g_sk_flags[P ? 2 * c2 + static_cast<int>(rank) : c2][q], abort_flag) ? 1 : 0;
         got = __shfl_sync(0xffffffffu, got, 0);
         __syncwarp();
         if (!got) {
@@ -442,7 +506,8 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
           continue;
         }
         for (int c2 = c_first; c2 < c_end; ++c2) {  // the later k-blocks' partial sums, in K order
-          const float* src = a.part + (static_cast<size_t>(c2) * kPM + q * 32 + lane) * NT + cc * 32;
+          const int cta2 = P ? 2 * c2 + static_cast<int>(rank) : c2;
+          const float* src = a.part + (static_cast<size_t>(cta2) * kPM + q * 32 + lane) * NT + cc * 32;
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
             const float4 u = __ldcg(reinterpret_cast<const float4*>(src + 4 * v));
@@ -509,14 +574,19 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
+      if (lane == 0) {
+        if (P)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[ab]), 0));  // the leader's
+        else
+          mbar_arrive(smem_u32(&acc_empty[ab]));
+      }
       if (sk_part) {
         __threadfence();  // every lane's partial rows are visible before the flag
         __syncwarp();
         if (lane == 0) st_release_gpu(&g_sk_flags[blockIdx.x][q], 1);
       }
-      if (c_end > c_first && lane == 0)
-        for (int c2 = c_first; c2 < c_end; ++c2) g_sk_flags[c2][q] = 0;  // read: ready for the next launch
+      if (c_end > c_first && lane == 0)  // read: ready for the next launch
+        for (int c2 = c_first; c2 < c_end; ++c2) g_sk_flags[P ? 2 * c2 + static_cast<int>(rank) : c2][q] = 0;
     }
   } else if (AM && warp < 6 + C::kConvWarps) {
     // ------------------------------------------------------------------ conv side-0 producer
@@ -537,8 +607,8 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     uint32_t phase = 0;
     bool ok = true;
     PSeg g;
-    for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, idx, g); ++idx) {
-      const int m0 = (g.t % a.tiles_m) * kPM;
+    for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, unit, units, idx, g); ++idx) {
+      const int m0 = (g.t % a.tiles_m) * C::kTileM + static_cast<int>(rank) * kPM;
       const int row_first = m0 + r_first;
       const int t_first = row_first % a.G;
       for (int kb = g.kb0; kb < g.kb1; ++kb) {
@@ -621,7 +691,7 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
     bool ok = true;
     const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
     PSeg g;
-    for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, idx, g); ++idx) {
+    for (int idx = 0; ok && p_seg(a, k_stages, n_tiles, unit, units, idx, g); ++idx) {
       for (int kb = g.kb0; kb < g.kb1; ++kb) {
         if (!mbar_wait_bounded_suspend(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs, 200)) {
           ok = false;
@@ -632,7 +702,7 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
         const __nv_bfloat16* sc = reinterpret_cast<const __nv_bfloat16*>(st + L::kOffScale);
         const __nv_bfloat16* bi = reinterpret_cast<const __nv_bfloat16*>(st + L::kOffBias);
 #pragma unroll
-        for (int i = 0; i < NT / 32; ++i) {
+        for (int i = 0; i < C::kBRows / 32; ++i) {
           const int job = pt + 256 * i;
           const int rr = job >> 3;
           const int c = job & 7;
@@ -664,10 +734,18 @@ __global__ void __launch_bounds__(PCfg<AM, BM, EM, NT>::kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+  if (P) {
+    cluster_sync_all();  // no MMA, commit or remote arrival is in flight towards either CTA
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    }
+  } else {
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, C::kTmemCols);
+    }
   }
 }
 
@@ -750,9 +828,29 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-template <int AM, int BM, int EM, int NT>
+// CTA pairs of the projection kernel variant that the current device holds at once (0: unknown).
+template <typename K>
+int proj_pair_capacity(K* kern, int threads, int smem) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  (void)cudaGetLastError();
+  return n;
+}
+
+template <int AM, int BM, int EM, int NT, int P>
 static int launch_proj_t(const ProjSpec& p, int k_splits, int sk_ctas, cudaStream_t st) {
-  using C = PCfg<AM, BM, EM, NT>;
+  using C = PCfg<AM, BM, EM, NT, P>;
   static_assert(C::kStages >= 2, "at least two pipeline stages");
   ProjMaps maps;
   const int a_rows = std::min(kPM, (p.M + 15) / 16 * 16);  // a small M loads only its own rows
@@ -761,19 +859,19 @@ static int launch_proj_t(const ProjSpec& p, int k_splits, int sk_ctas, cudaStrea
     return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (projection A)");
   maps.b = maps.base = maps.d0 = maps.scales = maps.biases = maps.a;
   if (BM) {
-    // packed codes [N][K / 8] 32-bit words: a box of 8 words (64 codes) x NT rows; scales and
-    // biases [K / 64][N] bf16: a box of NT values of one group
+    // packed codes [N][K / 8] 32-bit words: a box of 8 words (64 codes) x the CTA's weight rows;
+    // scales and biases [K / 64][N] bf16: a box of those rows' values of one group
     const uint64_t dims[2] = {static_cast<uint64_t>(p.K / 8), static_cast<uint64_t>(p.N)};
     const uint64_t strides[1] = {static_cast<uint64_t>(p.K / 8) * 4};
-    const uint32_t box[2] = {8, static_cast<uint32_t>(NT)};
+    const uint32_t box[2] = {8, static_cast<uint32_t>(C::kBRows)};
     const uint64_t sdims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K / kQGroup)};
     const uint64_t sstr[1] = {static_cast<uint64_t>(p.N) * 2};
-    const uint32_t sbox[2] = {static_cast<uint32_t>(NT), 1};
+    const uint32_t sbox[2] = {static_cast<uint32_t>(C::kBRows), 1};
     if (!make_tmap_plain(&maps.b, p.w, DFLASH2_F32, 2, dims, strides, box) ||
         !make_tmap_plain(&maps.scales, p.scales, DFLASH2_BF16, 2, sdims, sstr, sbox) ||
         !make_tmap_plain(&maps.biases, p.qbias, DFLASH2_BF16, 2, sdims, sstr, sbox))
       return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (4-bit weights)");
-  } else if (!make_tmap_sw128(&maps.b, p.w, static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K), NT)) {
+  } else if (!make_tmap_sw128(&maps.b, p.w, static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K), C::kBRows)) {
     return fail(DFLASH2_ERR_CUDA, "tensor map encode failed (projection W)");
   }
   if (AM) {
@@ -797,7 +895,7 @@ static int launch_proj_t(const ProjSpec& p, int k_splits, int sk_ctas, cudaStrea
   args.stream_k = sk_ctas > 0 ? 1 : 0;
   args.part = p.part;
   args.a_rows = a_rows;
-  args.tiles_m = (p.M + kPM - 1) / kPM;
+  args.tiles_m = (p.M + C::kTileM - 1) / C::kTileM;
   args.tiles_n = (p.N + NT - 1) / NT;
   args.G = p.G > 0 ? p.G : 1;
   args.gs = p.gs > 0 ? p.gs : 8;
@@ -808,12 +906,24 @@ static int launch_proj_t(const ProjSpec& p, int k_splits, int sk_ctas, cudaStrea
   args.out = static_cast<__nv_bfloat16*>(p.out);
   args.err = device_error_word();
   const int items = args.tiles_m * args.tiles_n * k_splits;
-  const int grid = sk_ctas > 0 ? sk_ctas : std::min(items, sm_count());
+  int grid = sk_ctas > 0 ? sk_ctas : std::min(items, sm_count());
   static unsigned done = 0;
-  auto kern = proj_kernel<AM, BM, EM, NT>;
+  auto kern = proj_kernel<AM, BM, EM, NT, P>;
   if (!ensure_smem_attr(kern, C::kSmem, &done))
     return fail(DFLASH2_ERR_CUDA, "cudaFuncSetAttribute failed (projection)");
-  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, st, nullptr, 0, maps, args);
+  cudaLaunchAttribute cl[1];
+  if (P) {
+    // every pair of the stream-K shares is resident at once (an owner waits for later pairs)
+    static int cap = -1;
+    if (cap < 0) cap = proj_pair_capacity(kern, C::kThreads, C::kSmem);
+    if (cap > 0) grid = std::min(grid, 2 * cap);
+    grid &= ~1;
+    cl[0].id = cudaLaunchAttributeClusterDimension;
+    cl[0].val.clusterDim.x = 2;
+    cl[0].val.clusterDim.y = 1;
+    cl[0].val.clusterDim.z = 1;
+  }
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, st, P ? cl : nullptr, P ? 1 : 0, maps, args);
   if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "projection launch failed: %s", cudaGetErrorString(e));
   if (k_splits > 1) {
     const size_t n = static_cast<size_t>(p.M) * (p.N / 8);
@@ -828,33 +938,44 @@ static int launch_proj_t(const ProjSpec& p, int k_splits, int sk_ctas, cudaStrea
 // (the weight-streaming case) the K range is split so that about every SM streams a share of the
 // weights through 256-column MMAs, the partial sums going through a workspace and a reduce pass;
 // when K is too short to split, 64-column tiles spread the columns instead.
-ProjPlan proj_plan(int M, int N, int K, int sms, bool epilogue_conv) {
+ProjPlan proj_plan(int M, int N, int K, int sms, bool epilogue_conv, bool producers) {
   const long long tiles256 = static_cast<long long>((M + kPM - 1) / kPM) * ((N + 255) / 256);
   const int k_stages = K / kPK;
   if (2 * tiles256 >= sms) {
     // stream-K: every SM gets the same number of k-blocks. Not with side 1 + residual in the
     // epilogue: every stream-K share ends in an owner epilogue that nothing overlaps, and the
     // conv epilogue's loads made that variant slower (103 against 93 us at 1024 x 5120 x 5120).
-    if (epilogue_conv) return ProjPlan{256, 1, 0};
-    return ProjPlan{256, 1, static_cast<int>(std::min<long long>(std::min(sms, kSkMaxCtas), tiles256 * k_stages))};
+    if (epilogue_conv) return ProjPlan{256, 1, 0, 0};
+    const int cap = std::min(sms, kSkMaxCtas);
+    // CTA pairs over 256-row tiles (a third fewer operand bytes per MMA) for the plain projection. With
+    // producer warps (side 0 in A, 4-bit dequant) the peer's warps would hand every stage over to the
+    // leader with a remote mbarrier arrival: measured at 1024 x 5120 x 5120 that hand-off per stage
+    // made the pair kernel twice as slow as single CTAs, so those variants keep single CTAs.
+    if (M >= 256 && !producers && DFL_PROJ_PAIR) {
+      const long long ptiles = static_cast<long long>((M + 255) / 256) * ((N + 255) / 256);
+      return ProjPlan{256, 1, 2 * static_cast<int>(std::min<long long>(cap / 2, ptiles * k_stages)), 1};
+    }
+    return ProjPlan{256, 1, static_cast<int>(std::min<long long>(cap, tiles256 * k_stages)), 0};
   }
   const int ks = static_cast<int>(std::min<long long>(sms / std::max<long long>(tiles256, 1), k_stages / 4));
-  if (ks >= 2) return ProjPlan{256, ks, 0};
-  return ProjPlan{64, 1, 0};
+  if (ks >= 2) return ProjPlan{256, ks, 0, 0};
+  return ProjPlan{64, 1, 0, 0};
 }
 
 size_t proj_workspace(int M, int N, int K, int sms) {
   if (proj_small_eligible(M, N, K)) return 0;  // the small-row kernel reduces in shared memory
-  const ProjPlan pl = proj_plan(M, N, K, sms, false);  // the largest workspace of the variants
+  const ProjPlan pl = proj_plan(M, N, K, sms, false, false);  // the largest workspace of the variants
   if (pl.ctas > 0) return static_cast<size_t>(pl.ctas) * kPM * 256 * sizeof(float);  // one partial tile per CTA
   return pl.k_splits > 1 ? static_cast<size_t>(pl.k_splits) * M * N * sizeof(float) : 0;
 }
 
 template <int AM, int BM, int EM>
 static int launch_proj_nt(const ProjSpec& p, cudaStream_t st) {
-  const ProjPlan pl = proj_plan(p.M, p.N, p.K, sm_count(), EM != 0);
-  if (pl.nt == 64) return launch_proj_t<AM, BM, EM, 64>(p, 1, 0, st);
-  return launch_proj_t<AM, BM, EM, 256>(p, pl.k_splits, pl.ctas, st);
+  const ProjPlan pl = proj_plan(p.M, p.N, p.K, sm_count(), EM != 0, AM != 0 || BM != 0);
+  if (pl.nt == 64) return launch_proj_t<AM, BM, EM, 64, 0>(p, 1, 0, st);
+  constexpr int kPairOk = (AM || BM || EM) ? 0 : 1;  // only the plain projection is built in pairs
+  if (kPairOk && pl.pair) return launch_proj_t<AM, BM, EM, 256, kPairOk>(p, 1, pl.ctas, st);
+  return launch_proj_t<AM, BM, EM, 256, 0>(p, pl.k_splits, pl.ctas, st);
 }
 
 int launch_proj(const ProjSpec& p, cudaStream_t st) {
