@@ -303,7 +303,12 @@ DFLASH2_API int dflash2_score_edges_ragged(const int32_t* cand, const float* una
  * workspace may be NULL, when the shape needs none: up to 128 rows the K range is split over the
  * CTAs of a thread-block cluster and reduced in shared memory; above, a shape whose tiles do not
  * fill the SMs splits K over them and the partial sums go through the workspace to a reduce pass
- * that applies the epilogue).
+ * that applies the epilogue; with at least half as many 128 x 256 tiles as SMs every SM takes an
+ * equal stream-K share of the tiles' k-blocks and the workspace holds one 128 x 256 fp32 partial
+ * tile per CTA, handed to the tile's owner through a flag array inside the library). The flags are
+ * per device and process: calls of these three entry points that can run at the same time on one
+ * device (on different streams) must not overlap; keep them on one stream. The contents of the
+ * workspace need no initialisation.
  *
  * Weights: wbits = 16: w is bf16 [N, K] (out, in). wbits = 4: affine 4-bit weights in groups of 64
  * along K (dflash2.ts quantizedWeight: quantize(w, 64, bits), mode "affine"): w is [N, K/8] uint32,
