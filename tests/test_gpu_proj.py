@@ -48,9 +48,11 @@ def _conv_case(seed, B, G, H, gs):
 
 
 # 1024 x 1024 x 5120 and 2048 x 256 x 4096: stream-K shares over CTA pairs (256-row tiles, pieces
-# that straddle tiles and hand their partial sums to the tile's owner)
+# that straddle tiles and hand their partial sums to the tile's owner); 600 x 512 x 4096: the last
+# pair tile has 88 rows, so its second CTA holds no row at all; 1000 x 320 x 2536: a ragged column
+# tile (N % 256 = 232) and a ragged row tile under stream-K
 @pytest.mark.parametrize("M,K,N", [(16, 256, 256), (300, 512, 264), (1024, 5120, 512), (129, 128, 1000),
-                                   (2048, 256, 4096), (1024, 1024, 5120)])
+                                   (2048, 256, 4096), (1024, 1024, 5120), (600, 512, 4096), (1000, 320, 2536)])
 def test_proj_bf16(torch, M, K, N):
     import dflash2_block_drafter_gb300 as d
     a = I.normal(M, "a", (M, K), 1.0)
@@ -89,9 +91,9 @@ def test_proj_w4_exact_codes_equal_the_bf16_weight(torch, M, K, N, same_plan):
             assert np.all(np.abs(y.float().cpu().numpy().astype(np.float64) - ref) <= bound)
 
 
-def test_proj_w4_parity(torch):
+@pytest.mark.parametrize("M,K,N", [(200, 1024, 384), (1000, 512, 4864)])  # split K; stream-K shares on single CTAs
+def test_proj_w4_parity(torch, M, K, N):
     import dflash2_block_drafter_gb300 as d
-    M, K, N = 200, 1024, 384
     q = I.affine4_weight(7, "w4", N, K)
     a = I.normal(7, "a", (M, K), 1.0)
     y = d.dflash2_proj(_dev(a), _u32(q.packed), w_scales=_gm(q.scales), w_biases=_gm(q.biases))
@@ -104,8 +106,10 @@ def test_proj_w4_parity(torch):
     assert np.all(np.abs(got - ref) <= _bound(I.to_f64(a), W) + 2.0 ** -9 * np.abs(I.to_f64(a)) @ np.abs(W).T)
 
 
+# (60, 16, 512, 16, 5120): stream-K shares on single CTAs with a ragged row tile and K split between
+# CTAs, where the plain projection runs in CTA pairs that split K elsewhere
 @pytest.mark.parametrize("B,G,H,gs,N", [(2, 16, 256, 16, 256), (9, 16, 5120, 16, 512), (5, 8, 512, 16, 136),
-                                        (64, 16, 1024, 16, 4864)])
+                                        (64, 16, 1024, 16, 4864), (60, 16, 512, 16, 4864), (60, 16, 512, 16, 5120)])
 def test_proj_conv_in(torch, B, G, H, gs, N):
     import dflash2_block_drafter_gb300 as d
     n, D, base = _conv_case(B * G, B, G, H, gs)
@@ -118,10 +122,19 @@ def test_proj_conv_in(torch, B, G, H, gs, N):
     rel = assert_close_scaled(y.float().cpu().numpy(), ref, what="conv side 0 + projection")
     record(f"proj conv-in B={B} G={G} H={H} N={N}", max_rel_err=f"{rel:.2e}")
     # identity coefficients: the fused operand is n itself, so the result is the plain GEMM's exactly
+    # where both split K at the same k-blocks (every case but the last, where the plain projection's
+    # CTA pairs split it elsewhere: there both hold the fp32-accumulation bound of the exact product)
     ident = np.zeros((2, 2, H), np.float32)
     ident[0, 0] = 1.0
     y_id = d.dflash2_proj_conv_in(_dev(n), _dev(np.zeros_like(d0)), _dev(ident), G, gs, _dev(W))
-    assert torch.equal(y_id, d.dflash2_proj(_dev(n), _dev(W)))
+    y_plain = d.dflash2_proj(_dev(n), _dev(W))
+    if N != 5120:
+        assert torch.equal(y_id, y_plain)
+    else:
+        exact = O.projection(I.to_f64(n), I.to_f64(W))
+        bound = _bound(I.to_f64(n), I.to_f64(W))
+        for yy in (y_id, y_plain):
+            assert np.all(np.abs(yy.float().cpu().numpy().astype(np.float64) - exact) <= bound)
 
 
 @pytest.mark.parametrize("B,G,K,H,gs,res", [(2, 16, 256, 256, 16, True), (9, 16, 512, 5120, 16, True),
