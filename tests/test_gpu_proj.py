@@ -259,3 +259,40 @@ def test_proj_small_rows_bf16_and_w4(torch, M, K, N):
     ye = d.dflash2_proj(_dev(a), _u32(qe.packed), w_scales=_gm(qe.scales), w_biases=_gm(qe.biases))
     assert torch.equal(ye, d.dflash2_proj(_dev(a), _dev(We)))
     assert d.dflash2_poll_error() == 0
+
+
+def test_stream_k_hand_off_repeats_in_a_graph(torch):
+    """Stream-K shares hand partial tiles to the tile owners through flags that the owners reset:
+    the same projections launched back to back and replayed from a CUDA graph give the same bits
+    every time (the plain projection on CTA pairs and the 4-bit one on single CTAs)."""
+    import dflash2_block_drafter_gb300 as d
+    M, K, N = 1000, 512, 4096
+    a = _dev(I.normal(11, "a", (M, K), 1.0))
+    W = _dev(I.normal(11, "W", (N, K), K ** -0.5))
+    q = I.affine4_weight(11, "w4", N, K)
+    codes, sc, bi = _u32(q.packed), _gm(q.scales), _gm(q.biases)
+    out16 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    out4 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(d.library().dflash2_proj_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    d.dflash2_proj(a, W, out=out16, workspace=ws)
+    d.dflash2_proj(a, codes, w_scales=sc, w_biases=bi, out=out4, workspace=ws)
+    torch.cuda.synchronize()
+    assert d.dflash2_poll_error() == 0
+    ref16, ref4 = out16.clone(), out4.clone()
+    for _ in range(3):
+        d.dflash2_proj(a, W, out=out16, workspace=ws)
+        d.dflash2_proj(a, codes, w_scales=sc, w_biases=bi, out=out4, workspace=ws)
+    torch.cuda.synchronize()
+    assert d.dflash2_poll_error() == 0
+    assert torch.equal(out16, ref16) and torch.equal(out4, ref4)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        d.dflash2_proj(a, W, out=out16, workspace=ws)
+        d.dflash2_proj(a, codes, w_scales=sc, w_biases=bi, out=out4, workspace=ws)
+    for _ in range(3):
+        out16.zero_()
+        out4.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert d.dflash2_poll_error() == 0
+        assert torch.equal(out16, ref16) and torch.equal(out4, ref4)
