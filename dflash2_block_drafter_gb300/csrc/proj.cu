@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -828,9 +829,17 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-// CTA pairs of the projection kernel variant that the current device holds at once (0: unknown).
+// CTA pairs of the projection kernel variant that the current device holds at once (0: unknown),
+// cached per device.
 template <typename K>
 int proj_pair_capacity(K* kern, int threads, int smem) {
+  constexpr int kMaxDev = 64;
+  static int cached[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] != 0) return cached[dev] > 0 ? cached[dev] : 0;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -845,7 +854,8 @@ int proj_pair_capacity(K* kern, int threads, int smem) {
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
   (void)cudaGetLastError();
-  return n;
+  cached[dev] = n > 0 ? n : -1;
+  return n > 0 ? n : 0;
 }
 
 template <int AM, int BM, int EM, int NT, int P>
@@ -914,8 +924,7 @@ static int launch_proj_t(const ProjSpec& p, int k_splits, int sk_ctas, cudaStrea
   cudaLaunchAttribute cl[1];
   if (P) {
     // every pair of the stream-K shares is resident at once (an owner waits for later pairs)
-    static int cap = -1;
-    if (cap < 0) cap = proj_pair_capacity(kern, C::kThreads, C::kSmem);
+    const int cap = proj_pair_capacity(kern, C::kThreads, C::kSmem);
     if (cap > 0) grid = std::min(grid, 2 * cap);
     grid &= ~1;
     cl[0].id = cudaLaunchAttributeClusterDimension;
