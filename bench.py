@@ -264,9 +264,11 @@ def make_call_timer(d, stream, flush, iters=10):
 def bandwidth_sweep(kind, iters=10):
     """Achieved bandwidth of one library call as the batch grows: the edge scores + walk at
     B = 64 .. 4096 blocks (uniform random candidates over the full vocabulary, so the gathered
-    codebook rows come from HBM after the L2 flush), or a prepare / finish pair of the conv at
-    B = 64 .. 512. Seeded synthetic device inputs; every timed call follows a 256 MB L2 flush;
-    CUDA events on the stream around the call, median over `iters`."""
+    codebook rows come from HBM after the L2 flush), a prepare / finish pair of the conv at
+    B = 64 .. 512, the stand-in projections (fused and unfused, bf16 and 4-bit) at 1, 8 and 64
+    blocks, or the head over a draft vocabulary against the full head at 1 and 64 blocks. Seeded
+    synthetic device inputs; every timed call follows a 256 MB L2 flush; CUDA events on the stream
+    around the call, median over `iters`."""
     import torch
     import dflash2_block_drafter_gb300 as d
     torch.cuda.set_device(0)
@@ -314,10 +316,45 @@ def bandwidth_sweep(kind, iters=10):
                            "finish_frac_hbm": bf / (ms_f / 1e3) / 1e9 / pk["hbm_gbs"]})
     elif kind == "proj":
         points = proj_sweep(d, gen, dev, time_call, pk)
+    elif kind == "vocab":
+        points = vocab_sweep(d, gen, dev, time_call, pk)
     print(json.dumps({"sweep": kind, "peak_hbm_gbs": pk["hbm_gbs"], "peak_source": pk["source"],
                       "timing": "median of CUDA-event times of single calls, 256 MB L2 flush before each",
                       "points": points}), flush=True)
     return 0
+
+
+def vocab_sweep(d, gen, dev, time_call, pk, H=5120, V=248320, n_listed=32768, K=16, R=64, steps=15):
+    """The head over a draft vocabulary (dflash2_head_topk_vocab: the GEMM over the listed rows
+    only, column -> token id in the merge) against the full head on the same rows, at 1 and 64
+    blocks of 15 rows: seeded device inputs, the listed rows gathered from the full head once
+    (as a caller does at load time), ascending ids. The draft vocabulary's size is not fixed by
+    the method; 32768 ids stand in for it."""
+    import torch
+    w_head = (torch.randn(V, H, generator=gen, device=dev) / H ** 0.5).to(torch.bfloat16)
+    w_proj = (torch.randn(R, H, generator=gen, device=dev) / H ** 0.5).to(torch.bfloat16)
+    ids = torch.sort(torch.randperm(V, generator=gen, device=dev)[:n_listed]).values.to(torch.int32)
+    w_listed = w_head.index_select(0, ids.long()).contiguous()
+    points = []
+    for B in (1, 64):
+        M = B * steps
+        h = torch.randn(M, H, generator=gen, device=dev).to(torch.bfloat16)
+        cand = torch.empty(M, K, dtype=torch.int32, device=dev)
+        unary = torch.empty(M, K, dtype=torch.float32, device=dev)
+        z = torch.empty(M, R, dtype=torch.float32, device=dev)
+        ws = torch.empty(max(256, d.dflash2_head_topk_workspace_bytes(M, H, V, K, R)), dtype=torch.uint8, device=dev)
+        ms_l = time_call(lambda: d.dflash2_head_topk_vocab(h, w_listed, ids, K, w_proj=w_proj, cand=cand, unary=unary,
+                                                           z=z, workspace=ws))
+        ms_f = time_call(lambda: d.dflash2_head_topk(h, w_head, K, w_proj=w_proj, cand=cand, unary=unary, z=z,
+                                                     workspace=ws))
+        pt = {"B": B, "rows": M, "V_listed": n_listed, "V": V}
+        for tag, ms, vv in (("listed", ms_l, n_listed), ("full", ms_f, V)):
+            fl = head_flops(M, vv, R, H) / (ms / 1e3) / 1e12
+            wb = 2.0 * (vv + R) * H / (ms / 1e3) / 1e9
+            pt[tag] = {"ms": ms, "tflops": fl, "frac_burst_bf16": fl / pk["bf16_tflops"], "weight_stream_gbs": wb,
+                       "frac_hbm": head_bytes(M, vv, R, H, K) / (ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+        points.append(pt)
+    return points
 
 
 def proj_sweep(d, gen, dev, time_call, pk, G=16, H=5120, gs=16, N=5120):
@@ -843,7 +880,7 @@ def main():
     ap.add_argument("--graph", dest="graph", action="store_true", default=True,
                     help="replay each part of a timed step as a CUDA graph (default)")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
-    ap.add_argument("--sweep", choices=["edges", "conv", "proj"], default=None,
+    ap.add_argument("--sweep", choices=["edges", "conv", "proj", "vocab"], default=None,
                     help="instead of the step benchmark: one call's bandwidth as the batch grows")
     args = ap.parse_args()
     if args.sweep is not None:
