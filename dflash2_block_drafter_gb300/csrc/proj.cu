@@ -971,11 +971,59 @@ ProjPlan proj_plan(int M, int N, int K, int sms, bool epilogue_conv, bool produc
   return ProjPlan{64, 1, 0, 0};
 }
 
+// Above this many rows a 4-bit weight is dequantised once into the workspace and the projection
+// runs on bf16 weights: each weight tile is otherwise dequantised again by every 128-row tile that
+// reads it (8 times at 1024 rows), in shared memory the MMA operands also need.
+constexpr int kW4OnceRows = 384;
+
+static size_t proj_w4_scratch_offset(int M, int N, int K, int sms) {
+  const ProjPlan pl = proj_plan(M, N, K, sms, false, false);  // the largest workspace of the variants
+  size_t b = 0;
+  if (pl.ctas > 0)
+    b = static_cast<size_t>(pl.ctas) * kPM * 256 * sizeof(float);  // one partial tile per CTA
+  else if (pl.k_splits > 1)
+    b = static_cast<size_t>(pl.k_splits) * M * N * sizeof(float);
+  return (b + 255) & ~static_cast<size_t>(255);
+}
+
 size_t proj_workspace(int M, int N, int K, int sms) {
   if (proj_small_eligible(M, N, K)) return 0;  // the small-row kernel reduces in shared memory
-  const ProjPlan pl = proj_plan(M, N, K, sms, false, false);  // the largest workspace of the variants
-  if (pl.ctas > 0) return static_cast<size_t>(pl.ctas) * kPM * 256 * sizeof(float);  // one partial tile per CTA
-  return pl.k_splits > 1 ? static_cast<size_t>(pl.k_splits) * M * N * sizeof(float) : 0;
+  const size_t off = proj_w4_scratch_offset(M, N, K, sms);
+  // (the query does not know the weight format: the bf16 scratch of a 4-bit weight is counted too)
+  return M > kW4OnceRows ? off + static_cast<size_t>(N) * K * 2 : off;
+}
+
+// W[n, k] = scale[k / 64][n] * q + bias[k / 64][n] as bf16, the same arithmetic as the dequant
+// producer warps (0x4300 | q is 128 + q exactly, minus 128, one bf16 FMA). Thread = one 32-bit word
+// (8 codes) of one row: reads 4 bytes of codes and writes 16 bytes of W.
+static __global__ void __launch_bounds__(256) w4_dequant_kernel(const uint32_t* __restrict__ codes,
+                                                         const __nv_bfloat16* __restrict__ scales,
+                                                         const __nv_bfloat16* __restrict__ biases, int N, int K,
+                                                         __nv_bfloat16* __restrict__ W) {
+  pdl_trigger();
+  pdl_wait();
+  const int wpr = K / 8;  // words per row
+  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<size_t>(N) * wpr) return;
+  const int n = static_cast<int>(idx / wpr);
+  const int w = static_cast<int>(idx - static_cast<size_t>(n) * wpr);
+  const int g = w >> 3;  // 64 codes per group: 8 words
+  const uint32_t word = __ldg(codes + idx);
+  const __nv_bfloat16 sc = scales[static_cast<size_t>(g) * N + n];
+  const __nv_bfloat16 bi = biases[static_cast<size_t>(g) * N + n];
+  const __nv_bfloat162 s2 = __halves2bfloat162(sc, sc);
+  const __nv_bfloat162 b2 = __halves2bfloat162(bi, bi);
+  const __nv_bfloat162 k128 = __floats2bfloat162_rn(128.f, 128.f);
+  uint32_t o[4];
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const uint32_t pair = 0x43004300u | ((word >> (8 * jj)) & 0xFu) | (((word >> (8 * jj + 4)) & 0xFu) << 16);
+    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pair);
+    v = __hsub2(v, k128);    // exact: q
+    v = __hfma2(s2, v, b2);  // scale * q + bias, one rounding
+    o[jj] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  *reinterpret_cast<uint4*>(W + static_cast<size_t>(n) * K + 8 * w) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 template <int AM, int BM, int EM>
@@ -987,8 +1035,24 @@ static int launch_proj_nt(const ProjSpec& p, cudaStream_t st) {
   return launch_proj_t<AM, BM, EM, 256, 0>(p, pl.k_splits, pl.ctas, st);
 }
 
-int launch_proj(const ProjSpec& p, cudaStream_t st) {
-  if (proj_small_eligible(p.M, p.N, p.K)) return launch_proj_small(p, st);
+int launch_proj(const ProjSpec& p_in, cudaStream_t st) {
+  if (proj_small_eligible(p_in.M, p_in.N, p_in.K)) return launch_proj_small(p_in, st);
+  ProjSpec p = p_in;
+  if (p.wbits == 4 && p.M > kW4OnceRows) {
+    // dequantise once into the workspace (after the partial-sum slots), then a bf16 projection
+    if (p.part == nullptr) return fail(DFLASH2_ERR_WORKSPACE, "the 4-bit projection at %d rows needs a workspace", p.M);
+    __nv_bfloat16* W = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(p.part) +
+                                                         proj_w4_scratch_offset(p.M, p.N, p.K, sm_count()));
+    const size_t words = static_cast<size_t>(p.N) * (p.K / 8);
+    const cudaError_t e = launch_pdl(w4_dequant_kernel, dim3(static_cast<unsigned>((words + 255) / 256)), dim3(256), 0,
+                                     st, nullptr, 0, static_cast<const uint32_t*>(p.w),
+                                     static_cast<const __nv_bfloat16*>(p.scales),
+                                     static_cast<const __nv_bfloat16*>(p.qbias), p.N, p.K, W);
+    if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "4-bit dequant launch failed: %s", cudaGetErrorString(e));
+    p.w = W;
+    p.wbits = 16;
+    p.scales = p.qbias = nullptr;
+  }
   const bool am = p.d0 != nullptr, bm = p.wbits == 4, em = p.coef1 != nullptr;
   if (am && bm && em) return launch_proj_nt<1, 1, 1>(p, st);
   if (am && bm) return launch_proj_nt<1, 1, 0>(p, st);

@@ -307,8 +307,10 @@ DFLASH2_API int dflash2_score_edges_ragged(const int32_t* cand, const float* una
  * equal stream-K share of the tiles' k-blocks and the workspace holds one 128 x 256 fp32 partial
  * tile per CTA, handed to the tile's owner through a flag array inside the library). The flags are
  * per device and process: calls of these three entry points that can run at the same time on one
- * device (on different streams) must not overlap; keep them on one stream. The contents of the
- * workspace need no initialisation.
+ * device (on different streams) must not overlap; keep them on one stream. Above 384 rows a 4-bit
+ * weight is dequantised once into the workspace (N x K bf16, after the partial tiles) and the
+ * projection runs on that copy, so the query (which does not know the weight format) counts those
+ * bytes from 385 rows on. The contents of the workspace need no initialisation.
  *
  * Weights: wbits = 16: w is bf16 [N, K] (out, in). wbits = 4: affine 4-bit weights in groups of 64
  * along K (dflash2.ts quantizedWeight: quantize(w, 64, bits), mode "affine"): w is [N, K/8] uint32,

@@ -65,11 +65,13 @@ def test_proj_bf16(torch, M, K, N):
     assert np.all(np.abs(got - ref) <= _bound(I.to_f64(a), I.to_f64(W))), "outside the fp32-accumulation bound"
 
 
-@pytest.mark.parametrize("M,K,N,same_plan", [(48, 256, 128, True), (272, 5120, 520, True), (1024, 512, 5120, False)])
+# 1024 rows: the 4-bit weight is dequantised once into the workspace and the bf16 path runs on it
+@pytest.mark.parametrize("M,K,N,same_plan", [(48, 256, 128, True), (272, 5120, 520, True), (1024, 512, 5120, True),
+                                             (320, 512, 6656, False)])
 def test_proj_w4_exact_codes_equal_the_bf16_weight(torch, M, K, N, same_plan):
     """4-bit weights whose scale * q + bias are bf16 values: the dequantised operand is exact, so the
     W4 GEMM equals the bf16 GEMM on that weight bit for bit where both run the same tiles and K
-    splits (same accumulation order). At 1024 rows the bf16 weight runs in CTA pairs and the 4-bit
+    splits (same accumulation order). At 320 rows the bf16 weight runs in CTA pairs and the 4-bit
     one on single CTAs, whose stream-K shares split K at other k-blocks: there both hold the
     fp32-accumulation bound against the exact product instead."""
     import dflash2_block_drafter_gb300 as d
@@ -208,9 +210,10 @@ def test_fused_site_equals_the_unfused_sequence(torch):
                         what="site output")
 
 
-def test_proj_w4_with_both_conv_fusions(torch):
+@pytest.mark.parametrize("B", [4, 40])  # 64 rows, and 640 rows (the weight dequantised once first)
+def test_proj_w4_with_both_conv_fusions(torch, B):
     import dflash2_block_drafter_gb300 as d
-    B, G, H, gs, N = 4, 16, 512, 16, 256
+    G, H, gs, N = 16, 512, 16, 256
     M = B * G
     n, D, base = _conv_case(5, B, G, H, gs)
     q_in = I.affine4_weight(5, "w_in", N, H)
