@@ -141,7 +141,7 @@ bool make_tmap_sw128_3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t
 
 // ---------------------------------------------------------------- sublayer projections (proj.cu)
 // out[M, N] = A[M, K] W[N, K]^T (bf16 in and out, fp32 accumulation), with optional fusions:
-//   d0 (non-null): A = Conv_0(a) with side-0 deltas d0 [M][2][groups] fp32 and base [2][2][K];
+//   d0 (non-null): A = Conv_0(a) with side-0 deltas d0 [2 taps][groups][M] fp32 and base [2][2][K];
 //   coef1 (non-null): out = residual + Conv_1(A W^T) with side-1 deltas coef1 [M][2][groups] bf16 and
 //                     base [2][2][N] (residual may be null);
 //   wbits = 4: w is packed affine 4-bit [N][K / 8] 32-bit words (value k at bits 4 (k % 8) of word

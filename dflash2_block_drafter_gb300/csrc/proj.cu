@@ -973,8 +973,11 @@ ProjPlan proj_plan(int M, int N, int K, int sms, bool epilogue_conv, bool produc
 
 // Above this many rows a 4-bit weight is dequantised once into the workspace and the projection
 // runs on bf16 weights: each weight tile is otherwise dequantised again by every 128-row tile that
-// reads it (8 times at 1024 rows), in shared memory the MMA operands also need.
+// reads it (8 times at 1024 rows), in shared memory the MMA operands also need. Likewise side 0 of
+// the conv is applied once to the rows (into the workspace) instead of by every column tile's
+// producer warps (20 times at N = 5120).
 constexpr int kW4OnceRows = 384;
+constexpr int kConvOnceRows = 384;
 
 static size_t proj_w4_scratch_offset(int M, int N, int K, int sms) {
   const ProjPlan pl = proj_plan(M, N, K, sms, false, false);  // the largest workspace of the variants
@@ -986,11 +989,45 @@ static size_t proj_w4_scratch_offset(int M, int N, int K, int sms) {
   return (b + 255) & ~static_cast<size_t>(255);
 }
 
+// Workspace: [partial-sum slots][bf16 copy of a 4-bit weight (M > kW4OnceRows)][conv side 0 of
+// the rows (M > kConvOnceRows)]; the query knows neither the weight format nor the fusion, so it
+// counts every part the shape can use.
+static size_t proj_conv_scratch_offset(int M, int N, int K, int sms) {
+  size_t b = proj_w4_scratch_offset(M, N, K, sms);
+  if (M > kW4OnceRows) b += static_cast<size_t>(N) * K * 2;
+  return (b + 255) & ~static_cast<size_t>(255);
+}
+
 size_t proj_workspace(int M, int N, int K, int sms) {
   if (proj_small_eligible(M, N, K)) return 0;  // the small-row kernel reduces in shared memory
-  const size_t off = proj_w4_scratch_offset(M, N, K, sms);
-  // (the query does not know the weight format: the bf16 scratch of a 4-bit weight is counted too)
-  return M > kW4OnceRows ? off + static_cast<size_t>(N) * K * 2 : off;
+  const size_t off = proj_conv_scratch_offset(M, N, K, sms);
+  return M > kConvOnceRows ? off + static_cast<size_t>(M) * K * 2 : off;
+}
+
+// A[m, c] = (base[0][0][c] + d0[0][g][m]) n[m, c] + (base[0][1][c] + d0[1][g][m]) n[m - 1, c] with
+// n[m - 1] = 0 at a block's first row (m % G == 0) and g = c / gs: the arithmetic of the conv
+// producer warps, rounded once to bf16. Thread = 8 channels of one row.
+static __global__ void __launch_bounds__(256) conv0_rows_kernel(const __nv_bfloat16* __restrict__ n,
+                                                                const float* __restrict__ d0,
+                                                                const float* __restrict__ base, int M, int K, int G,
+                                                                int gs, int groups, __nv_bfloat16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int vpr = K / 8;
+  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<size_t>(M) * vpr) return;
+  const int m = static_cast<int>(idx / vpr);
+  const int c = static_cast<int>(idx - static_cast<size_t>(m) * vpr) * 8;
+  const int g = c / gs;
+  float cur[8], prv[8] = {};
+  bf16x8_to_f32(*reinterpret_cast<const uint4*>(n + static_cast<size_t>(m) * K + c), cur);
+  if (m % G != 0) bf16x8_to_f32(*reinterpret_cast<const uint4*>(n + static_cast<size_t>(m - 1) * K + c), prv);
+  const float dd0 = d0[static_cast<size_t>(g) * M + m];
+  const float dd1 = d0[(static_cast<size_t>(groups) + g) * M + m];
+  float o[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = fmaf(base[c + e] + dd0, cur[e], (base[K + c + e] + dd1) * prv[e]);
+  *reinterpret_cast<uint4*>(out + static_cast<size_t>(m) * K + c) = f32x8_to_bf16(o);
 }
 
 // W[n, k] = scale[k / 64][n] * q + bias[k / 64][n] as bf16, the same arithmetic as the dequant
@@ -1052,6 +1089,19 @@ int launch_proj(const ProjSpec& p_in, cudaStream_t st) {
     p.w = W;
     p.wbits = 16;
     p.scales = p.qbias = nullptr;
+  }
+  if (p.d0 != nullptr && p.M > kConvOnceRows) {
+    // side 0 applied once to the rows (into the workspace), then the projection of those rows
+    if (p.part == nullptr) return fail(DFLASH2_ERR_WORKSPACE, "the fused projection at %d rows needs a workspace", p.M);
+    __nv_bfloat16* A = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(p.part) +
+                                                         proj_conv_scratch_offset(p.M, p.N, p.K, sm_count()));
+    const size_t items = static_cast<size_t>(p.M) * (p.K / 8);
+    const cudaError_t e = launch_pdl(conv0_rows_kernel, dim3(static_cast<unsigned>((items + 255) / 256)), dim3(256), 0,
+                                     st, nullptr, 0, static_cast<const __nv_bfloat16*>(p.a), p.d0, p.base, p.M, p.K,
+                                     p.G, p.gs, p.groups, A);
+    if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "conv side-0 launch failed: %s", cudaGetErrorString(e));
+    p.a = A;
+    p.d0 = nullptr;
   }
   const bool am = p.d0 != nullptr, bm = p.wbits == 4, em = p.coef1 != nullptr;
   if (am && bm && em) return launch_proj_nt<1, 1, 1>(p, st);

@@ -226,11 +226,12 @@ def test_projection_workspace_query(lib):
     """Up to 128 rows the projections reduce their K splits in shared memory and need no
     workspace; a few more rows than one 128-row tile split K through the workspace instead, and
     with at least half as many 256-column tiles as SMs the stream-K shares need one 128 x 256 fp32
-    partial tile per CTA; above 384 rows the query also counts the bf16 copy of a 4-bit weight (the
-    query is host-only and needs no device: 148 SMs are assumed)."""
+    partial tile per CTA; above 384 rows the query also counts the bf16 copy of a 4-bit weight and the
+    side-0 conv of the rows (the query is host-only and needs no device: 148 SMs are assumed)."""
     lib.dflash2_proj_workspace_bytes.restype = ctypes.c_size_t
     assert lib.dflash2_proj_workspace_bytes(1, 5120, 5120) == 0
     assert lib.dflash2_proj_workspace_bytes(128, 5120, 5120) == 0
     assert lib.dflash2_proj_workspace_bytes(129, 5120, 5120) == 3 * 129 * 5120 * 4  # 40 tiles: 3 K ranges
-    # 1024 rows: the stream-K slots, then room to dequantise a 4-bit weight once (5120 x 5120 bf16)
-    assert lib.dflash2_proj_workspace_bytes(1024, 5120, 5120) == 148 * 128 * 256 * 4 + 5120 * 5120 * 2
+    # 1024 rows: the stream-K slots, then room to dequantise a 4-bit weight once (5120 x 5120 bf16) and
+    # to apply the conv's side 0 to the rows once (1024 x 5120 bf16)
+    assert lib.dflash2_proj_workspace_bytes(1024, 5120, 5120) == 148 * 128 * 256 * 4 + 5120 * 5120 * 2 + 1024 * 5120 * 2

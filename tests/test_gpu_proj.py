@@ -108,8 +108,7 @@ def test_proj_w4_parity(torch, M, K, N):
     assert np.all(np.abs(got - ref) <= _bound(I.to_f64(a), W) + 2.0 ** -9 * np.abs(I.to_f64(a)) @ np.abs(W).T)
 
 
-# (60, 16, 512, 16, 5120): stream-K shares on single CTAs with a ragged row tile and K split between
-# CTAs, where the plain projection runs in CTA pairs that split K elsewhere
+# 960 and 1024 rows: side 0 applied to the rows once, then the plain projection (CTA pairs, stream-K)
 @pytest.mark.parametrize("B,G,H,gs,N", [(2, 16, 256, 16, 256), (9, 16, 5120, 16, 512), (5, 8, 512, 16, 136),
                                         (64, 16, 1024, 16, 4864), (60, 16, 512, 16, 4864), (60, 16, 512, 16, 5120)])
 def test_proj_conv_in(torch, B, G, H, gs, N):
@@ -124,19 +123,10 @@ def test_proj_conv_in(torch, B, G, H, gs, N):
     rel = assert_close_scaled(y.float().cpu().numpy(), ref, what="conv side 0 + projection")
     record(f"proj conv-in B={B} G={G} H={H} N={N}", max_rel_err=f"{rel:.2e}")
     # identity coefficients: the fused operand is n itself, so the result is the plain GEMM's exactly
-    # where both split K at the same k-blocks (every case but the last, where the plain projection's
-    # CTA pairs split it elsewhere: there both hold the fp32-accumulation bound of the exact product)
     ident = np.zeros((2, 2, H), np.float32)
     ident[0, 0] = 1.0
     y_id = d.dflash2_proj_conv_in(_dev(n), _dev(np.zeros_like(d0)), _dev(ident), G, gs, _dev(W))
-    y_plain = d.dflash2_proj(_dev(n), _dev(W))
-    if N != 5120:
-        assert torch.equal(y_id, y_plain)
-    else:
-        exact = O.projection(I.to_f64(n), I.to_f64(W))
-        bound = _bound(I.to_f64(n), I.to_f64(W))
-        for yy in (y_id, y_plain):
-            assert np.all(np.abs(yy.float().cpu().numpy().astype(np.float64) - exact) <= bound)
+    assert torch.equal(y_id, d.dflash2_proj(_dev(n), _dev(W)))
 
 
 @pytest.mark.parametrize("B,G,K,H,gs,res", [(2, 16, 256, 256, 16, True), (9, 16, 512, 5120, 16, True),
