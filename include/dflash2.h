@@ -309,8 +309,9 @@ DFLASH2_API int dflash2_score_edges_ragged(const int32_t* cand, const float* una
  * per device and process: calls of these three entry points that can run at the same time on one
  * device (on different streams) must not overlap; keep them on one stream. Above 384 rows a 4-bit
  * weight is dequantised once into the workspace (N x K bf16, after the partial tiles) and the
- * projection runs on that copy, so the query (which does not know the weight format) counts those
- * bytes from 385 rows on. The contents of the workspace need no initialisation.
+ * projection runs on that copy, and dflash2_proj_conv_in applies side 0 to the rows once (M x K
+ * bf16, after that) before its projection; the query, which knows neither the weight format nor the
+ * fusion, counts both from 385 rows on. The contents of the workspace need no initialisation.
  *
  * Weights: wbits = 16: w is bf16 [N, K] (out, in). wbits = 4: affine 4-bit weights in groups of 64
  * along K (dflash2.ts quantizedWeight: quantize(w, 64, bits), mode "affine"): w is [N, K/8] uint32,
