@@ -990,8 +990,8 @@ static size_t proj_w4_scratch_offset(int M, int N, int K, int sms) {
 }
 
 // Workspace: [partial-sum slots][bf16 copy of a 4-bit weight (M > kW4OnceRows)][conv side 0 of
-// the rows (M > kConvOnceRows)]; the query knows neither the weight format nor the fusion, so it
-// counts every part the shape can use.
+// the rows, M x K bf16, or the projection before side 1, M x N bf16 (M > kConvOnceRows)]; the
+// query knows neither the weight format nor the fusion, so it counts every part the shape can use.
 static size_t proj_conv_scratch_offset(int M, int N, int K, int sms) {
   size_t b = proj_w4_scratch_offset(M, N, K, sms);
   if (M > kW4OnceRows) b += static_cast<size_t>(N) * K * 2;
@@ -1001,7 +1001,7 @@ static size_t proj_conv_scratch_offset(int M, int N, int K, int sms) {
 size_t proj_workspace(int M, int N, int K, int sms) {
   if (proj_small_eligible(M, N, K)) return 0;  // the small-row kernel reduces in shared memory
   const size_t off = proj_conv_scratch_offset(M, N, K, sms);
-  return M > kConvOnceRows ? off + static_cast<size_t>(M) * K * 2 : off;
+  return M > kConvOnceRows ? off + static_cast<size_t>(M) * std::max(K, N) * 2 : off;
 }
 
 // A[m, c] = (base[0][0][c] + d0[0][g][m]) n[m, c] + (base[0][1][c] + d0[1][g][m]) n[m - 1, c] with
@@ -1102,6 +1102,19 @@ int launch_proj(const ProjSpec& p_in, cudaStream_t st) {
     if (e != cudaSuccess) return fail(DFLASH2_ERR_CUDA, "conv side-0 launch failed: %s", cudaGetErrorString(e));
     p.a = A;
     p.d0 = nullptr;
+  }
+  if (p.coef1 != nullptr && p.M > kConvOnceRows) {
+    // the projection into the workspace, then side 1 + residual as the finish pass applies them:
+    // the conv epilogue on whole persistent tiles exposes its loads after the last tile round
+    if (p.part == nullptr) return fail(DFLASH2_ERR_WORKSPACE, "the fused projection at %d rows needs a workspace", p.M);
+    ProjSpec q = p;
+    q.coef1 = nullptr;
+    q.residual = nullptr;
+    q.out = reinterpret_cast<uint8_t*>(p.part) + proj_conv_scratch_offset(p.M, p.N, p.K, sm_count());
+    const int rc = q.wbits == 4 ? launch_proj_nt<0, 1, 0>(q, st) : launch_proj_nt<0, 0, 0>(q, st);
+    if (rc != DFLASH2_OK) return rc;
+    const ConvShape s{p.M / p.G, p.G, p.N, p.gs, p.N / p.gs, DFLASH2_BF16};
+    return launch_conv_side1(s, q.out, p.coef1, p.base, p.residual, p.out, nullptr, 0.f, nullptr, 0, st);
   }
   const bool am = p.d0 != nullptr, bm = p.wbits == 4, em = p.coef1 != nullptr;
   if (am && bm && em) return launch_proj_nt<1, 1, 1>(p, st);

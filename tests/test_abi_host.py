@@ -233,5 +233,5 @@ def test_projection_workspace_query(lib):
     assert lib.dflash2_proj_workspace_bytes(128, 5120, 5120) == 0
     assert lib.dflash2_proj_workspace_bytes(129, 5120, 5120) == 3 * 129 * 5120 * 4  # 40 tiles: 3 K ranges
     # 1024 rows: the stream-K slots, then room to dequantise a 4-bit weight once (5120 x 5120 bf16) and
-    # to apply the conv's side 0 to the rows once (1024 x 5120 bf16)
+    # for the rows' side-0 conv or the projection before side 1 (1024 x 5120 bf16)
     assert lib.dflash2_proj_workspace_bytes(1024, 5120, 5120) == 148 * 128 * 256 * 4 + 5120 * 5120 * 2 + 1024 * 5120 * 2

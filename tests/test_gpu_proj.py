@@ -129,8 +129,10 @@ def test_proj_conv_in(torch, B, G, H, gs, N):
     assert torch.equal(y_id, d.dflash2_proj(_dev(n), _dev(W)))
 
 
+# 1024 and 640 rows: the projection into the workspace, then the finish pass applies side 1 (+ residual)
 @pytest.mark.parametrize("B,G,K,H,gs,res", [(2, 16, 256, 256, 16, True), (9, 16, 512, 5120, 16, True),
-                                            (12, 8, 128, 96, 8, False), (64, 16, 256, 5120, 16, True)])
+                                            (12, 8, 128, 96, 8, False), (64, 16, 256, 5120, 16, True),
+                                            (40, 16, 512, 1056, 32, False)])
 def test_proj_conv_out(torch, B, G, K, H, gs, res):
     import dflash2_block_drafter_gb300 as d
     M = B * G
